@@ -1,0 +1,160 @@
+"""CPU oracle for the Q8_0 W8A16 decode matmul -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It wraps ``q8ref.c`` (plain C, binary64
+arithmetic, no code shared with the CUDA library) through ctypes, and builds it
+with gcc on first use.
+
+Functions and what they follow (page titles of the source pages):
+
+* ``quantize_rows`` -- "MODEL-BASELINE-RESULTS" (fak), ACT 3 item 1 (32-wide
+  blocks, d = maxabs/127, int8 codes, ~1.06 B/weight -> binary16 scale) and
+  ACT 4 "Correctness" (round half away from zero, 0.49999997 -> 0).
+* ``matmul`` -- "Frigg" README, Finding 8 (W8A16: int8 weights x bf16
+  activations); dequantise-then-dot in binary64, plus the tolerance bound
+  B = sum |w' x|.
+* ``f32_to_f16`` / ``f16_to_f64`` / ``code`` -- the binary16 rounding and the
+  single-weight code rule, exposed for exhaustive pins.
+
+Every function is pinned by the CPU test suite (see tests/test_oracle_*.py);
+none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8ref.c")
+_LIB = os.path.join(_HERE, "libq8ref.so")
+_lock = threading.Lock()
+_lib = None
+
+FLAG_NONFINITE = 1
+FLAG_SCALE_OVF = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile q8ref.c with gcc (no fast-math, no FP contraction)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".tmp{os.getpid()}"
+            subprocess.check_call([
+                "gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        lib.q8ref_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.q8ref_f32_to_f16.restype = ctypes.c_uint16
+        lib.q8ref_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.q8ref_f16_to_f64.restype = ctypes.c_double
+        lib.q8ref_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.q8ref_bf16_to_f64.restype = ctypes.c_double
+        lib.q8ref_quantize_rows.argtypes = [P, I64, I64, P, P, P]
+        lib.q8ref_quantize_rows.restype = ctypes.c_uint32
+        lib.q8ref_matmul.argtypes = [P, P, I64, I64, P, I64, I64, I64, I64, P, P, I64]
+        lib.q8ref_matmul.restype = None
+        lib.q8ref_f32_to_f16_array.argtypes = [P, P, I64]
+        lib.q8ref_f16_to_f64_array.argtypes = [P, P, I64]
+        lib.q8ref_code_array.argtypes = [P, I64, ctypes.c_uint16, P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """binary32 -> binary16 bits (uint16), round to nearest even."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().q8ref_f32_to_f16_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def f16_to_f64(h) -> np.ndarray:
+    a = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(a.shape, dtype=np.float64)
+    _load().q8ref_f16_to_f64_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def code(w, s_bits: int) -> np.ndarray:
+    """Codes of the weights ``w`` against one stored binary16 scale."""
+    a = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.int8)
+    _load().q8ref_code_array(_ptr(a), a.size, ctypes.c_uint16(int(s_bits)), _ptr(out))
+    return out
+
+
+def quantize_rows(w: np.ndarray, with_flags: bool = False):
+    """Q8_0-quantize a [rows][K] binary32 matrix along K.
+
+    Returns (q int8 [rows][K], s uint16 binary16 bits [rows][K/32], flags) where
+    flags is the OR of all block flags, or the per-block array if
+    ``with_flags``.
+    """
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    if w.ndim != 2 or w.shape[1] % 32:
+        raise ValueError("w must be [rows][K] with K a multiple of 32")
+    rows, K = w.shape
+    q = np.empty((rows, K), dtype=np.int8)
+    s = np.empty((rows, K // 32), dtype=np.uint16)
+    fl = np.empty((rows, K // 32), dtype=np.uint32)
+    allf = _load().q8ref_quantize_rows(_ptr(w), rows, K, _ptr(q), _ptr(s), _ptr(fl))
+    return q, s, (fl if with_flags else int(allf))
+
+
+def matmul(q: np.ndarray, s: np.ndarray, x_bf16: np.ndarray, rows=None, threads: int = 1):
+    """Binary64 reference y[m][n] and bound B[m][n] for output rows ``rows``.
+
+    ``rows`` is None (all N rows) or an increasing array of row indices; the
+    result then has one column per listed row.  ``threads`` > 1 splits the rows
+    over host threads; every output is computed by one call in the same order,
+    so the bits do not depend on the thread count.
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    N, K = q.shape
+    M = x.shape[0]
+    if s.shape != (N, K // 32) or x.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if rows is None:
+        y = np.empty((M, N), dtype=np.float64)
+        B = np.empty((M, N), dtype=np.float64)
+        chunks = np.array_split(np.arange(N), max(1, threads))
+
+        def run(c):
+            if len(c):
+                lib.q8ref_matmul(_ptr(q), _ptr(s), N, K, _ptr(x), K, M,
+                                 int(c[0]), int(c[-1]) + 1, _ptr(y), _ptr(B), N)
+
+        if threads > 1:
+            with ThreadPoolExecutor(threads) as ex:
+                list(ex.map(run, chunks))
+        else:
+            run(np.arange(N))
+        return y, B
+    rows = np.asarray(rows, dtype=np.int64)
+    qs = np.ascontiguousarray(q[rows])
+    ss = np.ascontiguousarray(s[rows])
+    return matmul(qs, ss, x, None, threads)
