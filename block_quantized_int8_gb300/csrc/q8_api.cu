@@ -1,0 +1,177 @@
+// q8_api.cu -- the C ABI of libq8: argument checks (host only, before any
+// CUDA call), device checks, and dispatch to the kernels.
+#include <mutex>
+
+#include "q8_internal.h"
+
+namespace q8 {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+int g_ok[kMaxDevices];
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+}  // namespace
+
+const DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(g_once[dev], [dev]() {
+        DeviceInfo &d = g_info[dev];
+        d.device = dev;
+        g_ok[dev] = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess;
+    });
+    return g_ok[dev] ? &g_info[dev] : nullptr;
+}
+
+static q8_status check_arch(const DeviceInfo **out) {
+    const DeviceInfo *di = device_info();
+    if (!di) return Q8_ERR_CUDA;
+    if (di->cc_major != 10 || di->cc_minor != 3) return Q8_ERR_ARCH;
+    *out = di;
+    return Q8_OK;
+}
+
+static q8_status check_weights(const int8_t *q, const uint16_t *s, int64_t N, int64_t K) {
+    if (N < 0 || K <= 0 || (K % 32) != 0 || N > INT32_MAX || K > INT32_MAX) return Q8_ERR_SHAPE;
+    if (N == 0) return Q8_OK;
+    if (!q || !s) return Q8_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(s, 16)) return Q8_ERR_ALIGN;
+    return Q8_OK;
+}
+
+static q8_status check_desc(const q8_linear_desc &d, int32_t M) {
+    q8_status st = check_weights(d.q, d.s, d.N, d.K);
+    if (st != Q8_OK) return st;
+    if (d.N == 0) return Q8_OK;
+    if (!d.x || !d.y) return Q8_ERR_ARG;
+    if (d.ldx < d.K || (M > 1 && d.ldy < d.N) || d.ldy < 1) return Q8_ERR_SHAPE;
+    if (!aligned(d.x, 16) || (d.ldx % 8) != 0 || !aligned(d.y, 4)) return Q8_ERR_ALIGN;
+    return Q8_OK;
+}
+
+}  // namespace q8
+
+using namespace q8;
+
+extern "C" {
+
+int32_t q8_abi_version(void) { return Q8_ABI_VERSION; }
+
+const char *q8_status_str(q8_status st) {
+    switch (st) {
+        case Q8_OK: return "ok";
+        case Q8_ERR_ARG: return "invalid argument (null pointer or bad count)";
+        case Q8_ERR_ALIGN: return "misaligned pointer or leading dimension";
+        case Q8_ERR_SHAPE: return "bad shape (K must be a positive multiple of 32; check M and leading dimensions)";
+        case Q8_ERR_WORKSPACE: return "workspace missing or too small";
+        case Q8_ERR_ARCH: return "current device is not sm_103 (GB300)";
+        case Q8_ERR_CUDA: return "CUDA runtime error";
+        case Q8_ERR_UNSUPPORTED: return "not supported by this build";
+    }
+    return "unknown status";
+}
+
+q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K, int8_t *q, uint16_t *s,
+                           uint32_t *dev_status, q8_stream_t stream) {
+    if (rows < 0 || K <= 0 || (K % 32) != 0) return Q8_ERR_SHAPE;
+    if (rows == 0) return Q8_OK;
+    if (!w || !q || !s) return Q8_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(q, 16) || !aligned(s, 16)) return Q8_ERR_ALIGN;
+    if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
+    const DeviceInfo *di;
+    q8_status st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_quantize(w, rows, K, q, s, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {
+    if (N <= 0 || K <= 0 || (K % 32) != 0 || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
+    q8_linear_desc d{};
+    d.N = N;
+    d.K = K;
+    SplitPlan pl;
+    return plan_skinny(&d, 1, M, &pl);
+}
+
+size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M) {
+    if (!descs || count < 1 || count > Q8_MAX_BATCH || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
+    q8_linear_desc tmp[Q8_MAX_BATCH];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+        if (descs[i].N <= 0 || descs[i].K <= 0 || descs[i].K % 32) continue;
+        tmp[n++] = descs[i];
+    }
+    if (n == 0) return 0;
+    SplitPlan pl[Q8_MAX_BATCH];
+    return plan_skinny(tmp, n, M, pl);
+}
+
+q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant,
+                             void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+    if (!descs || count < 0 || count > Q8_MAX_BATCH) return Q8_ERR_ARG;
+    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_MMA) return Q8_ERR_ARG;
+    if (M < 0 || M > Q8_SKINNY_MAX_M) return Q8_ERR_SHAPE;
+    if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
+    // drop empty matrices; check the rest
+    q8_linear_desc live[Q8_MAX_BATCH];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+        q8_status st = check_desc(descs[i], M);
+        if (st != Q8_OK) return st;
+        if (descs[i].N > 0) live[n++] = descs[i];
+    }
+    if (M == 0 || n == 0) return Q8_OK;
+    const DeviceInfo *di;
+    q8_status st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_skinny(live, n, M, variant, ws, ws_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q8_status q8_linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M,
+                          void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+    return q8_linear_batch_ex(descs, count, M, Q8_VARIANT_AUTO, ws, ws_bytes, dev_status, stream);
+}
+
+q8_status q8_gemm_skinny(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                         const uint16_t *x, int64_t ldx, int32_t M, float *y, int64_t ldy,
+                         void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+    q8_linear_desc d;
+    d.q = q;
+    d.s = s;
+    d.x = x;
+    d.y = y;
+    d.N = N;
+    d.K = K;
+    d.ldx = ldx;
+    d.ldy = ldy;
+    return q8_linear_batch_ex(&d, 1, M, Q8_VARIANT_AUTO, ws, ws_bytes, dev_status, stream);
+}
+
+q8_status q8_gemv(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, float *y,
+                  void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+    return q8_gemm_skinny(q, s, N, K, x, K + ((8 - K % 8) % 8), 1, y, N > 0 ? N : 1, ws, ws_bytes,
+                          dev_status, stream);
+}
+
+q8_status q8_gemm(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
+                  int32_t M, uint16_t *y, int64_t ldy, uint32_t *dev_status, q8_stream_t stream) {
+    q8_status st = check_weights(q, s, N, K);
+    if (st != Q8_OK) return st;
+    if (M < 0) return Q8_ERR_SHAPE;
+    if (N == 0 || M == 0) return Q8_OK;
+    if (!x || !y) return Q8_ERR_ARG;
+    if (ldx < K || ldy < N) return Q8_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(y, 16) || (ldx % 8) || (ldy % 8)) return Q8_ERR_ALIGN;
+    if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
+    const DeviceInfo *di;
+    st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_gemm_tc(q, s, N, K, x, ldx, M, y, ldy, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,160 @@
+// q8_dev.cuh -- device helpers for libq8 (sm_103a): inline-PTX wrappers for
+// streaming loads, mbarriers, bulk async copies, warp MMA and code conversion.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q8.h"
+
+namespace q8 {
+
+// ---------------------------------------------------------------------------
+// global loads
+// ---------------------------------------------------------------------------
+// Weight codes and scales are read exactly once per call: read-only path, no
+// L1 allocation, and ask L2 to fetch whole 256-byte lines (rows are streamed
+// front to back, so the rest of the line is used by the neighbouring lanes and
+// the next iteration).
+__device__ __forceinline__ uint2 ldg_stream_u2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_stream_u4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float4 ldg_stream_f4(const void *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream_u16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// time, for bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Longest any wait in this library may spin before it gives up (ns).  The
+// waits are for copies of a few KB from L2/HBM, normally a few microseconds.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 0.2 s
+
+// ---------------------------------------------------------------------------
+// mbarrier (CTA scope) and bulk async copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete; false if kWaitLimitNs passed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+// 1-D bulk copy global -> shared, completing `bytes` on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// code conversion
+// ---------------------------------------------------------------------------
+// Four int8 codes (one 32-bit word) -> two bf16x2 words, exactly.
+// bf16 holds integers 0..255 exactly, but its 7 fraction bits give unit
+// spacing only on [128, 256): so write 128 + (c & 0x7f) there (0x43 is the
+// high byte of 128.0 in bf16) and subtract 128 (c >= 0) or 256 (c < 0, the
+// sign bit of c lands on the exponent LSB and turns 0x4300 into 0x4380):
+//   c >= 0: (128 + c) - 128 = c;   c < 0: (128 + c + 128) - 256 = c.
+// lo = codes 0,1 ; hi = codes 2,3 (element 0 in the low half).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ void codes4_to_bf16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t plo = __byte_perm(w, 0x43434343u, 0x4140);   // [43 c1 43 c0]
+    const uint32_t phi = __byte_perm(w, 0x43434343u, 0x4342);   // [43 c3 43 c2]
+    const uint32_t alo = plo & 0xFF7FFF7Fu;                      // 128 + (c & 0x7f)
+    const uint32_t ahi = phi & 0xFF7FFF7Fu;
+    const uint32_t blo = (plo & 0x00800080u) | 0x43004300u;     // 128 or 256
+    const uint32_t bhi = (phi & 0x00800080u) | 0x43004300u;
+    lo = bf16x2_sub(alo, blo);
+    hi = bf16x2_sub(ahi, bhi);
+}
+
+// Four int8 codes -> four floats, exactly: 0x4B000000 | u is 2^23 + u for a
+// byte u, and u = c ^ 0x80 = c + 128.
+__device__ __forceinline__ void codes4_to_f32(uint32_t w, float &f0, float &f1, float &f2, float &f3) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float bias = 8388736.0f;  // 2^23 + 128
+    f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - bias;
+    f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - bias;
+    f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - bias;
+    f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - bias;
+}
+
+// bf16 pair (low, high) -> floats
+__device__ __forceinline__ float bf16lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// binary16 bits -> float (exact)
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+    float f;
+    asm("{\n\t.reg .b16 t;\n\tmov.b16 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "h"((unsigned short)h));
+    return f;
+}
+
+// ---------------------------------------------------------------------------
+// warp MMA: D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16_16816(float &d0, float &d1, float &d2, float &d3,
+                                               uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+}  // namespace q8

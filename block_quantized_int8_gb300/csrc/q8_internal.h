@@ -1,0 +1,54 @@
+// q8_internal.h -- host-side declarations shared by the libq8 translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "q8.h"
+
+namespace q8 {
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int cc_major;
+    int cc_minor;
+};
+
+// Cached properties of the current device; nullptr if a CUDA call failed.
+const DeviceInfo *device_info();
+
+// ---- quantizer --------------------------------------------------------------
+q8_status launch_quantize(const float *w, int64_t rows, int64_t K, int8_t *q, uint16_t *s,
+                          uint32_t *dev_status, cudaStream_t stream);
+
+// ---- skinny matmul (M <= 32) -------------------------------------------------
+constexpr int kSkinnyWarps = 8;
+constexpr int kSkinnyThreads = kSkinnyWarps * 32;
+constexpr int kTileRows = kSkinnyWarps * 16;  // rows of W per work item
+
+// Blocks of K held in one x staging buffer, by M class.
+inline int ksb_for_m(int M) { return M <= 8 ? 64 : (M <= 16 ? 32 : 16); }
+
+// Per-matrix split of K and the offsets of its partial sums in the workspace.
+struct SplitPlan {
+    int32_t tiles;      // ceil(N / kTileRows)
+    int32_t S;          // K splits
+    int32_t bps;        // blocks per split
+    size_t part_off;    // byte offset of float partials [S][M][N] (if S > 1)
+    size_t ticket_off;  // byte offset of uint32 tickets [tiles] (if S > 1)
+};
+
+// Plans every descriptor and returns the workspace bytes needed.
+size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans);
+
+q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
+                        void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
+
+// ---- prefill GEMM (M > 32) ----------------------------------------------------
+q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                         const uint16_t *x, int64_t ldx, int32_t M, uint16_t *y, int64_t ldy,
+                         uint32_t *dev_status, cudaStream_t stream);
+
+}  // namespace q8

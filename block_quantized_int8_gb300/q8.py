@@ -1,0 +1,228 @@
+"""Thin ctypes binding of libq8 (include/q8.h): argument marshalling only.
+
+Every entry point takes torch CUDA tensors, passes their device pointers and
+the current (or given) CUDA stream to the C ABI, and raises ``Q8Error`` on a
+non-OK status.  There is no fallback: if ``libq8.so`` is missing or a call
+fails, the call raises.  Outputs may be pre-allocated by the caller or are
+allocated here with torch (device memory is the only thing torch is used for).
+
+Tensor conventions (raw bits are accepted in any 16-bit dtype):
+  q  int8 [N, K]           codes
+  s  16-bit [N, K/32]      binary16 scale bits (torch.float16 or int16/uint16)
+  x  16-bit [M, K]         bf16 activation bits (torch.bfloat16 or int16/uint16)
+  y  float32 [M, N]        (bf16 [M, N] for q8_gemm)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libq8.so")
+
+Q8_OK = 0
+Q8_ERR_ARG, Q8_ERR_ALIGN, Q8_ERR_SHAPE, Q8_ERR_WORKSPACE, Q8_ERR_ARCH, Q8_ERR_CUDA, Q8_ERR_UNSUPPORTED = range(1, 8)
+Q8_DEV_NONFINITE = 0x1
+Q8_DEV_SCALE_OVF = 0x2
+Q8_DEV_TIMEOUT = 0x4
+Q8_SKINNY_MAX_M = 32
+Q8_MAX_BATCH = 64
+Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA = 0, 1, 2
+
+EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
+           "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
+           "q8_abi_version")
+
+
+class Q8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} (status {status})")
+
+
+class LinearDesc(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("ldy", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libq8.so from the package directory (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m block_quantized_int8_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, SZ, U32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+        L.q8_quantize_rows.argtypes = [P, I64, I64, P, P, U32P, P]
+        L.q8_gemv.argtypes = [P, P, I64, I64, P, P, P, SZ, U32P, P]
+        L.q8_gemm_skinny.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, P, SZ, U32P, P]
+        L.q8_linear_batch.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, P, SZ, U32P, P]
+        L.q8_linear_batch_ex.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, I32, P, SZ, U32P, P]
+        L.q8_workspace_size.argtypes = [I64, I64, I32]
+        L.q8_workspace_size.restype = SZ
+        L.q8_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32, I32]
+        L.q8_linear_batch_workspace_size.restype = SZ
+        L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
+        L.q8_status_str.argtypes = [ctypes.c_int]
+        L.q8_status_str.restype = ctypes.c_char_p
+        L.q8_abi_version.restype = I32
+        for name in ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
+                     "q8_linear_batch_ex", "q8_gemm"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_str(st: int) -> str:
+    return lib().q8_status_str(int(st)).decode()
+
+
+def _check(st: int, what: str):
+    if st != Q8_OK:
+        raise Q8Error(st, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(t, name, dtypes, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return t
+
+
+_B16 = (torch.bfloat16, torch.float16, torch.int16, torch.uint16)
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor | None:
+    """A zeroed workspace of ``nbytes`` (None if 0).  Zero once, reuse freely."""
+    if nbytes == 0:
+        return None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------------------
+def q8_quantize_rows(w, q=None, s=None, dev_status=None, stream=None):
+    """Q8_0-quantize float32 w[rows, K] -> (q int8 [rows, K], s float16 [rows, K/32])."""
+    _cuda(w, "w", (torch.float32,), 2)
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    rows, K = w.shape
+    if q is None:
+        q = torch.empty((rows, K), dtype=torch.int8, device=w.device)
+    if s is None:
+        s = torch.empty((rows, max(K // 32, 0)), dtype=torch.float16, device=w.device)
+    st = lib().q8_quantize_rows(_p(w), rows, K, _p(q), _p(s), _p(dev_status), _stream(stream))
+    _check(st, "q8_quantize_rows")
+    return q, s
+
+
+def q8_workspace_size(N: int, K: int, M: int) -> int:
+    return int(lib().q8_workspace_size(N, K, M))
+
+
+def _desc(q, s, x, y):
+    _cuda(q, "q", (torch.int8,), 2)
+    _cuda(s, "s", _B16, 2)
+    _cuda(x, "x", _B16)
+    _cuda(y, "y", (torch.float32,))
+    N, K = q.shape
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    y2 = y if y.dim() == 2 else y.view(1, -1)
+    if x2.stride(1) != 1 or y2.stride(1) != 1 or not q.is_contiguous() or not s.is_contiguous():
+        raise ValueError("q, s must be contiguous; x, y must have unit inner stride")
+    return LinearDesc(q.data_ptr(), s.data_ptr(), x2.data_ptr(), y2.data_ptr(), N, K,
+                      x2.stride(0) if x2.shape[0] > 1 else K, y2.stride(0) if y2.shape[0] > 1 else max(N, 1)), x2.shape[0]
+
+
+def q8_gemv(q, s, x, y=None, ws=None, dev_status=None, stream=None):
+    """y[N] = dequant(q, s) @ x[K] (fp32)."""
+    N, K = q.shape
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=q.device)
+    need = q8_workspace_size(N, K, 1)
+    if ws is None and need:
+        ws = workspace(need, q.device)
+    st = lib().q8_gemv(_p(q), _p(s), N, K, _p(x), _p(y), _p(ws), 0 if ws is None else ws.numel(),
+                       _p(dev_status), _stream(stream))
+    _check(st, "q8_gemv")
+    return y
+
+
+def q8_gemm_skinny(q, s, x, y=None, ws=None, dev_status=None, stream=None):
+    """y[M, N] = x[M, K] @ dequant(q, s)^T (fp32), 1 <= M <= 32."""
+    N, K = q.shape
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=q.device)
+    d, _ = _desc(q, s, x, y)
+    need = q8_workspace_size(N, K, M)
+    if ws is None and need:
+        ws = workspace(need, q.device)
+    st = lib().q8_gemm_skinny(_p(q), _p(s), N, K, _p(x), d.ldx, M, _p(y), d.ldy, _p(ws),
+                              0 if ws is None else ws.numel(), _p(dev_status), _stream(stream))
+    _check(st, "q8_gemm_skinny")
+    return y
+
+
+def make_descs(mats):
+    """[(q, s, x, y), ...] -> (ctypes array of LinearDesc, M)."""
+    arr = (LinearDesc * len(mats))()
+    M = None
+    for i, (q, s, x, y) in enumerate(mats):
+        arr[i], m = _desc(q, s, x, y)
+        if M is not None and m != M:
+            raise ValueError("all matrices of a batch share M")
+        M = m
+    return arr, (M or 0)
+
+
+def q8_linear_batch_workspace_size(descs, M: int) -> int:
+    return int(lib().q8_linear_batch_workspace_size(descs, len(descs), M))
+
+
+def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None, stream=None,
+                    descs=None, M=None):
+    """Run several skinny matmuls in one launch.  ``mats`` = [(q, s, x, y), ...],
+    or pass prepared ``descs`` (from make_descs) and ``M``."""
+    if descs is None:
+        descs, M = make_descs(mats)
+    need = q8_linear_batch_workspace_size(descs, M)
+    if ws is None and need:
+        ws = workspace(need)
+    st = lib().q8_linear_batch_ex(descs, len(descs), M, variant, _p(ws), 0 if ws is None else ws.numel(),
+                                  _p(dev_status), _stream(stream))
+    _check(st, "q8_linear_batch")
+
+
+def q8_gemm(q, s, x, y=None, dev_status=None, stream=None):
+    """y[M, N] (bf16) = x[M, K] @ dequant(q, s)^T for M > 32 (tcgen05 path)."""
+    _cuda(q, "q", (torch.int8,), 2)
+    _cuda(x, "x", _B16, 2)
+    N, K = q.shape
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
+    st = lib().q8_gemm(_p(q), _p(s), N, K, _p(x), x.stride(0), M, _p(y), y.stride(0), _p(dev_status),
+                       _stream(stream))
+    _check(st, "q8_gemm")
+    return y

@@ -1,0 +1,192 @@
+/*
+ * q8.h -- C ABI of libq8: the Q8_0 W8A16 decode matmul on GB300 (sm_103a).
+ *
+ * Format (from "MODEL-BASELINE-RESULTS" (fak), ACT 3 item 1 and ACT 4
+ * "Correctness"): a weight matrix W[N][K] is cut along K into blocks of 32.
+ * Each block stores one scale d = maxabs/127, kept as IEEE binary16 (the page's
+ * ~1.06 bytes per weight is 32 one-byte codes plus a two-byte scale), and 32
+ * int8 codes q = round-half-away-from-zero(w/d), so that w ~= d*q.  The
+ * matmul is W8A16 ("Frigg" README, Finding 8): int8 weights times bf16
+ * activations, each weight read from memory once per call, fp32 accumulation.
+ *
+ * Storage is planar and row-major:
+ *   codes   int8      q[N][K]        (row n at q + n*K)
+ *   scales  binary16  s[N][K/32]     (raw bits in uint16_t)
+ *   x       bfloat16  x[M][ldx]      (raw bits in uint16_t)
+ *   y       float     y[M][ldy]      (bf16 bits for q8_gemm)
+ * so that y[m][n] = sum_k s[n][k/32] * q[n][k] * x[m][k].
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or synchronises; work is enqueued on `stream`
+ *    (NULL = the legacy default stream) and may still be running on return.
+ *  - Arguments are checked on the host before any CUDA call; a failed check
+ *    returns an error status and enqueues nothing.  Launch failures return
+ *    Q8_ERR_CUDA (the CUDA error is left for cudaGetLastError()).
+ *  - `dev_status` (nullable) is a device word the kernels OR bits into
+ *    (Q8_DEV_*) when they meet bad data or give up waiting; read it after
+ *    your own synchronisation.  The kernels never trap.
+ *  - Alignment: q, s and x must be 16-byte aligned, ldx a multiple of 8;
+ *    y must be 4-byte aligned (2-byte for bf16 output).  K must be a
+ *    positive multiple of 32.  N == 0 or M == 0 is a no-op.
+ *  - Results are bitwise reproducible from run to run and under CUDA-graph
+ *    replay for the same arguments (split-K partial sums are combined in a
+ *    fixed order, never with floating-point atomics).
+ */
+#ifndef Q8_H_
+#define Q8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *q8_stream_t;
+
+typedef enum q8_status {
+    Q8_OK = 0,
+    Q8_ERR_ARG = 1,        /* null pointer or bad count */
+    Q8_ERR_ALIGN = 2,      /* pointer or leading dimension misaligned */
+    Q8_ERR_SHAPE = 3,      /* K not a positive multiple of 32, M out of range, ld too small */
+    Q8_ERR_WORKSPACE = 4,  /* workspace missing or smaller than the *_workspace_size() result */
+    Q8_ERR_ARCH = 5,       /* current device is not compute capability 10.3 */
+    Q8_ERR_CUDA = 6,       /* a CUDA runtime call failed */
+    Q8_ERR_UNSUPPORTED = 7 /* valid request this build does not implement */
+} q8_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define Q8_DEV_NONFINITE 0x1u /* quantizer: a block held NaN/Inf; stored as zero codes, zero scale */
+#define Q8_DEV_SCALE_OVF 0x2u /* quantizer: amax/127 overflowed binary16; block stored as zeros */
+#define Q8_DEV_TIMEOUT   0x4u /* a bounded wait gave up; outputs of that call are not valid */
+
+#define Q8_BLOCK 32          /* weights per block along K */
+#define Q8_SKINNY_MAX_M 32   /* largest M for q8_gemv / q8_gemm_skinny / q8_linear_batch */
+#define Q8_MAX_BATCH 64      /* most descriptors per q8_linear_batch call */
+
+/* Kernel variants for the M <= 32 path (the _ex entry points). */
+#define Q8_VARIANT_AUTO 0
+#define Q8_VARIANT_SIMT 1    /* CUDA-core FFMA: codes dequantised in registers, one FMA per weight per row */
+#define Q8_VARIANT_MMA  2    /* warp mma.sync bf16 on exact bf16 codes, block scale applied in fp32 */
+
+/*
+ * q8_quantize_rows -- Q8_0-quantize binary32 weights w[rows][K] along K.
+ * Source: "MODEL-BASELINE-RESULTS" (fak), ACT 3 item 1 (blocks of 32,
+ * d = maxabs/127), ACT 4 "Correctness" (round half away from zero; 0.49999997
+ * gives 0), ACT 5 item 3 (exact on zeros, denormals, exact halves).
+ * Per block: amax = max|w| (binary32), d = amax/127 (binary32, round to
+ * nearest even), s = binary16(d) (nearest even, subnormals kept), then
+ * q = clamp(round-half-away(w/s), -127, 127) with the quotient taken exactly
+ * against the stored s; s == 0 gives q = 0.  A block holding NaN/Inf, or whose
+ * s overflows, is stored as zeros and sets Q8_DEV_NONFINITE / Q8_DEV_SCALE_OVF.
+ *   w  : float [rows][K], 16-byte aligned     (in)
+ *   q  : int8  [rows][K], 16-byte aligned     (out)
+ *   s  : binary16 bits [rows][K/32], 16-byte aligned (out)
+ * The result is bit-identical to the definition above (no tolerance).
+ */
+q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K,
+                           int8_t *q, uint16_t *s,
+                           uint32_t *dev_status, q8_stream_t stream);
+
+/*
+ * q8_gemv -- y[n] = sum_k s[n][k/32]*q[n][k]*x[k] for one activation row (M = 1).
+ * Source: "Frigg" README, "The machine" (at batch 1 every decode GEMM is this
+ * GEMV shape) and Finding 8 (W8A16: read each weight once).
+ *   q, s : Q8_0 weights [N][K], [N][K/32]      (in)
+ *   x    : bf16 bits [K]                        (in)
+ *   y    : float [N]                            (out)
+ *   ws   : workspace of q8_workspace_size(N, K, 1) bytes (may be NULL if that
+ *          is 0).  Zero it once after allocation; the kernels leave it zeroed
+ *          again, so it can be reused across calls and graph replays, but not
+ *          by two calls that run at the same time.
+ * Accuracy: |y - y_ref| <= 2e-3 * sum_k |s*q*x| + 1e-6 per output, where y_ref
+ * is the exact dequantise-then-dot value.
+ */
+q8_status q8_gemv(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                  const uint16_t *x, float *y,
+                  void *ws, size_t ws_bytes,
+                  uint32_t *dev_status, q8_stream_t stream);
+
+/*
+ * q8_gemm_skinny -- Y[M][N] = X[M][K] * W^T for 1 <= M <= 32 decode rows.
+ * Source: "Frigg" README, Finding 8 (a batched W8A16 kernel reads each weight
+ * matrix once for the whole batch; split-K through a partials buffer rather
+ * than atomics so that replays are bit-identical).
+ *   x : bf16 bits [M][ldx], ldx >= K and a multiple of 8   (in)
+ *   y : float [M][ldy], ldy >= N                            (out)
+ *   ws: q8_workspace_size(N, K, M) bytes, zeroed once (see q8_gemv).
+ * Accuracy as q8_gemv.
+ */
+q8_status q8_gemm_skinny(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                         const uint16_t *x, int64_t ldx, int32_t M,
+                         float *y, int64_t ldy,
+                         void *ws, size_t ws_bytes,
+                         uint32_t *dev_status, q8_stream_t stream);
+
+/* One matrix of a q8_linear_batch call: y = x * W^T with W = (q, s). */
+typedef struct q8_linear_desc {
+    const int8_t *q;     /* int8 [N][K] */
+    const uint16_t *s;   /* binary16 bits [N][K/32] */
+    const uint16_t *x;   /* bf16 bits [M][ldx] */
+    float *y;            /* float [M][ldy] */
+    int64_t N, K, ldx, ldy;
+} q8_linear_desc;
+
+/*
+ * q8_linear_batch -- several independent skinny matmuls (same M, any shapes)
+ * in ONE persistent launch that walks a static list of (matrix, row tile,
+ * K split) work items.  Source: "Frigg" README, Finding 3 and Finding 8 (a
+ * decode step of many small matmuls is launch-bound before it is
+ * bandwidth-bound).
+ *   descs : HOST array of `count` descriptors, 1 <= count <= Q8_MAX_BATCH;
+ *           copied into the launch, may be reused on return.
+ *   ws    : q8_linear_batch_workspace_size(descs, count, M) bytes, zeroed once.
+ * Each output equals, bit for bit, what q8_gemm_skinny returns for that matrix.
+ * Outputs must not overlap each other or any input.
+ */
+q8_status q8_linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M,
+                          void *ws, size_t ws_bytes,
+                          uint32_t *dev_status, q8_stream_t stream);
+
+/* As q8_linear_batch / q8_gemm_skinny with an explicit kernel variant
+ * (Q8_VARIANT_*), for side-by-side measurement.  Variants agree within the
+ * accuracy bound, not bit for bit. */
+q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t M,
+                             int32_t variant, void *ws, size_t ws_bytes,
+                             uint32_t *dev_status, q8_stream_t stream);
+
+/* Workspace bytes (split-K partial sums and tickets) for the calls above;
+ * depends only on the shapes, not on the device.  0 means none is needed. */
+size_t q8_workspace_size(int64_t N, int64_t K, int32_t M);
+size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M);
+
+/*
+ * q8_gemm -- prefill-shaped Y[M][N] = X[M][K] * W^T for M > 32 on the 5th
+ * generation tensor cores (tcgen05): each weight tile is dequantised to bf16
+ * (bf16(s*q), round to nearest even) in shared memory and multiplied in bf16
+ * with fp32 accumulation in tensor memory; y is bf16 (round to nearest even).
+ * Source: "MODEL-BASELINE-RESULTS" (fak), ACT 4 (batched prefill GEMM that
+ * reads each weight once for all tokens) and "Parity lane" item 2.
+ *   x : bf16 bits [M][ldx]; y : bf16 bits [M][ldy]; ldx, ldy multiples of 8.
+ * Accuracy: |y - y_ref| <= 2e-3 * sum_k |s*q*x| + 1e-6 + half a bf16 ulp of y_ref
+ * on the tested workloads (the bf16 weight tile rounds each weight by up to
+ * 2^-9 relative; see the design notes).
+ */
+q8_status q8_gemm(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                  const uint16_t *x, int64_t ldx, int32_t M,
+                  uint16_t *y, int64_t ldy,
+                  uint32_t *dev_status, q8_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *q8_status_str(q8_status st);
+
+/* ABI version of this header (bumped on any signature change). */
+int32_t q8_abi_version(void);
+#define Q8_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q8_H_ */

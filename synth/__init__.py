@@ -5,8 +5,8 @@ rounding of codes, no dot products).  It only draws random numbers and lays
 out special values, so that the oracle and the CUDA path see the same inputs.
 
 Every tensor is drawn from ``numpy.random.PCG64`` seeded with
-``SeedSequence([seed, crc32(tag)])``: the same (seed, tag) always gives the same
-numbers on any machine, and different tags give independent streams.
+``SeedSequence([seed, crc32(tag), chunk])``: the same (seed, tag) always gives
+the same numbers on any machine, and different tags give independent streams.
 
 Workload recipe (shapes, distributions) follows the decode matmul it feeds:
 weights ~ N(0, 0.02) in binary32 (quantized to Q8_0 before use), activations
@@ -15,7 +15,9 @@ RMS-normalised row scaled by 1/sqrt(K)).
 """
 from __future__ import annotations
 
+import os
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -27,11 +29,33 @@ def rng(seed: int, tag: str) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(ss))
 
 
+_CHUNK = 1 << 22
+
+
 def normal_f32(shape, seed: int, tag: str, std: float = 1.0) -> np.ndarray:
-    a = rng(seed, tag).standard_normal(size=shape, dtype=np.float32)
-    if std != 1.0:
-        a *= np.float32(std)
-    return a
+    """N(0, std^2) binary32 draws.  The flat array is filled in fixed chunks of
+    2^22 values, chunk i from its own stream (seed, crc32(tag), i), so the
+    values do not depend on how many threads fill it."""
+    shape = (shape,) if isinstance(shape, (int, np.integer)) else tuple(shape)
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.float32)
+    crc = zlib.crc32(tag.encode())
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def fill(i):
+        ss = np.random.SeedSequence([int(seed) & 0xFFFFFFFF, crc, i])
+        g = np.random.Generator(np.random.PCG64(ss))
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        g.standard_normal(out=out[lo:hi], dtype=np.float32)
+        if std != 1.0:
+            out[lo:hi] *= np.float32(std)
+
+    if nchunks > 1:
+        with ThreadPoolExecutor(min(nchunks, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(nchunks)))
+    elif n:
+        fill(0)
+    return out.reshape(shape)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:

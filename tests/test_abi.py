@@ -1,0 +1,135 @@
+"""libq8 C ABI: the library loads, exports every function include/q8.h
+declares, and rejects bad arguments on the host before any CUDA call (so
+these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q8.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_quantized_int8_gb300 import build, q8
+    build.build()
+    return q8.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(q8_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_gemm"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    from block_quantized_int8_gb300 import q8
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert set(q8.EXPORTS) <= set(declared_functions())
+    assert L.q8_abi_version() == 1
+
+
+def test_status_strings(L):
+    from block_quantized_int8_gb300 import q8
+    for st in range(0, 8):
+        assert q8.status_str(st)
+    assert q8.status_str(99) == "unknown status"
+
+
+# Fake, well-aligned device addresses: the calls below must fail validation
+# before touching them.
+A = 1 << 20
+
+
+def call_gemv(L, q=A, s=A, N=128, K=64, x=A, y=A, ws=None, wsb=0):
+    return L.q8_gemv(q, s, N, K, x, y, ws, wsb, None, None)
+
+
+def test_gemv_validation(L):
+    from block_quantized_int8_gb300 import q8
+    assert call_gemv(L, K=33) == q8.Q8_ERR_SHAPE
+    assert call_gemv(L, K=0) == q8.Q8_ERR_SHAPE
+    assert call_gemv(L, K=-32) == q8.Q8_ERR_SHAPE
+    assert call_gemv(L, N=-1) == q8.Q8_ERR_SHAPE
+    assert call_gemv(L, q=None) == q8.Q8_ERR_ARG
+    assert call_gemv(L, x=None) == q8.Q8_ERR_ARG
+    assert call_gemv(L, y=None) == q8.Q8_ERR_ARG
+    assert call_gemv(L, q=A + 8) == q8.Q8_ERR_ALIGN
+    assert call_gemv(L, s=A + 2) == q8.Q8_ERR_ALIGN
+    assert call_gemv(L, x=A + 4) == q8.Q8_ERR_ALIGN
+    assert call_gemv(L, y=A + 2) == q8.Q8_ERR_ALIGN
+    assert call_gemv(L, N=0) == q8.Q8_OK          # empty: no-op, no CUDA call
+
+
+def test_skinny_validation(L):
+    from block_quantized_int8_gb300 import q8
+    f = L.q8_gemm_skinny
+    assert f(A, A, 64, 64, A, 64, 33, A, 64, None, 0, None, None) == q8.Q8_ERR_SHAPE   # M > 32
+    assert f(A, A, 64, 64, A, 64, -1, A, 64, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, A, 64, 64, A, 60, 2, A, 64, None, 0, None, None) == q8.Q8_ERR_SHAPE    # ldx < K
+    assert f(A, A, 64, 64, A, 64, 2, A, 63, None, 0, None, None) == q8.Q8_ERR_SHAPE    # ldy < N
+    assert f(A, A, 64, 64, A, 68, 2, A, 64, None, 0, None, None) == q8.Q8_ERR_ALIGN    # ldx % 8
+    assert f(A, A, 64, 64, A, 64, 0, A, 64, None, 0, None, None) == q8.Q8_OK           # M == 0
+    assert f(A, A, 64, 64, A, 64, 2, A, 64, None, 0, A + 1, None) == q8.Q8_ERR_ALIGN   # dev_status
+
+
+def test_batch_validation(L):
+    from block_quantized_int8_gb300 import q8
+    d = (q8.LinearDesc * 2)()
+    for i in range(2):
+        d[i] = q8.LinearDesc(A, A, A, A, 64, 64, 64, 64)
+    assert L.q8_linear_batch(d, 65, 1, None, 0, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_batch(None, 1, 1, None, 0, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_batch_ex(d, 2, 1, 7, None, 0, None, None) == q8.Q8_ERR_ARG
+    d[1].K = 48
+    assert L.q8_linear_batch(d, 2, 1, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    d[1].K = 64
+    d[1].x = A + 2
+    assert L.q8_linear_batch(d, 2, 1, None, 0, None, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_linear_batch(d, 0, 1, None, 0, None, None) == q8.Q8_OK
+
+
+def test_quantize_validation(L):
+    from block_quantized_int8_gb300 import q8
+    f = L.q8_quantize_rows
+    assert f(A, 4, 40, A, A, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, -1, 64, A, A, None, None) == q8.Q8_ERR_SHAPE
+    assert f(None, 4, 64, A, A, None, None) == q8.Q8_ERR_ARG
+    assert f(A + 4, 4, 64, A, A, None, None) == q8.Q8_ERR_ALIGN
+    assert f(A, 0, 64, A, A, None, None) == q8.Q8_OK
+
+
+def test_gemm_validation(L):
+    from block_quantized_int8_gb300 import q8
+    f = L.q8_gemm
+    assert f(A, A, 64, 48, A, 64, 64, A, 64, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, A, 64, 64, A, 64, 64, A, 60, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, A, 64, 64, A, 64, 64, A + 8, 64, None, None) == q8.Q8_ERR_ALIGN
+
+
+def test_workspace_sizes(L):
+    from block_quantized_int8_gb300 import q8
+    # invalid shapes need nothing
+    assert L.q8_workspace_size(0, 64, 1) == 0
+    assert L.q8_workspace_size(64, 33, 1) == 0
+    assert L.q8_workspace_size(64, 64, 33) == 0
+    # a huge N needs no split; a short-N, long-K matrix does
+    assert L.q8_workspace_size(262144, 1536, 1) == 0
+    w = L.q8_workspace_size(1536, 4096, 1)
+    assert w > 0 and w % 256 == 0
+    # a batch needs the sum of its members' workspaces
+    d = (q8.LinearDesc * 2)()
+    d[0] = q8.LinearDesc(A, A, A, A, 1536, 4096, 4096, 1536)
+    d[1] = q8.LinearDesc(A, A, A, A, 262144, 1536, 1536, 262144)
+    assert L.q8_linear_batch_workspace_size(d, 2, 1) == w
+    # and the size does not depend on which device is current (host arithmetic)
+    assert L.q8_workspace_size(1536, 4096, 32) >= L.q8_workspace_size(1536, 4096, 1)

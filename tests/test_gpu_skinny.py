@@ -1,0 +1,243 @@
+"""M <= 32 matmul kernels (q8_gemv, q8_gemm_skinny, q8_linear_batch) vs the
+oracle.  Exactly representable inputs must match bit for bit; random Q8_0
+inputs must satisfy |y - y_ref| <= 2e-3 * sum|w'x| + 1e-6 per output."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from helpers import check_tol, dev, weights_dev, x_dev
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [1, 2]  # Q8_VARIANT_SIMT, Q8_VARIANT_MMA
+
+
+def run_batch(mats_np, M, variant, ws_extra=0):
+    """mats_np = [(q, s, x_bits)]; returns list of y (numpy fp32)."""
+    from block_quantized_int8_gb300 import q8
+    mats = []
+    outs = []
+    for (qn, sn, xn) in mats_np:
+        q, s = weights_dev(qn, sn)
+        x = x_dev(xn)
+        y = torch.full((M, qn.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+        mats.append((q, s, x, y))
+        outs.append(y)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8.q8_linear_batch(mats, variant=variant, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return [y.cpu().numpy() for y in outs]
+
+
+# ---------------------------------------------------------------------------
+# exact cases: every product and sum is exact in fp32 -> bit-exact
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 64), (128, 96), (129, 1536), (300, 4096), (1536, 1536)])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16, 17, 32])
+def test_exact_cases_bit_exact(oracle, variant, N, K, M):
+    q, s, x = synth.exact_case(N, K, M, 0, f"ex{N}.{K}.{M}")
+    y_ref, _ = oracle.matmul(q, s, x)
+    (y,) = run_batch([(q, s, x)], M, variant)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_unit_vectors(oracle, variant):
+    N, K = 200, 1536
+    q, s, _ = oracle.quantize_rows(synth.weights(N, K, 0, "uvec"))
+    for k in [0, 31, 32, 700, 1535]:
+        x = synth.unit_vector_x(K, k)
+        (y,) = run_batch([(q, s, x)], 1, variant)
+        expect = s[:, k // 32].view(np.float16).astype(np.float64) * q[:, k]
+        assert np.array_equal(y[0].astype(np.float64), expect)
+
+
+# ---------------------------------------------------------------------------
+# random Q8_0 weights, tolerance; sizes span several tiles, splits and a tail
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("N,K", [(300, 1536), (1536, 4096), (4097, 1536), (33, 32)])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 13, 32])
+def test_random_tolerance(oracle, variant, N, K, M):
+    q, s, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"rt{N}.{K}"))
+    x = synth.activations(M, K, 0, f"rtx{M}.{K}")
+    y_ref, B = oracle.matmul(q, s, x, threads=8)
+    (y,) = run_batch([(q, s, x)], M, variant)
+    check_tol(y, y_ref, B, f"N={N} K={K} M={M} variant={variant}")
+
+
+def test_gemv_and_skinny_entry_points(oracle):
+    from block_quantized_int8_gb300 import q8
+    N, K = 1536, 4096
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, "ep"))
+    xn = synth.activations(4, K, 0, "epx")
+    y_ref, B = oracle.matmul(qn, sn, xn)
+    q, s = weights_dev(qn, sn)
+    x = x_dev(xn)
+    y1 = q8.q8_gemv(q, s, x[0].contiguous())
+    y4 = q8.q8_gemm_skinny(q, s, x)
+    torch.cuda.synchronize()
+    check_tol(y1.cpu().numpy()[None], y_ref[:1], B[:1], "gemv")
+    check_tol(y4.cpu().numpy(), y_ref, B, "skinny")
+
+
+def test_strided_x_and_y(oracle):
+    from block_quantized_int8_gb300 import q8
+    N, K, M = 520, 1536, 3
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, "strided"))
+    xn = synth.activations(M, K, 0, "stridedx")
+    y_ref, B = oracle.matmul(qn, sn, xn)
+    q, s = weights_dev(qn, sn)
+    xb = torch.zeros((M, K + 64), dtype=torch.bfloat16, device="cuda")
+    xb[:, :K] = x_dev(xn)
+    yb = torch.full((M, N + 40), -7.0, dtype=torch.float32, device="cuda")
+    q8.q8_gemm_skinny(q, s, xb[:, :K], yb[:, :N])
+    torch.cuda.synchronize()
+    out = yb.cpu().numpy()
+    check_tol(out[:, :N], y_ref, B, "strided")
+    assert np.all(out[:, N:] == -7.0)  # nothing written past ldy's live columns
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads of the benchmark (sampled or full comparisons)
+# ---------------------------------------------------------------------------
+def test_tiny_gemv_full(oracle):
+    N, K = 4096, 1536
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, "tiny"))
+    xn = synth.activations(1, K, 0, "tinyx")
+    y_ref, B = oracle.matmul(qn, sn, xn, threads=8)
+    for v in VARIANTS:
+        (y,) = run_batch([(qn, sn, xn)], 1, v)
+        check_tol(y, y_ref, B, f"tiny v{v}")
+
+
+def test_vocab_gemv_sampled(oracle):
+    from block_quantized_int8_gb300 import q8
+    N, K = synth.VOCAB, synth.HIDDEN
+    w = synth.weights(N, K, 0, "vocab")
+    q, s = q8.q8_quantize_rows(dev(w))
+    xn = synth.unit_activation(K, 0)
+    y = q8.q8_gemv(q, s, x_dev(xn)[0].contiguous())
+    torch.cuda.synchronize()
+    rows = np.sort(synth.rng(0, "vocab.rows").choice(N, 4096, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, N - 1]]))
+    qn, sn, _ = oracle.quantize_rows(w[rows])
+    y_ref, B = oracle.matmul(qn, sn, xn)
+    check_tol(y.cpu().numpy()[rows][None], y_ref, B, "vocab")
+
+
+@pytest.mark.parametrize("K,N", synth.SWEEP_SHAPES)
+@pytest.mark.parametrize("M", synth.SWEEP_M)
+def test_sweep_full(oracle, K, N, M):
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"sweep{K}.{N}"))
+    xn = synth.activations(M, K, 0, f"sweepx{M}.{K}")
+    rows = np.arange(N) if M <= 8 else np.unique(np.concatenate(
+        [synth.rng(0, "sweep.rows").choice(N, 1024, replace=False), [0, N - 1]]))
+    y_ref, B = oracle.matmul(qn[rows], sn[rows], xn, threads=8)
+    for v in VARIANTS:
+        (y,) = run_batch([(qn, sn, xn)], M, v)
+        check_tol(y[:, rows], y_ref, B, f"sweep K={K} N={N} M={M} v{v}")
+
+
+def test_layer_set_batch_sampled(oracle):
+    """One pass of the decode layer set (16 layers x 4 matrices) as one batch."""
+    from block_quantized_int8_gb300 import q8
+    mats, refs = [], []
+    xs = {K: synth.activations(1, K, 0, synth.layer_x_tag(0, K)) for K in (synth.HIDDEN, synth.INTER)}
+    for layer in range(synth.LAYERS):
+        for (name, K, N) in synth.LAYER_MATRICES:
+            w = synth.weights(N, K, 0, synth.layer_weight_tag(layer, name))
+            q, s = q8.q8_quantize_rows(dev(w))
+            y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+            mats.append((q, s, x_dev(xs[K]), y))
+            rows = np.unique(np.concatenate([synth.rng(layer, name).choice(N, 48, replace=False), [0, N - 1]]))
+            refs.append((w, rows, xs[K]))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8.q8_linear_batch(mats, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for (q, s, x, y), (w, rows, xn) in zip(mats, refs):
+        qn, sn, _ = oracle.quantize_rows(w[rows])
+        y_ref, B = oracle.matmul(qn, sn, xn)
+        check_tol(y.cpu().numpy()[:, rows], y_ref, B, "layer set")
+
+
+# ---------------------------------------------------------------------------
+# determinism, graph replay, batch == separate calls
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_batch_equals_separate_calls_bitwise(oracle, variant):
+    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 64)]
+    M = 3
+    mats_np = []
+    for i, (N, K) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"bs{i}"))
+        mats_np.append((qn, sn, synth.activations(M, K, 0, f"bsx{i}")))
+    together = run_batch(mats_np, M, variant)
+    for m_np, y_t in zip(mats_np, together):
+        (y_s,) = run_batch([m_np], M, variant)
+        assert np.array_equal(y_s, y_t)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_deterministic_and_graph_replay(oracle, variant):
+    from block_quantized_int8_gb300 import q8
+    N, K, M = 1536, 4096, 4   # split-K path
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, "det"))
+    q, s = weights_dev(qn, sn)
+    x = x_dev(synth.activations(M, K, 0, "detx"))
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    descs, _ = q8.make_descs([(q, s, x, y)])
+    ws = q8.workspace(q8.q8_linear_batch_workspace_size(descs, M))
+    assert ws is not None   # this shape is split along K
+    q8.q8_linear_batch(descs=descs, M=M, ws=ws, variant=variant)
+    torch.cuda.synchronize()
+    first = y.clone()
+    for _ in range(3):
+        y.zero_()
+        q8.q8_linear_batch(descs=descs, M=M, ws=ws, variant=variant)
+        torch.cuda.synchronize()
+        assert torch.equal(y, first)
+    # capture into a CUDA graph and replay
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        q8.q8_linear_batch(descs=descs, M=M, ws=ws, variant=variant)  # warm on the capture stream
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        q8.q8_linear_batch(descs=descs, M=M, ws=ws, variant=variant)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, first)
+    # the split-K tickets (first words of the workspace) are reset after every call
+    tiles = (N + 127) // 128
+    assert int(ws[: 4 * tiles].ne(0).sum().item()) == 0
+
+
+def test_workspace_too_small_is_rejected(oracle):
+    from block_quantized_int8_gb300 import q8
+    N, K = 1536, 4096
+    q = torch.zeros((N, K), dtype=torch.int8, device="cuda")
+    s = torch.zeros((N, K // 32), dtype=torch.float16, device="cuda")
+    x = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    need = q8.q8_workspace_size(N, K, 1)
+    ws = q8.workspace(need - 256)
+    with pytest.raises(q8.Q8Error) as e:
+        q8.q8_gemm_skinny(q, s, x, y, ws=ws)
+    assert e.value.status == q8.Q8_ERR_WORKSPACE
+
+
+def test_empty_shapes_noop():
+    from block_quantized_int8_gb300 import q8
+    q = torch.zeros((0, 64), dtype=torch.int8, device="cuda")
+    s = torch.zeros((0, 2), dtype=torch.float16, device="cuda")
+    x = torch.zeros((2, 64), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((2, 0), dtype=torch.float32, device="cuda")
+    q8.q8_gemm_skinny(q, s, x, y)
+    torch.cuda.synchronize()
