@@ -43,6 +43,10 @@ struct SplitPlan {
 // Plans every descriptor and returns the workspace bytes needed.
 size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans);
 
+// M = 1 bulk-copy pipeline (q8_gemv.cu): matrices with K <= 16384.
+bool gemv_supported(const q8_linear_desc *descs, int count);
+q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_status, cudaStream_t stream);
+
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
 

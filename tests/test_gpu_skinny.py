@@ -224,9 +224,10 @@ def test_workspace_too_small_is_rejected(oracle):
     N, K = 1536, 4096
     q = torch.zeros((N, K), dtype=torch.int8, device="cuda")
     s = torch.zeros((N, K // 32), dtype=torch.float16, device="cuda")
-    x = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
-    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
-    need = q8.q8_workspace_size(N, K, 1)
+    x = torch.zeros((4, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((4, N), dtype=torch.float32, device="cuda")
+    need = q8.q8_workspace_size(N, K, 4)
+    assert need > 256   # M = 4 on this short-N, long-K shape splits K
     ws = q8.workspace(need - 256)
     with pytest.raises(q8.Q8Error) as e:
         q8.q8_gemm_skinny(q, s, x, y, ws=ws)
@@ -241,3 +242,34 @@ def test_empty_shapes_noop():
     y = torch.zeros((2, 0), dtype=torch.float32, device="cuda")
     q8.q8_gemm_skinny(q, s, x, y)
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# the M = 1 pipeline: K slicing (1, 2, 4, 8 slices), scale tails that are not
+# a multiple of 16 bytes, and the fallback beyond its largest K
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("K", [32, 96, 1568, 2080, 4096, 6176, 8192, 12320, 16384, 16416])
+@pytest.mark.parametrize("N", [1, 7, 33, 300])
+def test_gemv_k_slicing_exact(oracle, K, N):
+    q, s, x = synth.exact_case(N, K, 1, 0, f"gk{N}.{K}")
+    y_ref, _ = oracle.matmul(q, s, x)
+    for v in VARIANTS:
+        (y,) = run_batch([(q, s, x)], 1, v)
+        assert np.array_equal(y.astype(np.float64), y_ref), f"variant {v}"
+
+
+def test_gemv_mixed_batch_tolerance(oracle):
+    """Matrices of different K (different slice counts) in one M = 1 launch."""
+    shapes = [(300, 96), (1000, 1536), (77, 4096), (513, 8192), (5, 32), (129, 2080)]
+    mats_np = []
+    for i, (N, K) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"mix{i}"))
+        mats_np.append((qn, sn, synth.activations(1, K, 0, f"mixx{i}")))
+    ys = run_batch(mats_np, 1, 0)
+    for (qn, sn, xn), y in zip(mats_np, ys):
+        y_ref, B = oracle.matmul(qn, sn, xn)
+        check_tol(y, y_ref, B, f"mixed N={qn.shape[0]} K={qn.shape[1]}")
+    # and each matrix alone gives the same bits
+    for m_np, y in zip(mats_np, ys):
+        (y1,) = run_batch([m_np], 1, 0)
+        assert np.array_equal(y1, y)
