@@ -37,8 +37,8 @@ import synth  # noqa: E402
 METRIC = "Q8_0 W8A16 decode GEMV achieved HBM GB/s and % of GB300 peak, M=1..32"
 WORKLOAD = ("decode layer set: 16 layers x 8 passes, M=1, Q8_0 weights "
             "K1536->N4608 (QKV), 1536->1536 (o_proj), 1536->8192 (gate+up), 4096->1536 (down)")
-KERNEL_SOURCES = ["block_quantized_int8_gb300/csrc/q8_skinny.cu", "block_quantized_int8_gb300/csrc/q8_dev.cuh"]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "skinny_kernel_layer_set.md")
+KERNEL_SOURCES = ["block_quantized_int8_gb300/csrc/q8_gemv.cu", "block_quantized_int8_gb300/csrc/q8_dev.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_kernel_layer_set.md")
 
 
 def log(*a):
@@ -547,7 +547,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                         else "fallback 6.8 TB/s", "kernel": "skinny_kernel (q8_linear_batch, one pass)",
+                         else "fallback 6.8 TB/s", "kernel": "gemv_kernel (q8_linear_batch, M=1, one pass of 64 matrices)",
                          "launch_us": round(launch_ms * 1e3, 2), "bytes_per_launch": bytes_pass},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
