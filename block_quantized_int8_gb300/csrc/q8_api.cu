@@ -54,6 +54,12 @@ static q8_status check_desc(const q8_linear_desc &d, int32_t M) {
     return Q8_OK;
 }
 
+// Host-only argument check of one skinny matmul (no CUDA call).
+q8_status check_skinny_args(const q8_linear_desc &d, int32_t M) {
+    if (M < 0 || M > Q8_SKINNY_MAX_M) return Q8_ERR_SHAPE;
+    return check_desc(d, M);
+}
+
 }  // namespace q8
 
 using namespace q8;

@@ -50,6 +50,9 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_stat
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
 
+// Host-only argument check of one skinny matmul, as q8_gemm_skinny does it.
+q8_status check_skinny_args(const q8_linear_desc &d, int32_t M);
+
 // ---- prefill GEMM (M > 32) ----------------------------------------------------
 q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                          const uint16_t *x, int64_t ldx, int32_t M, uint16_t *y, int64_t ldy,

@@ -33,7 +33,8 @@ Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA = 0, 1, 2
 
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
            "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
-           "q8_abi_version")
+           "q8_abi_version", "q8_gemm_skinny_noalloc")
+Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class Q8Error(RuntimeError):
@@ -69,11 +70,12 @@ def lib():
         L.q8_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32, I32]
         L.q8_linear_batch_workspace_size.restype = SZ
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
+        L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_status_str.argtypes = [ctypes.c_int]
         L.q8_status_str.restype = ctypes.c_char_p
         L.q8_abi_version.restype = I32
         for name in ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
-                     "q8_linear_batch_ex", "q8_gemm"):
+                     "q8_linear_batch_ex", "q8_gemm", "q8_gemm_skinny_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -181,6 +183,22 @@ def q8_gemm_skinny(q, s, x, y=None, ws=None, dev_status=None, stream=None):
     st = lib().q8_gemm_skinny(_p(q), _p(s), N, K, _p(x), d.ldx, M, _p(y), d.ldy, _p(ws),
                               0 if ws is None else ws.numel(), _p(dev_status), _stream(stream))
     _check(st, "q8_gemm_skinny")
+    return y
+
+
+def q8_gemm_skinny_noalloc(q, s, x, y=None, dev_status=None, stream=None):
+    """As q8_gemm_skinny, for callers that cannot allocate device memory: the
+    split-K scratch is the library's built-in device array (shapes needing more
+    than Q8_NOALLOC_SCRATCH_BYTES are rejected).  Calls that may overlap on the
+    GPU must not use it concurrently."""
+    N, K = q.shape
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=q.device)
+    d, _ = _desc(q, s, x, y)
+    st = lib().q8_gemm_skinny_noalloc(_p(q), _p(s), N, K, _p(x), d.ldx, M, _p(y), d.ldy,
+                                      _p(dev_status), _stream(stream))
+    _check(st, "q8_gemm_skinny_noalloc")
     return y
 
 

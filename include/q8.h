@@ -179,6 +179,30 @@ q8_status q8_gemm(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                   uint16_t *y, int64_t ldy,
                   uint32_t *dev_status, q8_stream_t stream);
 
+/*
+ * q8_gemm_skinny_noalloc -- q8_gemm_skinny for callers that cannot allocate
+ * device memory when they run the matmul (a fixed memory pool, a loop that
+ * must not enter the allocator, a host that passes only inputs and outputs).
+ * The source pages have no counterpart to this entry point; it exists for
+ * library users.
+ *   Arguments, layouts, accuracy and errors: as q8_gemm_skinny, with no
+ *   workspace argument.  The split-K scratch is a device array built into the
+ *   library of Q8_NOALLOC_SCRATCH_BYTES (4 MiB), held by every GPU that loads
+ *   the library until the process exits.  A shape whose scratch need
+ *   (q8_workspace_size(N, K, M)) exceeds it returns Q8_ERR_WORKSPACE before
+ *   any CUDA call.  Nothing is allocated or freed.
+ *   The first call on a device looks the array's device address up (once per
+ *   device, with that device current): make it outside any stream capture.
+ *   All calls on a device share the array: calls whose kernels may overlap on
+ *   the GPU (unordered streams) race on it; calls ordered on one stream do
+ *   not.  Each call clears the ticket words it needs before its kernel runs.
+ */
+#define Q8_NOALLOC_SCRATCH_BYTES (4u << 20)
+q8_status q8_gemm_skinny_noalloc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                                 const uint16_t *x, int64_t ldx, int32_t M,
+                                 float *y, int64_t ldy,
+                                 uint32_t *dev_status, q8_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *q8_status_str(q8_status st);
 
