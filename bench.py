@@ -340,6 +340,19 @@ def extra_rows(torch, q8, peak):
                 rows[f"{name}_M{M}_{vn}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
                                              "us": round(t * 1e6, 2), "GMAC/s": round(M * N * K / t / 1e9, 1)}
         del cps
+    # prefill-shaped GEMM on tcgen05 (compute-bound: report TFLOP/s)
+    peaks, _ = measured_peaks()
+    tpk = float(peaks.get("bf16_tflops", 1900.0))
+    M = synth.PREFILL_M
+    for (K, N) in synth.SWEEP_SHAPES:
+        q0, s0 = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, f"pf{K}.{N}")).to(dev))
+        x = torch.from_numpy(synth.activations(M, K, 0, f"pfx{K}").view(np.int16)).view(torch.bfloat16).to(dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        t = timed([lambda q0=q0, s0=s0, x=x, y=y: q8.q8_gemm(q0, s0, x, y)], reps=50)
+        tf = 2.0 * M * N * K / t / 1e12
+        rows[f"prefill_gemm_M{M}_K{K}_N{N}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / tpk, 4),
+                                                "us": round(t * 1e6, 2),
+                                                "GB/s": round(matmul_bytes(N, K, M, 2) / t / 1e9, 1)}
     torch.cuda.empty_cache()
     return rows
 

@@ -1,11 +1,363 @@
-// q8_gemm_tc.cu -- prefill-shaped Q8_0 W8A16 GEMM (M > 32) on tcgen05.
+// q8_gemm_tc.cu -- prefill-shaped Q8_0 W8A16 GEMM (M > 32) on the 5th
+// generation tensor cores (tcgen05, TMEM accumulators).
+//
+// Y[m][n] = sum_k x[m][k] * bf16(s[n][k/32] * q[n][k]), fp32 accumulation,
+// bf16 output.  "MODEL-BASELINE-RESULTS" (fak), ACT 4 (a batched prefill GEMM
+// reads each weight once for all tokens, which makes the op compute-bound) and
+// "Parity lane" item 2; the weight tile is dequantised to bf16 in shared
+// memory so the tensor cores see a plain bf16 x bf16 product.
+//
+// One CTA computes a 128 (m) x 128 (n) tile of Y over all of K, in k-tiles of
+// 64, through a kStages-deep ring of shared-memory stages:
+//   warp 0, lane 0  TMA producer: for each k-tile, the x tile (bf16, 128 rows
+//                   x 128 bytes, 128-byte swizzle = the tensor core's K-major
+//                   layout) and the raw code tile (int8, 128 rows x 64 bytes)
+//                   via cp.async.bulk.tensor, completion on full_tma.
+//   warp 1, lane 0  MMA issuer: 4 x tcgen05.mma.kind::f16 (M=128, N=128,
+//                   K=16) per k-tile into a 128-column fp32 TMEM accumulator;
+//                   tcgen05.commit releases the stage (empty) and, after the
+//                   last k-tile, signals acc_full.
+//   warps 4-7       dequantisers: code tile (shared) x block scale (shared,
+//                   loaded once per CTA) -> bf16(s*q) written in the swizzled
+//                   K-major layout, fence.proxy.async, arrive on full_w; then
+//                   the epilogue: tcgen05.ld of their 32 TMEM lanes each,
+//                   fp32 -> bf16, store Y.
+// All waits are bounded; on expiry the CTA reports Q8_DEV_TIMEOUT, stops
+// issuing work, lets its copies and MMAs drain (bounded) and frees its TMEM.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "q8_dev.cuh"
 #include "q8_internal.h"
 
 namespace q8 {
 
-q8_status launch_gemm_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const uint16_t *, int64_t,
-                         int32_t, uint16_t *, int64_t, uint32_t *, cudaStream_t) {
-    return Q8_ERR_UNSUPPORTED;
+namespace {
+
+constexpr int kBM = 128;          // rows of x / Y per tile (MMA M)
+constexpr int kBN = 128;          // weight rows per tile (MMA N)
+constexpr int kBK = 64;           // k per stage (128 bytes of bf16)
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kMaxScaleBytes = 48 * 1024;  // kBN * (K/32) * 2 -> K <= 6144
+constexpr int kTmemCols = kBN;             // fp32 accumulator columns
+
+struct __align__(1024) GemmSmem {
+    uint8_t x[kStages][kBM * 128];     // bf16 x tile, SW128 K-major
+    uint8_t w[kStages][kBN * 128];     // bf16 weight tile, SW128 K-major
+    uint8_t codes[kStages][kBN * 64];  // raw int8 code tile (row-major, 64 B rows)
+    uint8_t scales[kMaxScaleBytes];    // binary16 scales of the CTA's kBN rows, all K
+    uint64_t full_tma[kStages];
+    uint64_t full_w[kStages];
+    uint64_t empty[kStages];
+    uint64_t scales_full;
+    uint64_t acc_full;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+struct GemmParams {
+    CUtensorMap tm_x;      // bf16 [M][ldx], box {64, 128}, 128-byte swizzle
+    CUtensorMap tm_q;      // int8 [N][K],   box {64, 128}, no swizzle
+    const uint16_t *s;     // binary16 scales [N][K/32]
+    uint16_t *y;           // bf16 [M][ldy]
+    uint32_t *status;
+    int32_t M, N, K, nb;
+    int64_t ldy;
+};
+
+// ---- tcgen05 / TMA wrappers ---------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), leading offset unused for this layout.
+__device__ __forceinline__ uint64_t sw128_desc(const void *tile) {
+    const uint64_t addr = smem_addr(tile);
+    uint64_t d = 0;
+    d |= (addr & 0x3FFFFull) >> 4;          // start address
+    d |= static_cast<uint64_t>(1) << 16;    // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;    // descriptor version (sm_100 family)
+    d |= static_cast<uint64_t>(2) << 61;    // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A bf16, B bf16, both K-major,
+// N = kBN, M = kBM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(tmem_d), "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A bounded wait that also gives up at once when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(GemmSmem &sm, uint64_t *bar, uint32_t parity, uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int32_t *>(&sm.abort_flag)) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicExch(&sm.abort_flag, 1);
+            if (status) atomicOr(status, Q8_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // the tiles need 1024-byte alignment (128-byte swizzle atoms)
+    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int n0 = blockIdx.x * kBN;
+    const int m0 = blockIdx.y * kBM;
+    const int KT = (p.K + kBK - 1) / kBK;
+    const int rows_n = min(kBN, p.N - n0);
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full_tma[i], 1);
+            mbar_init(&sm.full_w[i], 4);
+            mbar_init(&sm.empty[i], 1);
+        }
+        mbar_init(&sm.scales_full, 1);
+        mbar_init(&sm.acc_full, 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_addr(&sm.tmem_base)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // -------------------------------------------------------- TMA producer
+        // scales of this CTA's rows, all K: contiguous in global memory
+        const uint32_t sbytes = static_cast<uint32_t>(rows_n) * static_cast<uint32_t>(p.nb) * 2u;
+        const uint32_t sb16 = sbytes & ~15u;
+        const uint8_t *ssrc = reinterpret_cast<const uint8_t *>(p.s + static_cast<int64_t>(n0) * p.nb);
+        for (uint32_t b = sb16; b < sbytes; b += 2)
+            *reinterpret_cast<uint16_t *>(sm.scales + b) = *reinterpret_cast<const uint16_t *>(ssrc + b);
+        mbar_arrive_expect_tx(&sm.scales_full, sb16);
+        if (sb16) bulk_g2s(sm.scales, ssrc, sb16, &sm.scales_full);
+        for (int kt = 0; kt < KT; ++kt) {
+            const int st = kt % kStages;
+            if (kt >= kStages && !wait_or_abort(sm, &sm.empty[st], ((kt / kStages) - 1) & 1, p.status)) break;
+            mbar_arrive_expect_tx(&sm.full_tma[st], kBM * 128 + kBN * 64);
+            tma_load_2d(sm.x[st], &p.tm_x, kt * kBK, m0, &sm.full_tma[st]);
+            tma_load_2d(sm.codes[st], &p.tm_q, kt * kBK, n0, &sm.full_tma[st]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        for (int kt = 0; kt < KT; ++kt) {
+            const int st = kt % kStages;
+            const uint32_t par = (kt / kStages) & 1;
+            if (!wait_or_abort(sm, &sm.full_tma[st], par, p.status)) break;
+            if (!wait_or_abort(sm, &sm.full_w[st], par, p.status)) break;
+            tc_fence_after();
+            const uint64_t da = sw128_desc(sm.x[st]);
+            const uint64_t db = sw128_desc(sm.w[st]);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                // advance 16 elements (32 bytes) along K inside the swizzled rows
+                umma_bf16(tmem, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2),
+                          (kt > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&sm.empty[st]);
+        }
+        umma_commit(&sm.acc_full);
+    } else if (warp >= 4) {
+        // ------------------------------------------------ dequantise, epilogue
+        const int t = tid - 128;  // 0..127
+        bool ok = wait_or_abort(sm, &sm.scales_full, 0, p.status);
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(sm.scales);
+        for (int kt = 0; ok && kt < KT; ++kt) {
+            const int st = kt % kStages;
+            if (!wait_or_abort(sm, &sm.full_tma[st], (kt / kStages) & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            // 128 rows x 4 chunks of 16 codes; task j -> row j/4, chunk j%4
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = t + 128 * i;
+                const int row = j >> 2;
+                const int c = j & 3;  // 16-code chunk within the 64-code k-tile
+                const int kb = kt * 2 + (c >> 1);  // block index along K
+                const uint4 w = *reinterpret_cast<const uint4 *>(sm.codes[st] + row * 64 + c * 16);
+                const float s = (row < rows_n && kb < p.nb) ? f16_bits_to_f32(sc[row * p.nb + kb]) : 0.f;
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                uint32_t out[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float f0, f1, f2, f3;
+                    codes4_to_f32(words[e], f0, f1, f2, f3);
+                    out[2 * e] = pack_bf16x2(f0 * s, f1 * s);
+                    out[2 * e + 1] = pack_bf16x2(f2 * s, f3 * s);
+                }
+                // logical 16-byte chunks 2c and 2c+1 of the row, swizzled by row % 8
+                uint8_t *wrow = sm.w[st] + row * 128;
+                *reinterpret_cast<uint4 *>(wrow + (((2 * c) ^ (row & 7)) << 4)) =
+                    make_uint4(out[0], out[1], out[2], out[3]);
+                *reinterpret_cast<uint4 *>(wrow + (((2 * c + 1) ^ (row & 7)) << 4)) =
+                    make_uint4(out[4], out[5], out[6], out[7]);
+            }
+            fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.full_w[st])) : "memory");
+        }
+        // epilogue: TMEM lanes 32*(warp%4) .. +31 hold rows m0 + 32*(warp%4) + lane
+        if (ok && wait_or_abort(sm, &sm.acc_full, 0, p.status)) {
+            tc_fence_after();
+            const int r = 32 * (warp & 3) + lane;
+            const int m = m0 + r;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(c0), v);
+                if (m < p.M) {
+                    uint16_t *yrow = p.y + static_cast<int64_t>(m) * p.ldy + n0 + c0;
+                    if (n0 + c0 + 32 <= p.N) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const uint4 o = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7])));
+                            *reinterpret_cast<uint4 *>(yrow + 8 * q4) = o;
+                        }
+                    } else {
+                        for (int e = 0; e < 32 && n0 + c0 + e < p.N; ++e) {
+                            const uint32_t h = pack_bf16x2(__uint_as_float(v[e]), 0.f);
+                            yrow[e] = static_cast<uint16_t>(h & 0xFFFFu);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    // If a role gave up, let in-flight copies and MMAs land (bounded) first.
+    if (tid == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort_flag)) {
+        for (int i = 0; i < kStages; ++i) {
+            (void)mbar_try_wait(&sm.full_tma[i], 0);
+        }
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+bool encode_maps(GemmParams &p, const int8_t *q, const uint16_t *x, int64_t N, int64_t K, int64_t M,
+                 int64_t ldx) {
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
+        const cuuint32_t box[2] = {kBK, kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (cuTensorMapEncodeTiled(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
+                                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+        const cuuint32_t box[2] = {kBK, kBN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (cuTensorMapEncodeTiled(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(q), dims, strides,
+                                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+int g_configured_dev = -1;
+
+}  // namespace
+
+q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
+                         int32_t M, uint16_t *y, int64_t ldy, uint32_t *dev_status, cudaStream_t stream) {
+    const int64_t nb = K / 32;
+    if (static_cast<int64_t>(kBN) * nb * 2 > kMaxScaleBytes) return Q8_ERR_UNSUPPORTED;  // K > 6144
+    const DeviceInfo *di = device_info();
+    if (!di) return Q8_ERR_CUDA;
+    const size_t smem = sizeof(GemmSmem) + 1024;  // + alignment slack
+    if (g_configured_dev != di->device) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return Q8_ERR_CUDA;
+        g_configured_dev = di->device;
+    }
+    GemmParams p;
+    if (!encode_maps(p, q, x, N, K, M, ldx)) return Q8_ERR_CUDA;
+    p.s = s;
+    p.y = y;
+    p.status = dev_status;
+    p.M = M;
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.nb = static_cast<int32_t>(nb);
+    p.ldy = ldy;
+    const dim3 grid(static_cast<unsigned>((N + kBN - 1) / kBN), static_cast<unsigned>((M + kBM - 1) / kBM));
+    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 
 }  // namespace q8
