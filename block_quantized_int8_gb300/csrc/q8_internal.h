@@ -47,6 +47,10 @@ size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *pla
 bool gemv_supported(const q8_linear_desc *descs, int count);
 q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_status, cudaStream_t stream);
 
+// 1 <= M <= 8 bulk-copy pipeline with warp MMA (q8_pipe.cu): K <= 4096.
+bool pipe_supported(const q8_linear_desc *descs, int count, int M);
+q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
+
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
 

@@ -387,8 +387,13 @@ q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int varia
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
+    // M = 1: the CUDA-core bulk-copy GEMV (AUTO, SIMT); M <= 8: the warp-MMA
+    // bulk-copy pipeline (AUTO for M >= 2, MMA for any M <= 8); otherwise the
+    // general tile kernel below
     if (M == 1 && variant != Q8_VARIANT_MMA && gemv_supported(descs, count))
         return launch_gemv(descs, count, dev_status, stream);
+    if (M <= 8 && variant != Q8_VARIANT_SIMT && pipe_supported(descs, count, M))
+        return launch_pipe(descs, count, M, dev_status, stream);
     SplitPlan plans[Q8_MAX_BATCH];
     const size_t need = plan_skinny(descs, count, M, plans);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;

@@ -10,7 +10,7 @@ from helpers import check_tol, dev, weights_dev, x_dev
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1, 2]  # Q8_VARIANT_SIMT, Q8_VARIANT_MMA
+VARIANTS = [0, 1, 2]  # Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA
 
 
 def run_batch(mats_np, M, variant, ws_extra=0):
@@ -224,10 +224,10 @@ def test_workspace_too_small_is_rejected(oracle):
     N, K = 1536, 4096
     q = torch.zeros((N, K), dtype=torch.int8, device="cuda")
     s = torch.zeros((N, K // 32), dtype=torch.float16, device="cuda")
-    x = torch.zeros((4, K), dtype=torch.bfloat16, device="cuda")
-    y = torch.empty((4, N), dtype=torch.float32, device="cuda")
-    need = q8.q8_workspace_size(N, K, 4)
-    assert need > 256   # M = 4 on this short-N, long-K shape splits K
+    x = torch.zeros((16, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((16, N), dtype=torch.float32, device="cuda")
+    need = q8.q8_workspace_size(N, K, 16)
+    assert need > 256   # M = 16 on this short-N, long-K shape splits K
     ws = q8.workspace(need - 256)
     with pytest.raises(q8.Q8Error) as e:
         q8.q8_gemm_skinny(q, s, x, y, ws=ws)
