@@ -173,11 +173,31 @@ class LayerSet:
         # activations: one vector per (pass, input width); bf16 bits
         self.x_host = {(p, K): synth.activations(1, K, seed, synth.layer_x_tag(p, K))
                        for p in range(synth.PASSES) for K in self.widths}
-        self.x = {key: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev)
-                  for key, v in self.x_host.items()}
-        self.y = [[{name: torch.empty((1, N), dtype=torch.float32, device=dev)
-                    for (name, K, N) in synth.LAYER_MATRICES} for _ in range(synth.LAYERS)]
-                  for _ in range(synth.PASSES)]
+        # all activations in one device buffer and all outputs in another, so an
+        # end-to-end step moves them with one copy each way
+        self.x_keys = sorted(self.x_host)
+        x_elems = sum(self.x_host[k].size for k in self.x_keys)
+        self.x_all = torch.empty(x_elems, dtype=torch.bfloat16, device=dev)
+        self.x = {}
+        off = 0
+        for key in self.x_keys:
+            v = self.x_host[key]
+            self.x[key] = self.x_all[off:off + v.size].view(1, -1)
+            self.x[key].view(torch.int16).copy_(torch.from_numpy(v.view(np.int16)).view(1, -1))
+            off += v.size
+        n_out = sum(N for (_, _, N) in synth.LAYER_MATRICES) * synth.LAYERS * synth.PASSES
+        self.y_all = torch.empty(n_out, dtype=torch.float32, device=dev)
+        self.y = []
+        off = 0
+        for _ in range(synth.PASSES):
+            per_pass = []
+            for _ in range(synth.LAYERS):
+                per_layer = {}
+                for (name, K, N) in synth.LAYER_MATRICES:
+                    per_layer[name] = self.y_all[off:off + N].view(1, N)
+                    off += N
+                per_pass.append(per_layer)
+            self.y.append(per_pass)
         self.descs = []
         ws_need = 0
         for p in range(synth.PASSES):
@@ -236,23 +256,18 @@ def per_launch_ms(torch, ls, reps, variant=0):
 
 
 def e2e_gbs(torch, ls, steps, bytes_per_step):
-    """Whole step through the public API with host buffers: pinned H2D of every
-    pass's activations, the 8 batch launches, D2H of every output, and a
-    host-side wait for the result, timed by the host clock."""
-    keys = sorted(ls.x_host)
-    xh = {k: torch.from_numpy(ls.x_host[k].view(np.int16)).pin_memory() for k in keys}
-    outs = [ls.y[p][l][n] for p in range(synth.PASSES) for l in range(synth.LAYERS)
-            for (n, _, _) in synth.LAYER_MATRICES]
-    yh = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    h2d = sum(v.numel() * 2 for v in xh.values())
-    d2h = sum(o.numel() * 4 for o in outs)
+    """Whole step through the public API with host buffers: one pinned H2D copy
+    of every pass's activations, the 8 batch launches, one D2H copy of every
+    output, and a host-side wait for the result, timed by the host clock."""
+    xh = torch.from_numpy(np.concatenate([ls.x_host[k].reshape(-1) for k in ls.x_keys]).view(np.int16)).pin_memory()
+    yh = torch.empty(ls.y_all.shape, dtype=ls.y_all.dtype, pin_memory=True)
+    h2d = xh.numel() * 2
+    d2h = yh.numel() * 4
 
     def one():
-        for k in keys:
-            ls.x[k].view(torch.int16).copy_(xh[k], non_blocking=True)
+        ls.x_all.view(torch.int16).copy_(xh, non_blocking=True)
         ls.step()
-        for o, h in zip(outs, yh):
-            h.copy_(o, non_blocking=True)
+        yh.copy_(ls.y_all, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(3):
@@ -339,6 +354,16 @@ def extra_rows(torch, q8, peak):
                 t = timed(fns, reps=3)
                 rows[f"{name}_M{M}_{vn}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
                                              "us": round(t * 1e6, 2), "GMAC/s": round(M * N * K / t / 1e9, 1)}
+            # steady state: the distinct copies as ONE batched launch (default kernels)
+            nb_ = min(len(cps), q8.Q8_MAX_BATCH)
+            ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(nb_)]
+            bd, _ = q8.make_descs([(cps[i][0], cps[i][1], x, ys[i]) for i in range(nb_)])
+            wsb = q8.workspace(q8.q8_linear_batch_workspace_size(bd, M), dev)
+            t = timed([lambda bd=bd, M=M, wsb=wsb: q8.q8_linear_batch(descs=bd, M=M, ws=wsb)], reps=5)
+            bb = by * nb_
+            rows[f"{name}_M{M}_batch{nb_}"] = {"GB/s": round(bb / t / 1e9, 1), "frac": round(bb / t / 1e9 / peak, 3),
+                                               "us": round(t * 1e6, 2), "GMAC/s": round(nb_ * M * N * K / t / 1e9, 1)}
+            del ys, wsb
         del cps
     # prefill-shaped GEMM on tcgen05 (compute-bound: report TFLOP/s)
     peaks, _ = measured_peaks()

@@ -122,10 +122,23 @@ struct RowPair {
     uint32_t hA[NJ], hB[NJ];
 };
 
-template <int NJ>
+// FULL: both rows exist and every lane has NJ chunks (the common case), so
+// the loads need no predicates and no zero fill.
+template <int NJ, bool FULL>
 __device__ __forceinline__ void load_rows(RowPair<NJ> &rp, const uint8_t *cA, const uint8_t *cB,
                                           const uint16_t *sA, const uint16_t *sB, bool vA, bool vB, int lane,
                                           int chunks_slice) {
+    if constexpr (FULL) {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int c = lane + 32 * j;
+            rp.wA[j] = *reinterpret_cast<const uint4 *>(cA + 16 * c);
+            rp.wB[j] = *reinterpret_cast<const uint4 *>(cB + 16 * c);
+            rp.hA[j] = sA[c >> 1];
+            rp.hB[j] = sB[c >> 1];
+        }
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int c = lane + 32 * j;
@@ -171,13 +184,13 @@ __device__ __forceinline__ void dot_rows(const RowPair<NJ> &rp, const unsigned l
 }
 
 // Load this warp's part of the stage, release the slot, then compute.
-template <int NJ, int KJ>
+template <int NJ, int KJ, bool FULL>
 __device__ __forceinline__ void stage_rows(const uint8_t *cA, const uint8_t *cB, const uint16_t *sA,
                                            const uint16_t *sB, bool vA, bool vB, int lane, int chunks_slice,
                                            const unsigned long long (&xr)[KJ][8], uint64_t *empty_bar,
                                            float &accA, float &accB) {
     RowPair<NJ> rp;
-    load_rows<NJ>(rp, cA, cB, sA, sB, vA, vB, lane, chunks_slice);
+    load_rows<NJ, FULL>(rp, cA, cB, sA, sB, vA, vB, lane, chunks_slice);
     // the arrive has release semantics: every lane's shared-memory reads above
     // are ordered before the producer may overwrite the slot
     __syncwarp();
@@ -316,11 +329,20 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
         const uint16_t *sA = scales + rA * D.nb + (k0 >> 5);
         const uint16_t *sB = scales + rB * D.nb + (k0 >> 5);
         float accA = 0.f, accB = 0.f;
-        switch (nj) {
-            case 1: stage_rows<1, KJ>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-            case 2: stage_rows<2, KJ>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-            case 3: if constexpr (KJ >= 3) stage_rows<3, KJ>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-            default: if constexpr (KJ >= 4) stage_rows<4, KJ>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+        if (vA && vB && chunks_slice == 32 * nj) {
+            switch (nj) {
+                case 1: stage_rows<1, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+                case 2: stage_rows<2, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+                case 3: if constexpr (KJ >= 3) stage_rows<3, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+                default: if constexpr (KJ >= 4) stage_rows<4, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+            }
+        } else {
+            switch (nj) {
+                case 1: stage_rows<1, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+                case 2: stage_rows<2, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+                case 3: if constexpr (KJ >= 3) stage_rows<3, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+                default: if constexpr (KJ >= 4) stage_rows<4, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+            }
         }
         // reduce both rows at once: after the first exchange lanes 0-15 carry
         // row A and lanes 16-31 row B, then a 4-step tree within each half
