@@ -20,10 +20,11 @@
 //    bank-conflict free) and x^T as B (columns = activation rows, zero past
 //    M).  Codes become bf16 exactly (|q| <= 127); each block's fp32 result is
 //    scaled by its binary16 scale.
-//  * The 8 partial sums of a row are added in warp order 0..7 by whichever
-//    warp finishes the stage last (shared-memory counter; nobody waits), so
-//    results are deterministic and independent of batching; that warp stores
-//    y and the slot is released after its reads.
+//  * With 8-row stages each warp copies its share into registers and releases
+//    the slot before any arithmetic.  The 8 partial sums of a row are added in
+//    warp order 0..7 by whichever warp finishes the stage last (shared-memory
+//    counter over a small ring; nobody waits), so results are deterministic
+//    and independent of batching.
 // Every wait is bounded (Q8_DEV_TIMEOUT on expiry).
 #include <algorithm>
 
@@ -43,6 +44,9 @@ constexpr int kSlotBytes = kCodeCap + kScaleCap;
 constexpr int kPipeMaxK = 4096;          // x fragments: at most 16 blocks per warp
 constexpr int kMaxBpw = 16;
 constexpr int kMaxGrid = 1024;
+// Partial-sum ring: a warp can run at most kStages stages ahead of the last
+// warp's combine, so kStages + 2 entries are never reused too early.
+constexpr int kRed = kStages + 2;
 
 struct PDesc {
     const int8_t *q;
@@ -71,8 +75,8 @@ struct PParams {
 
 struct PSmem {
     alignas(128) uint8_t slot[kStages][kSlotBytes];
-    float red[kStages][kWarps][32][4];  // per-warp partial D fragments of a stage
-    uint32_t cnt[kStages];
+    float red[kRed][kWarps][32][4];  // per-warp partial D fragments, ring over stages
+    uint32_t cnt[kRed];
     uint64_t full[kStages];
     uint64_t empty[kStages];
 };
@@ -92,36 +96,99 @@ __device__ __forceinline__ int find_pdesc(const PParams &p, int stage) {
     return d;
 }
 
-// One warp's part of a stage: BPW blocks (the last ones masked by kb < kb1).
-template <int BPW>
-__device__ __forceinline__ void stage_mma(const uint8_t *codes, const uint16_t *scales, int RS, int nb, int kb0,
-                                          int kb1, int g, int t, bool two_groups, const uint4 (&xr)[kMaxBpw],
-                                          float (&acc)[4]) {
+// One warp's part of a stage in registers: BPW blocks (the last ones masked
+// by kb < kb1) of rows g and g+8, with their scales.
+// TWO: the stage has 16 rows (a second row group g+8); with 8-row stages the
+// upper half of the A operand is zero and needs no registers.
+template <int BPW, bool TWO>
+struct PFrag {
+    uint2 cg[BPW];
+    uint32_t sg[BPW];
+    uint2 ch[TWO ? BPW : 1];
+    uint32_t sh[TWO ? BPW : 1];
+};
+
+template <int BPW, bool TWO>
+__device__ __forceinline__ void load_frag(PFrag<BPW, TWO> &f, const uint8_t *codes, const uint16_t *scales, int RS,
+                                          int nb, int kb0, int kb1, int g, int t) {
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
         const int kb = kb0 + j;
+        f.cg[j] = make_uint2(0u, 0u);
+        f.sg[j] = 0u;
+        if constexpr (TWO) {
+            f.ch[j] = f.cg[j];
+            f.sh[j] = 0u;
+        }
         if (kb < kb1) {
-            const uint2 cg = *reinterpret_cast<const uint2 *>(codes + g * RS + kb * 32 + 8 * t);
-            uint2 ch = make_uint2(0u, 0u);
-            float sh = 0.f;
-            if (two_groups) {
-                ch = *reinterpret_cast<const uint2 *>(codes + (g + 8) * RS + kb * 32 + 8 * t);
-                sh = f16_bits_to_f32(scales[(g + 8) * nb + kb]);
+            f.cg[j] = *reinterpret_cast<const uint2 *>(codes + g * RS + kb * 32 + 8 * t);
+            f.sg[j] = scales[g * nb + kb];
+            if constexpr (TWO) {
+                f.ch[j] = *reinterpret_cast<const uint2 *>(codes + (g + 8) * RS + kb * 32 + 8 * t);
+                f.sh[j] = scales[(g + 8) * nb + kb];
             }
-            const float sg = f16_bits_to_f32(scales[g * nb + kb]);
-            uint32_t g01, g23, g45, g67, h01, h23, h45, h67;
-            codes4_to_bf16x2(cg.x, g01, g23);
-            codes4_to_bf16x2(cg.y, g45, g67);
-            codes4_to_bf16x2(ch.x, h01, h23);
-            codes4_to_bf16x2(ch.y, h45, h67);
-            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-            mma_bf16_16816(d0, d1, d2, d3, g01, h01, g23, h23, xr[j].x, xr[j].y);
-            mma_bf16_16816(d0, d1, d2, d3, g45, h45, g67, h67, xr[j].z, xr[j].w);
-            acc[0] = fmaf(sg, d0, acc[0]);
-            acc[1] = fmaf(sg, d1, acc[1]);
+        }
+    }
+}
+
+template <int BPW, bool TWO>
+__device__ __forceinline__ void mma_frag(const PFrag<BPW, TWO> &f, const uint4 (&xr)[kMaxBpw], float (&acc)[4]) {
+#pragma unroll
+    for (int j = 0; j < BPW; ++j) {
+        uint32_t g01, g23, g45, g67, h01 = 0u, h23 = 0u, h45 = 0u, h67 = 0u;
+        codes4_to_bf16x2(f.cg[j].x, g01, g23);
+        codes4_to_bf16x2(f.cg[j].y, g45, g67);
+        if constexpr (TWO) {
+            codes4_to_bf16x2(f.ch[j].x, h01, h23);
+            codes4_to_bf16x2(f.ch[j].y, h45, h67);
+        }
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        mma_bf16_16816(d0, d1, d2, d3, g01, h01, g23, h23, xr[j].x, xr[j].y);
+        mma_bf16_16816(d0, d1, d2, d3, g45, h45, g67, h67, xr[j].z, xr[j].w);
+        const float sg = f16_bits_to_f32(f.sg[j]);
+        acc[0] = fmaf(sg, d0, acc[0]);
+        acc[1] = fmaf(sg, d1, acc[1]);
+        if constexpr (TWO) {
+            const float sh = f16_bits_to_f32(f.sh[j]);
             acc[2] = fmaf(sh, d2, acc[2]);
             acc[3] = fmaf(sh, d3, acc[3]);
         }
+    }
+}
+
+// 8-row stages (TWO false): copy this warp's share of the stage into
+// registers, hand the slot back to the producer (the release orders every
+// lane's reads before any refill), then do the arithmetic.  16-row stages
+// hold twice the registers, so they compute block by block straight from
+// shared memory and release the slot afterwards.
+template <int BPW, bool TWO>
+__device__ __forceinline__ void stage_mma(const uint8_t *codes, const uint16_t *scales, int RS, int nb, int kb0,
+                                          int kb1, int g, int t, const uint4 (&xr)[kMaxBpw],
+                                          uint64_t *empty_bar, int lane, float (&acc)[4]) {
+    if constexpr (TWO) {
+#pragma unroll
+        for (int j = 0; j < BPW; ++j) {
+            const int kb = kb0 + j;
+            if (kb < kb1) {
+                PFrag<1, true> f;
+                f.cg[0] = *reinterpret_cast<const uint2 *>(codes + g * RS + kb * 32 + 8 * t);
+                f.ch[0] = *reinterpret_cast<const uint2 *>(codes + (g + 8) * RS + kb * 32 + 8 * t);
+                f.sg[0] = scales[g * nb + kb];
+                f.sh[0] = scales[(g + 8) * nb + kb];
+                const uint4 xj[kMaxBpw] = {xr[j]};
+                mma_frag<1, true>(f, xj, acc);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
+    } else {
+        PFrag<BPW, TWO> f;
+        load_frag<BPW, TWO>(f, codes, scales, RS, nb, kb0, kb1, g, t);
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
+        mma_frag<BPW, TWO>(f, xr, acc);
     }
 }
 
@@ -141,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], kWarps);
-            sm.cnt[i] = 0u;
         }
+        for (int i = 0; i < kRed; ++i) sm.cnt[i] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
@@ -231,26 +298,33 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         const bool two = D.RT == 16;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const int bpw = D.bpw;
-        if (bpw <= 2) stage_mma<2>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, two, xr, acc);
-        else if (bpw <= 4) stage_mma<4>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, two, xr, acc);
-        else if (bpw <= 6) stage_mma<6>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, two, xr, acc);
-        else if (bpw <= 8) stage_mma<8>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, two, xr, acc);
-        else if (bpw <= 12) stage_mma<12>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, two, xr, acc);
-        else stage_mma<16>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, two, xr, acc);
+        uint64_t *eb = &sm.empty[slot];
+        // 16-row stages have K <= 2048 (bpw <= 8); 8-row stages have K > 1984 (bpw >= 8)
+        if (two) {
+            if (bpw <= 2) stage_mma<2, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            else if (bpw <= 4) stage_mma<4, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            else if (bpw <= 6) stage_mma<6, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            else stage_mma<8, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+        } else {
+            if (bpw <= 8) stage_mma<8, false>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            else if (bpw <= 12) stage_mma<12, false>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            else stage_mma<16, false>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+        }
+        const int rs = k % kRed;
 
         // publish this warp's partials; the last warp adds all 8 in warp order
-        *reinterpret_cast<float4 *>(&sm.red[slot][warp][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(&sm.red[rs][warp][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __threadfence_block();
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(&sm.cnt[slot], 1u);
+        if (lane == 0) prev = atomicAdd(&sm.cnt[rs], 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == kWarps - 1) {
             __threadfence_block();
-            float4 v = *reinterpret_cast<const float4 *>(&sm.red[slot][0][lane][0]);
+            float4 v = *reinterpret_cast<const float4 *>(&sm.red[rs][0][lane][0]);
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) {
-                const float4 u = *reinterpret_cast<const float4 *>(&sm.red[slot][w][lane][0]);
+                const float4 u = *reinterpret_cast<const float4 *>(&sm.red[rs][w][lane][0]);
                 v.x += u.x;
                 v.y += u.y;
                 v.z += u.z;
@@ -267,11 +341,8 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
                 if (m0 < M) D.y[m0 * D.ldy + nh] = v.z;
                 if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + nh] = v.w;
             }
-            if (lane == 0) sm.cnt[slot] = 0u;
+            if (lane == 0) sm.cnt[rs] = 0u;
         }
-        __syncwarp();
-        if (lane == 0)
-            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.empty[slot])) : "memory");
     }
 }
 
