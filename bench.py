@@ -477,6 +477,14 @@ def profile_case(torch, q8, args):
         ls = LayerSet(torch, q8)
         for i in range(args.warmup + 3):
             q8.q8_linear_batch(descs=ls.descs[i % synth.PASSES], M=1, ws=ls.ws, variant=args.variant)
+    elif args.profile == "prefill":
+        K, N = synth.SWEEP_SHAPES[0]
+        M = synth.PREFILL_M
+        q0, s0 = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, f"pf{K}.{N}")).cuda())
+        x = torch.from_numpy(synth.activations(M, K, 0, f"pfx{K}").view(np.int16)).view(torch.bfloat16).cuda()
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup + 3):
+            q8.q8_gemm(q0, s0, x, y)
     else:
         N, K = synth.VOCAB, synth.HIDDEN
         wq, ws_ = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, "vocab")).cuda())
@@ -499,7 +507,7 @@ def main():
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 SIMT, 2 MMA")
     ap.add_argument("--no-rows", action="store_true", help="skip the context rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--profile", choices=["layerset", "vocab"], default=None,
+    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill"], default=None,
                     help="run a few launches of one workload and exit (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -17,11 +17,11 @@
 //                   K=16) per k-tile into a 128-column fp32 TMEM accumulator;
 //                   tcgen05.commit releases the stage (empty) and, after the
 //                   last k-tile, signals acc_full.
-//   warps 4-7       dequantisers: code tile (shared) x block scale (shared,
+//   warps 4-11      dequantisers: code tile (shared) x block scale (shared,
 //                   loaded once per CTA) -> bf16(s*q) written in the swizzled
 //                   K-major layout, fence.proxy.async, arrive on full_w; then
-//                   the epilogue: tcgen05.ld of their 32 TMEM lanes each,
-//                   fp32 -> bf16, store Y.
+//                   the epilogue: tcgen05.ld of their 32 TMEM lanes (warp % 4)
+//                   and half of the columns each, fp32 -> bf16, store Y.
 // All waits are bounded; on expiry the CTA reports Q8_DEV_TIMEOUT, stops
 // issuing work, lets its copies and MMAs drain (bounded) and frees its TMEM.
 #include <cuda.h>
@@ -39,15 +39,21 @@ constexpr int kBM = 128;          // rows of x / Y per tile (MMA M)
 constexpr int kBN = 128;          // weight rows per tile (MMA N)
 constexpr int kBK = 64;           // k per stage (128 bytes of bf16)
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;           // warps 0-1 roles, 2-3 idle, 4-11 dequantise + epilogue
+constexpr int kDeqThreads = 256;
 constexpr int kMaxScaleBytes = 48 * 1024;  // kBN * (K/32) * 2 -> K <= 6144
 constexpr int kTmemCols = kBN;             // fp32 accumulator columns
+constexpr size_t kTwoCtaSmem = 115712;      // (228 KB - 2 x 1 KB reserved) / 2
 
-struct __align__(1024) GemmSmem {
-    uint8_t x[kStages][kBM * 128];     // bf16 x tile, SW128 K-major
-    uint8_t w[kStages][kBN * 128];     // bf16 weight tile, SW128 K-major
-    uint8_t codes[kStages][kBN * 64];  // raw int8 code tile (row-major, 64 B rows)
-    uint8_t scales[kMaxScaleBytes];    // binary16 scales of the CTA's kBN rows, all K
+constexpr int kXBytes = kBM * 128;
+constexpr int kWBytes = kBN * 128;
+constexpr int kCBytes = kBN * 64;
+constexpr int kStageBytes = kXBytes + kWBytes + kCBytes;
+
+// Shared memory: [x tiles][w tiles][code tiles] for S stages (S chosen at
+// launch: 2 when two CTAs fit on an SM, else kStages), then the scales, then
+// this control block.  Tiles start on 1024-byte boundaries.
+struct GemmCtl {
     uint64_t full_tma[kStages];
     uint64_t full_w[kStages];
     uint64_t empty[kStages];
@@ -57,6 +63,15 @@ struct __align__(1024) GemmSmem {
     int32_t abort_flag;
 };
 
+struct GemmSmem {
+    uint8_t *base;
+    int S;
+    __device__ __forceinline__ uint8_t *x(int s) const { return base + s * kXBytes; }
+    __device__ __forceinline__ uint8_t *w(int s) const { return base + S * kXBytes + s * kWBytes; }
+    __device__ __forceinline__ uint8_t *codes(int s) const { return base + S * (kXBytes + kWBytes) + s * kCBytes; }
+    __device__ __forceinline__ uint8_t *scales() const { return base + S * kStageBytes; }
+};
+
 struct GemmParams {
     CUtensorMap tm_x;      // bf16 [M][ldx], box {64, 128}, 128-byte swizzle
     CUtensorMap tm_q;      // int8 [N][K],   box {64, 128}, no swizzle
@@ -64,6 +79,8 @@ struct GemmParams {
     uint16_t *y;           // bf16 [M][ldy]
     uint32_t *status;
     int32_t M, N, K, nb;
+    int32_t S;             // pipeline stages
+    int32_t ctl_off;       // byte offset of the control block from the aligned base
     int64_t ldy;
 };
 
@@ -127,7 +144,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // A bounded wait that also gives up at once when another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(GemmSmem &sm, uint64_t *bar, uint32_t parity, uint32_t *status) {
+__device__ __forceinline__ bool wait_or_abort(GemmCtl &sm, uint64_t *bar, uint32_t parity, uint32_t *status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -141,11 +158,14 @@ __device__ __forceinline__ bool wait_or_abort(GemmSmem &sm, uint64_t *bar, uint3
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // the tiles need 1024-byte alignment (128-byte swizzle atoms)
-    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(
+    uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const GemmSmem L{base, p.S};
+    GemmCtl &sm = *reinterpret_cast<GemmCtl *>(base + p.ctl_off);
+    const int S = p.S;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -155,9 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int rows_n = min(kBN, p.N - n0);
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(&sm.full_tma[i], 1);
-            mbar_init(&sm.full_w[i], 4);
+            mbar_init(&sm.full_w[i], kDeqThreads / 32);
             mbar_init(&sm.empty[i], 1);
         }
         mbar_init(&sm.scales_full, 1);
@@ -182,26 +202,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const uint32_t sb16 = sbytes & ~15u;
         const uint8_t *ssrc = reinterpret_cast<const uint8_t *>(p.s + static_cast<int64_t>(n0) * p.nb);
         for (uint32_t b = sb16; b < sbytes; b += 2)
-            *reinterpret_cast<uint16_t *>(sm.scales + b) = *reinterpret_cast<const uint16_t *>(ssrc + b);
+            *reinterpret_cast<uint16_t *>(L.scales() + b) = *reinterpret_cast<const uint16_t *>(ssrc + b);
         mbar_arrive_expect_tx(&sm.scales_full, sb16);
-        if (sb16) bulk_g2s(sm.scales, ssrc, sb16, &sm.scales_full);
+        if (sb16) bulk_g2s(L.scales(), ssrc, sb16, &sm.scales_full);
         for (int kt = 0; kt < KT; ++kt) {
-            const int st = kt % kStages;
-            if (kt >= kStages && !wait_or_abort(sm, &sm.empty[st], ((kt / kStages) - 1) & 1, p.status)) break;
+            const int st = kt % S;
+            if (kt >= S && !wait_or_abort(sm, &sm.empty[st], ((kt / S) - 1) & 1, p.status)) break;
             mbar_arrive_expect_tx(&sm.full_tma[st], kBM * 128 + kBN * 64);
-            tma_load_2d(sm.x[st], &p.tm_x, kt * kBK, m0, &sm.full_tma[st]);
-            tma_load_2d(sm.codes[st], &p.tm_q, kt * kBK, n0, &sm.full_tma[st]);
+            tma_load_2d(L.x(st), &p.tm_x, kt * kBK, m0, &sm.full_tma[st]);
+            tma_load_2d(L.codes(st), &p.tm_q, kt * kBK, n0, &sm.full_tma[st]);
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------- MMA issuer
         for (int kt = 0; kt < KT; ++kt) {
-            const int st = kt % kStages;
-            const uint32_t par = (kt / kStages) & 1;
+            const int st = kt % S;
+            const uint32_t par = (kt / S) & 1;
             if (!wait_or_abort(sm, &sm.full_tma[st], par, p.status)) break;
             if (!wait_or_abort(sm, &sm.full_w[st], par, p.status)) break;
             tc_fence_after();
-            const uint64_t da = sw128_desc(sm.x[st]);
-            const uint64_t db = sw128_desc(sm.w[st]);
+            const uint64_t da = sw128_desc(L.x(st));
+            const uint64_t db = sw128_desc(L.w(st));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
                 // advance 16 elements (32 bytes) along K inside the swizzled rows
@@ -213,23 +233,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         umma_commit(&sm.acc_full);
     } else if (warp >= 4) {
         // ------------------------------------------------ dequantise, epilogue
-        const int t = tid - 128;  // 0..127
+        const int t = tid - 128;  // 0..255
         bool ok = wait_or_abort(sm, &sm.scales_full, 0, p.status);
-        const uint16_t *sc = reinterpret_cast<const uint16_t *>(sm.scales);
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(L.scales());
         for (int kt = 0; ok && kt < KT; ++kt) {
-            const int st = kt % kStages;
-            if (!wait_or_abort(sm, &sm.full_tma[st], (kt / kStages) & 1, p.status)) {
+            const int st = kt % S;
+            if (!wait_or_abort(sm, &sm.full_tma[st], (kt / S) & 1, p.status)) {
                 ok = false;
                 break;
             }
             // 128 rows x 4 chunks of 16 codes; task j -> row j/4, chunk j%4
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = t + 128 * i;
+            for (int i = 0; i < 2; ++i) {
+                const int j = t + kDeqThreads * i;
                 const int row = j >> 2;
                 const int c = j & 3;  // 16-code chunk within the 64-code k-tile
                 const int kb = kt * 2 + (c >> 1);  // block index along K
-                const uint4 w = *reinterpret_cast<const uint4 *>(sm.codes[st] + row * 64 + c * 16);
+                const uint4 w = *reinterpret_cast<const uint4 *>(L.codes(st) + row * 64 + c * 16);
                 const float s = (row < rows_n && kb < p.nb) ? f16_bits_to_f32(sc[row * p.nb + kb]) : 0.f;
                 const uint32_t words[4] = {w.x, w.y, w.z, w.w};
                 uint32_t out[8];
@@ -241,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     out[2 * e + 1] = pack_bf16x2(f2 * s, f3 * s);
                 }
                 // logical 16-byte chunks 2c and 2c+1 of the row, swizzled by row % 8
-                uint8_t *wrow = sm.w[st] + row * 128;
+                uint8_t *wrow = L.w(st) + row * 128;
                 *reinterpret_cast<uint4 *>(wrow + (((2 * c) ^ (row & 7)) << 4)) =
                     make_uint4(out[0], out[1], out[2], out[3]);
                 *reinterpret_cast<uint4 *>(wrow + (((2 * c + 1) ^ (row & 7)) << 4)) =
@@ -251,13 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.full_w[st])) : "memory");
         }
-        // epilogue: TMEM lanes 32*(warp%4) .. +31 hold rows m0 + 32*(warp%4) + lane
+        // epilogue: TMEM lanes 32*(warp%4) .. +31 hold rows m0 + 32*(warp%4) + lane;
+        // warps 4-7 drain columns [0, 64), warps 8-11 columns [64, 128)
         if (ok && wait_or_abort(sm, &sm.acc_full, 0, p.status)) {
             tc_fence_after();
             const int r = 32 * (warp & 3) + lane;
             const int m = m0 + r;
+            const int cbeg = warp < 8 ? 0 : kBN / 2;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kBN; c0 += 32) {
+            for (int c0 = cbeg; c0 < cbeg + kBN / 2; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(c0), v);
                 if (m < p.M) {
@@ -286,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // ------------------------------------------------------------- teardown
     // If a role gave up, let in-flight copies and MMAs land (bounded) first.
     if (tid == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort_flag)) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < S; ++i) {
             (void)mbar_try_wait(&sm.full_tma[i], 0);
         }
         const uint64_t t0 = globaltimer_ns();
@@ -338,10 +360,20 @@ q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t 
     if (static_cast<int64_t>(kBN) * nb * 2 > kMaxScaleBytes) return Q8_ERR_UNSUPPORTED;  // K > 6144
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
-    const size_t smem = sizeof(GemmSmem) + 1024;  // + alignment slack
+    // two CTAs per SM (2 stages each) when they fit, so one CTA's prologue and
+    // epilogue overlap the other's main loop; else one CTA with kStages stages
+    const int scale_bytes = static_cast<int>((static_cast<int64_t>(kBN) * nb * 2 + 1023) / 1024 * 1024);
+    auto smem_for = [&](int S) {
+        return static_cast<size_t>(1008 + S * kStageBytes + scale_bytes) + sizeof(GemmCtl);
+    };
+    int S = 2;
+    if (smem_for(2) > kTwoCtaSmem) S = kStages;
+    const size_t smem = smem_for(S);
     if (g_configured_dev != di->device) {
+        // the largest layout any supported K can need
+        const size_t smem_max = 1008 + static_cast<size_t>(kStages) * kStageBytes + kMaxScaleBytes + sizeof(GemmCtl);
         if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
+                                 static_cast<int>(smem_max)) != cudaSuccess)
             return Q8_ERR_CUDA;
         g_configured_dev = di->device;
     }
@@ -355,6 +387,8 @@ q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t 
     p.K = static_cast<int32_t>(K);
     p.nb = static_cast<int32_t>(nb);
     p.ldy = ldy;
+    p.S = S;
+    p.ctl_off = S * kStageBytes + scale_bytes;
     const dim3 grid(static_cast<unsigned>((N + kBN - 1) / kBN), static_cast<unsigned>((M + kBM - 1) / kBM));
     gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
