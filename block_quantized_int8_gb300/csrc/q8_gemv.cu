@@ -119,7 +119,7 @@ __device__ __forceinline__ unsigned long long dot4(uint32_t w, unsigned long lon
 template <int NJ>
 struct RowPair {
     uint4 wA[NJ], wB[NJ];
-    uint32_t hA[NJ], hB[NJ];
+    uint32_t h[NJ];  // binary16 scale bits: row A low half, row B high half
 };
 
 // FULL: both rows exist and every lane has NJ chunks (the common case), so
@@ -134,8 +134,7 @@ __device__ __forceinline__ void load_rows(RowPair<NJ> &rp, const uint8_t *cA, co
             const int c = lane + 32 * j;
             rp.wA[j] = *reinterpret_cast<const uint4 *>(cA + 16 * c);
             rp.wB[j] = *reinterpret_cast<const uint4 *>(cB + 16 * c);
-            rp.hA[j] = sA[c >> 1];
-            rp.hB[j] = sB[c >> 1];
+            rp.h[j] = static_cast<uint32_t>(sA[c >> 1]) | (static_cast<uint32_t>(sB[c >> 1]) << 16);
         }
         return;
     }
@@ -145,14 +144,14 @@ __device__ __forceinline__ void load_rows(RowPair<NJ> &rp, const uint8_t *cA, co
         const bool in = c < chunks_slice;
         rp.wA[j] = make_uint4(0u, 0u, 0u, 0u);
         rp.wB[j] = rp.wA[j];
-        rp.hA[j] = rp.hB[j] = 0u;
+        rp.h[j] = 0u;
         if (in && vA) {
             rp.wA[j] = *reinterpret_cast<const uint4 *>(cA + 16 * c);
-            rp.hA[j] = sA[c >> 1];
+            rp.h[j] = sA[c >> 1];
         }
         if (in && vB) {
             rp.wB[j] = *reinterpret_cast<const uint4 *>(cB + 16 * c);
-            rp.hB[j] = sB[c >> 1];
+            rp.h[j] |= static_cast<uint32_t>(sB[c >> 1]) << 16;
         }
     }
 }
@@ -176,10 +175,10 @@ __device__ __forceinline__ void dot_rows(const RowPair<NJ> &rp, const unsigned l
         b1 = dot4(rp.wB[j].w, xr[j][6], xr[j][7], b1);
         const unsigned long long a = add_f32x2(a0, a1);
         const unsigned long long b = add_f32x2(b0, b1);
-        accA = fmaf(f16_bits_to_f32(rp.hA[j]), __uint_as_float(static_cast<uint32_t>(a)) +
-                                                  __uint_as_float(static_cast<uint32_t>(a >> 32)), accA);
-        accB = fmaf(f16_bits_to_f32(rp.hB[j]), __uint_as_float(static_cast<uint32_t>(b)) +
-                                                  __uint_as_float(static_cast<uint32_t>(b >> 32)), accB);
+        accA = fmaf(f16_bits_to_f32(rp.h[j] & 0xFFFFu), __uint_as_float(static_cast<uint32_t>(a)) +
+                                                           __uint_as_float(static_cast<uint32_t>(a >> 32)), accA);
+        accB = fmaf(f16_bits_to_f32(rp.h[j] >> 16), __uint_as_float(static_cast<uint32_t>(b)) +
+                                                       __uint_as_float(static_cast<uint32_t>(b >> 32)), accB);
     }
 }
 
