@@ -18,9 +18,11 @@
 //    CTA is 8 warps, so two CTAs fit on an SM without capping registers
 //    (a ninth warp would put five warps on one SM sub-partition).
 //  * All 8 warps consume; each copies its share of a stage into registers and
-//    releases the slot before doing any arithmetic.  A row is split into P = pow2(ceil(K/2048))
-//    K-slices; each warp always owns the same slice (w % P), so its part of x
-//    stays in registers as fp32 (at most 64 values per lane), reloaded only
+//    releases the slot before doing any arithmetic.  A row is split into
+//    P = pow2(ceil(K/1536)) K-slices and a stage holds the most rows that fit
+//    48 KB in groups of 16/P, so a stage is a whole number (>= 2) of row pairs
+//    for every warp: the units (row, slice) warp + 8j, j = 0, 1, ...  Each warp always owns the same slice (w % P), so its part of x
+//    stays in registers as fp32 (at most 48 values per lane), reloaded only
 //    when the matrix changes.  Lanes read 16-byte chunks of the row from
 //    shared memory (consecutive lanes, consecutive chunks: no bank
 //    conflicts), turn codes into floats exactly (2^23 + byte trick) and use
@@ -42,14 +44,16 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = kConsumerWarps * 32;
-constexpr int kStages = 3;
-constexpr int kUnits = 16;                     // (row, slice) units per stage = RT * P
-constexpr int kCodeBytes = 32768;              // RT * K <= 32 KB per stage
+constexpr int kStages = 2;
+constexpr int kSliceK = 1536;                  // widest K slice of one warp
+constexpr int kCodeBytes = 32 * kSliceK;       // RT * K <= 48 KB per stage
+constexpr int kRedRows = 32;                   // rows per stage when P > 1 (at most 24)
+constexpr int kMaxPairs = 4;                   // row pairs per warp per stage: RT * P <= 64
 constexpr int kScaleBytes = kCodeBytes / 16 + 16;  // RT * K / 16, plus up to 14 bytes of alignment offset
 constexpr int kStageBytes = kCodeBytes + kScaleBytes;
-constexpr int kMaxK = 8 * 2048;                // P <= 8 with 2048-wide slices
+constexpr int kMaxK = 8 * kSliceK;             // P <= 8
 constexpr int kMaxGrid = 1024;
-constexpr int kJMax = 4;                       // 16-code chunks per lane per slice (2048 k)
+constexpr int kJMax = 3;                       // 16-code chunks per lane per slice (1536 k)
 
 struct GDesc {
     const int8_t *q;
@@ -60,7 +64,8 @@ struct GDesc {
     int32_t K;
     int32_t nb;          // K / 32
     int32_t P;           // slices per row (power of two <= 8)
-    int32_t RT;          // rows per stage = min(16 / P, 24576 / K)
+    int32_t lp;          // log2(P)
+    int32_t RT;          // rows per stage: a multiple of 16 / P, RT * K <= 48 KB
     int32_t bps;         // blocks per slice
     int32_t stage_begin; // first global stage index of this matrix
     int32_t stages;      // ceil(N / RT)
@@ -76,8 +81,8 @@ struct GParams {
 
 struct Smem {
     alignas(128) uint8_t stage[kStages][kStageBytes];
-    float red[2 * kStages][kUnits][8];   // per-stage slice sums (P > 1), ring of 2*kStages
-    uint32_t cnt[2 * kStages][kUnits];
+    float red[2 * kStages][kRedRows][8];   // per-stage slice sums (P > 1), ring of 2*kStages
+    uint32_t cnt[2 * kStages][kRedRows];
     uint64_t full[kStages];
     uint64_t empty[kStages];
 };
@@ -136,22 +141,21 @@ __device__ __forceinline__ void load_rows(RowPair<NJ> &rp, const uint8_t *cA, co
             rp.wB[j] = *reinterpret_cast<const uint4 *>(cB + 16 * c);
             rp.h[j] = static_cast<uint32_t>(sA[c >> 1]) | (static_cast<uint32_t>(sB[c >> 1]) << 16);
         }
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int c = lane + 32 * j;
-        const bool in = c < chunks_slice;
-        rp.wA[j] = make_uint4(0u, 0u, 0u, 0u);
-        rp.wB[j] = rp.wA[j];
-        rp.h[j] = 0u;
-        if (in && vA) {
-            rp.wA[j] = *reinterpret_cast<const uint4 *>(cA + 16 * c);
-            rp.h[j] = sA[c >> 1];
-        }
-        if (in && vB) {
-            rp.wB[j] = *reinterpret_cast<const uint4 *>(cB + 16 * c);
-            rp.h[j] |= static_cast<uint32_t>(sB[c >> 1]) << 16;
+        for (int j = 0; j < NJ; ++j) {
+            const int c = lane + 32 * j;
+            rp.wA[j] = make_uint4(0u, 0u, 0u, 0u);
+            rp.wB[j] = rp.wA[j];
+            rp.h[j] = 0u;
+            if (c < chunks_slice && vA) {
+                rp.wA[j] = *reinterpret_cast<const uint4 *>(cA + 16 * c);
+                rp.h[j] = sA[c >> 1];
+            }
+            if (c < chunks_slice && vB) {
+                rp.wB[j] = *reinterpret_cast<const uint4 *>(cB + 16 * c);
+                rp.h[j] |= static_cast<uint32_t>(sB[c >> 1]) << 16;
+            }
         }
     }
 }
@@ -163,6 +167,7 @@ __device__ __forceinline__ void load_rows(RowPair<NJ> &rp, const uint8_t *cA, co
 template <int NJ, int KJ>
 __device__ __forceinline__ void dot_rows(const RowPair<NJ> &rp, const unsigned long long (&xr)[KJ][8],
                                          float &accA, float &accB) {
+    static_assert(NJ <= KJ, "x chunk out of range");
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         unsigned long long a0 = dot4(rp.wA[j].x, xr[j][0], xr[j][1], 0ull);
@@ -182,7 +187,8 @@ __device__ __forceinline__ void dot_rows(const RowPair<NJ> &rp, const unsigned l
     }
 }
 
-// Load this warp's part of the stage, release the slot, then compute.
+// Load a row pair of the stage into registers, release the slot if this is
+// the warp's last pair of the stage (empty_bar != nullptr), then compute.
 template <int NJ, int KJ, bool FULL>
 __device__ __forceinline__ void stage_rows(const uint8_t *cA, const uint8_t *cB, const uint16_t *sA,
                                            const uint16_t *sB, bool vA, bool vB, int lane, int chunks_slice,
@@ -190,13 +196,97 @@ __device__ __forceinline__ void stage_rows(const uint8_t *cA, const uint8_t *cB,
                                            float &accA, float &accB) {
     RowPair<NJ> rp;
     load_rows<NJ, FULL>(rp, cA, cB, sA, sB, vA, vB, lane, chunks_slice);
-    // the arrive has release semantics: every lane's shared-memory reads above
-    // are ordered before the producer may overwrite the slot
-    __syncwarp();
-    if (lane == 0) {
-        asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
+    if (empty_bar) {
+        // the arrive has release semantics: every lane's shared-memory reads
+        // above are ordered before the producer may overwrite the slot
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
+        }
     }
     dot_rows<NJ, KJ>(rp, xr, accA, accB);
+}
+
+// This warp's share of one stage.  Its (row, slice) units are warp + 8j, all
+// of slice `slice`, taken as row pairs (warp + 16t, warp + 16t + 8): rows
+// (warp >> lp) + t * (16 >> lp) and that plus (8 >> lp), t < nsteps <= kMaxPairs.
+// Only a ragged last stage (U < RT * P valid units) leaves a pair with one
+// row.  The slot is released after the warp's last loads of the stage.  The
+// lanes' partial sums of all (up to 8) rows are reduced together at the end:
+// a transposed butterfly halves the values a lane carries at each of the
+// first three exchanges, so lane l ends with row value (l >> 2) & 7 and the
+// stage costs 9 shuffles and one dependent chain, not one per pair.
+template <int NJ, int KJ>
+__device__ __forceinline__ void stage_pairs(Smem &sm, int slot, int rs, const uint8_t *cA, const uint16_t *sA,
+                                            int K, int nb, int lp, int U, int nsteps, int warp, int lane, int slice,
+                                            bool full_slice, int chunks_slice, float *yrow, int wrow,
+                                            const unsigned long long (&xr)[KJ][8]) {
+    const int pstride = 16 >> lp;  // rows from one pair of the warp to the next
+    const int boff = 8 >> lp;      // row B - row A
+    float acc[2 * kMaxPairs];
+#pragma unroll
+    for (int t = 0; t < kMaxPairs; ++t) {
+        acc[2 * t] = 0.f;
+        acc[2 * t + 1] = 0.f;
+        if (t < nsteps) {
+            const bool vB = warp + 16 * t + 8 < U;
+            const uint8_t *ca = cA + t * pstride * K;
+            const uint16_t *sa = sA + t * pstride * nb;
+            uint64_t *rel = (t == nsteps - 1) ? &sm.empty[slot] : nullptr;
+            if (vB && full_slice)
+                stage_rows<NJ, KJ, true>(ca, ca + boff * K, sa, sa + boff * nb, true, vB, lane, chunks_slice, xr,
+                                         rel, acc[2 * t], acc[2 * t + 1]);
+            else
+                stage_rows<NJ, KJ, false>(ca, ca + boff * K, sa, sa + boff * nb, true, vB, lane, chunks_slice, xr,
+                                          rel, acc[2 * t], acc[2 * t + 1]);
+        }
+    }
+    // transposed butterfly: keep the half of the values selected by the lane
+    // bit, add the partner's copy of that half
+    float h4[4], h2[2];
+    const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const float keep = b4 ? acc[v + 4] : acc[v];
+        const float give = b4 ? acc[v] : acc[v + 4];
+        h4[v] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+    }
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+        const float keep = b3 ? h4[v + 2] : h4[v];
+        const float give = b3 ? h4[v] : h4[v + 2];
+        h2[v] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+    }
+    float r;
+    {
+        const float keep = b2 ? h2[1] : h2[0];
+        const float give = b2 ? h2[0] : h2[1];
+        r = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+    }
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    // lane 4v holds value v: pair v >> 1, row A (v even) or B (v odd)
+    const int v = lane >> 2;
+    const int t = v >> 1;
+    const bool isB = (v & 1) != 0;
+    if ((lane & 3) == 0 && t < nsteps && (!isB || warp + 16 * t + 8 < U)) {
+        const int row = wrow + t * pstride + (isB ? boff : 0);
+        if (lp == 0) {
+            yrow[row] = r;
+        } else {
+            const int P = 1 << lp;
+            sm.red[rs][row][slice] = r;
+            __threadfence_block();
+            const uint32_t prev = atomicAdd(&sm.cnt[rs][row], 1u);
+            if (prev == static_cast<uint32_t>(P - 1)) {
+                __threadfence_block();
+                float tot = sm.red[rs][row][0];
+                for (int sl = 1; sl < P; ++sl) tot += sm.red[rs][row][sl];
+                yrow[row] = tot;
+                sm.cnt[rs][row] = 0u;
+            }
+        }
+    }
 }
 
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
@@ -215,7 +305,7 @@ __device__ __forceinline__ int find_gdesc(const GParams &p, int stage) {
 }
 
 // The work of one CTA over stages [begin, end); KJ is the number of 16-code
-// chunks per lane in a warp's K slice (4: slices up to 2048 wide).
+// chunks per lane in a warp's K slice (3: slices up to 1536 wide).
 // `ring` counts the stages this CTA has already passed through its ring of
 // kStages slots; slot and mbarrier phase follow from it.
 template <int KJ>
@@ -319,58 +409,25 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
         const uint16_t *scales = reinterpret_cast<const uint16_t *>(
             sm.stage[slot] + kCodeBytes + ((static_cast<int64_t>(r0) * D.nb * 2) & 15));
         const int rows = min(D.RT, D.N - r0);
-        // this warp's two units of the stage: rows rA and rB, both of slice `slice`
-        const int rA = warp / D.P;
-        const int rB = (warp + kConsumerWarps) / D.P;
-        const bool vA = rA < rows, vB = rB < rows;
-        const uint8_t *cA = codes + rA * D.K + k0;
-        const uint8_t *cB = codes + rB * D.K + k0;
-        const uint16_t *sA = scales + rA * D.nb + (k0 >> 5);
-        const uint16_t *sB = scales + rB * D.nb + (k0 >> 5);
-        float accA = 0.f, accB = 0.f;
-        if (vA && vB && chunks_slice == 32 * nj) {
-            switch (nj) {
-                case 1: stage_rows<1, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-                case 2: stage_rows<2, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-                case 3: if constexpr (KJ >= 3) stage_rows<3, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-                default: if constexpr (KJ >= 4) stage_rows<4, KJ, true>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
+        const int U = rows << D.lp;                       // valid (row, slice) units
+        const int nsteps = (max(0, (U - warp + 7) >> 3) + 1) >> 1;  // this warp's row pairs
+        if (nsteps == 0) {
+            __syncwarp();
+            if (lane == 0) {
+                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.empty[slot])) : "memory");
             }
-        } else {
-            switch (nj) {
-                case 1: stage_rows<1, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-                case 2: stage_rows<2, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-                case 3: if constexpr (KJ >= 3) stage_rows<3, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-                default: if constexpr (KJ >= 4) stage_rows<4, KJ, false>(cA, cB, sA, sB, vA, vB, lane, chunks_slice, xr, &sm.empty[slot], accA, accB); break;
-            }
+            continue;
         }
-        // reduce both rows at once: after the first exchange lanes 0-15 carry
-        // row A and lanes 16-31 row B, then a 4-step tree within each half
-        {
-            const bool hi = (lane & 16) != 0;
-            const float keep = hi ? accB : accA;
-            const float give = hi ? accA : accB;
-            float v = keep + __shfl_xor_sync(0xffffffffu, give, 16);
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            const int row = hi ? rB : rA;
-            const bool valid = hi ? vB : vA;
-            if ((lane & 15) == 0 && valid) {
-                if (D.P == 1) {
-                    D.y[r0 + row] = v;
-                } else {
-                    const int rs = (ring + k) % (2 * kStages);
-                    sm.red[rs][row][slice] = v;
-                    __threadfence_block();
-                    const uint32_t prev = atomicAdd(&sm.cnt[rs][row], 1u);
-                    if (prev == static_cast<uint32_t>(D.P - 1)) {
-                        __threadfence_block();
-                        float t = sm.red[rs][row][0];
-                        for (int sl = 1; sl < D.P; ++sl) t += sm.red[rs][row][sl];
-                        D.y[r0 + row] = t;
-                        sm.cnt[rs][row] = 0u;
-                    }
-                }
-            }
+        const int wrow = warp >> D.lp;
+        const uint8_t *cA = codes + wrow * D.K + k0;
+        const uint16_t *sA = scales + wrow * D.nb + (k0 >> 5);
+        const int rs = (ring + k) % (2 * kStages);
+        const bool full_slice = chunks_slice == 32 * nj;
+        float *yrow = D.y + r0;
+        switch (nj) {
+            case 1: stage_pairs<1, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr); break;
+            case 2: stage_pairs<2, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr); break;
+            default: stage_pairs<3, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr); break;
         }
     }
 }
@@ -391,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         }
         fence_mbar_init();
     }
-    for (int i = tid; i < 2 * kStages * kUnits; i += kThreads) (&sm.cnt[0][0])[i] = 0u;
+    for (int i = tid; i < 2 * kStages * kRedRows; i += kThreads) (&sm.cnt[0][0])[i] = 0u;
     __syncthreads();
     if (end > begin) cta_work<kJMax>(p, sm, begin, end, warp, lane, 0);
 }
@@ -427,7 +484,7 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_stat
         GDesc &D = p.d[i];
         const int K = static_cast<int>(descs[i].K);
         int P = 1;
-        while (P * 2048 < K) P *= 2;
+        while (P * kSliceK < K) P *= 2;
         D.q = descs[i].q;
         D.s = descs[i].s;
         D.x = descs[i].x;
@@ -436,7 +493,11 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_stat
         D.K = K;
         D.nb = K / 32;
         D.P = P;
-        D.RT = std::min(kUnits / P, kCodeBytes / K);
+        D.lp = __builtin_ctz(static_cast<unsigned>(P));
+        // the most rows that fit kCodeBytes in whole groups of 16 / P rows, so
+        // every stage is whole row pairs for all 8 warps (RT * P = 16 * pairs);
+        // K <= P * kSliceK guarantees at least two pairs; at most kMaxPairs
+        D.RT = std::min((kCodeBytes / K) / (16 / P) * (16 / P), 16 * kMaxPairs / P);
         D.bps = (D.nb + P - 1) / P;
         D.stage_begin = stages;
         D.stages = (D.N + D.RT - 1) / D.RT;
