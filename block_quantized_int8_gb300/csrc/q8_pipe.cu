@@ -1,4 +1,4 @@
-// q8_pipe.cu -- Q8_0 W8A16 matmul for 2 <= M <= 8 activation rows over one or
+// q8_pipe.cu -- Q8_0 W8A16 matmul for 1 <= M <= 8 activation rows over one or
 // several matrices in one persistent launch (K <= 4096).
 //
 // Y[m][n] = sum_k s[n][k/32] * q[n][k] * x[m][k]; "Frigg" README, Finding 8
@@ -6,25 +6,36 @@
 // and Finding 3 (one launch for the many small matrices of a decode step).
 //
 // Design (bulk-copy fed, tensor cores through warp mma):
-//  * A stage is RT = 16 weight rows (8 when K > 1984) with their full K.  Lane
-//    0 of warp 0 copies each row with one cp.async.bulk into a shared-memory
-//    row padded to K + 16 bytes, and the RT*K/16 scale bytes (contiguous in
-//    global memory) with one more; kStages stages in flight per CTA, two CTAs
-//    per SM, byte-balanced contiguous stage ranges per CTA (as q8_gemv.cu).
-//  * The 8 warps split K: warp w owns blocks [w*bpw, (w+1)*bpw).  Its part of
-//    x stays in registers in the mma B-fragment layout, reloaded only when
-//    the matrix changes.
-//  * Per 32-code block a warp runs two mma.sync.m16n8k16 (bf16 in, fp32 out)
-//    with the weights as the 16-row A operand (lane (g, t) holds bytes
-//    [8t, 8t+8) of rows g and g+8; the 16-byte row skew makes these reads
-//    bank-conflict free) and x^T as B (columns = activation rows, zero past
-//    M).  Codes become bf16 exactly (|q| <= 127); each block's fp32 result is
-//    scaled by its binary16 scale.
-//  * With 8-row stages each warp copies its share into registers and releases
-//    the slot before any arithmetic.  The 8 partial sums of a row are added in
-//    warp order 0..7 by whichever warp finishes the stage last (shared-memory
-//    counter over a small ring; nobody waits), so results are deterministic
-//    and independent of batching.
+//  * A stage is RT consecutive weight rows with their full K, about 48 KB.
+//    Each row goes by one cp.async.bulk into a
+//    shared-memory row padded to K + 32 bytes (the padding puts the rows that
+//    one mma reads at the same k on distinct banks), and the RT*K/16 scale
+//    bytes with one more copy.  The ring has S = 2 or 3 slots (as many as the
+//    launch's largest stage allows with two CTAs per SM).  There is no
+//    producer warp: thread 0 issues the first S stages and then the warp that
+//    releases a slot last (a shared-memory counter) issues the stage S later
+//    into it, so a slot is refilled the moment it is free.  CTAs own
+//    byte-balanced contiguous stage ranges (as in q8_gemv.cu).
+//  * Rows come in groups of 8 and K in P slices (P a power of two <= 8).  A
+//    full-tile stage has 16/P groups and slices of at most 384: each warp
+//    owns one slice (w % P) of two groups, one whole m16n8k16 tile.  A
+//    half-tile stage has 8/P groups and slices of at most 512: each warp owns
+//    one slice of one group, half a tile (the upper rows of the mma operand
+//    are zero and never converted).  Per K the host takes the shape with more
+//    bytes in flight (e.g. K = 1536: 32-row full tiles, two slots; K = 4096:
+//    8-row half tiles, three slots).  A warp's x slice stays in registers in
+//    the mma B-fragment layout (at most 16 blocks), reloaded only when the
+//    matrix changes.
+//  * Per 32-code block two mma.sync.m16n8k16 (bf16 in, fp32 out) with the
+//    weights as the 16-row A operand (lane (g, t) holds bytes [8t, 8t+8) of
+//    its rows) and x^T as B (columns = activation rows, zero past M).  Codes
+//    become bf16 exactly (|q| <= 127); each block's fp32 result is scaled by
+//    its binary16 scale.  The warps compute straight from shared memory.
+//  * The P partial tiles of a stage are added in slice order by whichever of
+//    the P warps finishes last (shared-memory counter, nobody waits), so the
+//    results are deterministic and independent of batching.  A warp releases
+//    its slot after its partial is published (the last one after reading all
+//    partials), which also protects the partial buffers, one per slot.
 // Every wait is bounded (Q8_DEV_TIMEOUT on expiry).
 #include <algorithm>
 
@@ -37,16 +48,15 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 2;
-constexpr int kCodeCap = 33280;          // RT * (K + 16): 16 rows of K <= 2064 or 8 rows of K <= 4144
-constexpr int kScaleCap = 2064;          // RT * K / 16 + alignment offset
-constexpr int kSlotBytes = kCodeCap + kScaleCap;
-constexpr int kPipeMaxK = 4096;          // x fragments: at most 16 blocks per warp
-constexpr int kMaxBpw = 16;
+constexpr int kPad = 32;               // bytes after each shared-memory row
+constexpr int kSliceK = 384;           // widest slice of a full-tile stage
+constexpr int kHalfSliceK = 512;       // widest slice of a half-tile stage
+constexpr int kMaxBpw = 16;            // x blocks per warp (half tiles: 512 / 32)
+constexpr int kPipeMaxK = 4096;
+constexpr int kMaxSlots = 3;
 constexpr int kMaxGrid = 1024;
-// Partial-sum ring: a warp can run at most kStages stages ahead of the last
-// warp's combine, so kStages + 2 entries are never reused too early.
-constexpr int kRed = kStages + 2;
+constexpr int kSmemBudget = 115712;    // dynamic shared memory per CTA, two CTAs per SM
+constexpr int kCtlBytes = 256;         // counters and mbarriers
 
 struct PDesc {
     const int8_t *q;
@@ -58,9 +68,13 @@ struct PDesc {
     int32_t N;
     int32_t K;
     int32_t nb;
-    int32_t RT;          // rows per stage (16 or 8)
-    int32_t RS;          // shared-memory row stride, K + 16
-    int32_t bpw;         // blocks per warp = ceil(nb / 8)
+    int32_t RT;          // rows per stage (a multiple of 8)
+    int32_t RS;          // shared-memory row stride, K + kPad
+    int32_t P;           // K slices (power of two <= 8)
+    int32_t lp;          // log2(P)
+    int32_t half;        // 1: one 8-row group per stage, half tiles
+    int32_t bps;         // blocks per slice
+    int32_t scale_off;   // offset of the scales in a slot: RT * RS
     int32_t stage_begin;
     int32_t stages;
 };
@@ -70,25 +84,13 @@ struct PParams {
     uint32_t *status;
     int32_t count;
     int32_t M;
+    int32_t S;           // slots in the ring
+    int32_t slot_bytes;
+    int32_t red_off;     // partial tiles: S entries of red_entry bytes
+    int32_t red_entry;   // 8 warps x 32 lanes x (float4 full tiles, float2 half tiles)
+    int32_t ctl_off;     // counters [kMaxSlots][8], release counts [kMaxSlots], then full[kMaxSlots]
     int32_t cta_begin[kMaxGrid + 1];
 };
-
-struct PSmem {
-    alignas(128) uint8_t slot[kStages][kSlotBytes];
-    float red[kRed][kWarps][32][4];  // per-warp partial D fragments, ring over stages
-    uint32_t cnt[kRed];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-};
-
-__device__ __forceinline__ bool test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-    return ok != 0;
-}
 
 __device__ __forceinline__ int find_pdesc(const PParams &p, int stage) {
     int d = 0;
@@ -96,105 +98,52 @@ __device__ __forceinline__ int find_pdesc(const PParams &p, int stage) {
     return d;
 }
 
-// One warp's part of a stage in registers: BPW blocks (the last ones masked
-// by kb < kb1) of rows g and g+8, with their scales.
-// TWO: the stage has 16 rows (a second row group g+8); with 8-row stages the
-// upper half of the A operand is zero and needs no registers.
-template <int BPW, bool TWO>
-struct PFrag {
-    uint2 cg[BPW];
-    uint32_t sg[BPW];
-    uint2 ch[TWO ? BPW : 1];
-    uint32_t sh[TWO ? BPW : 1];
-};
-
-template <int BPW, bool TWO>
-__device__ __forceinline__ void load_frag(PFrag<BPW, TWO> &f, const uint8_t *codes, const uint16_t *scales, int RS,
-                                          int nb, int kb0, int kb1, int g, int t) {
+// One warp's share of a stage: BPW blocks of its slice for row ra (lower half
+// of the mma tile) and, if TWO, row rb (upper half), straight from shared
+// memory.  FULL: both rows exist and the slice has BPW blocks, so nothing is
+// predicated.  acc[0..1]: row ra, activation rows 2t, 2t+1; acc[2..3]: rb.
+template <int BPW, bool TWO, bool FULL>
+__device__ __forceinline__ void tile_mma(const uint8_t *ca, const uint8_t *cb, const uint16_t *sa,
+                                         const uint16_t *sb, bool va, bool vb, int nblk, int t,
+                                         const uint4 (&xr)[kMaxBpw], float (&acc)[4]) {
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
-        const int kb = kb0 + j;
-        f.cg[j] = make_uint2(0u, 0u);
-        f.sg[j] = 0u;
-        if constexpr (TWO) {
-            f.ch[j] = f.cg[j];
-            f.sh[j] = 0u;
+        if (!FULL && j >= nblk) break;
+        uint2 wa = make_uint2(0u, 0u), wb = wa;
+        uint32_t ha = 0u, hb = 0u;
+        if (FULL || va) {
+            wa = *reinterpret_cast<const uint2 *>(ca + 32 * j + 8 * t);
+            ha = sa[j];
         }
-        if (kb < kb1) {
-            f.cg[j] = *reinterpret_cast<const uint2 *>(codes + g * RS + kb * 32 + 8 * t);
-            f.sg[j] = scales[g * nb + kb];
-            if constexpr (TWO) {
-                f.ch[j] = *reinterpret_cast<const uint2 *>(codes + (g + 8) * RS + kb * 32 + 8 * t);
-                f.sh[j] = scales[(g + 8) * nb + kb];
+        if constexpr (TWO) {
+            if (FULL || vb) {
+                wb = *reinterpret_cast<const uint2 *>(cb + 32 * j + 8 * t);
+                hb = sb[j];
             }
         }
-    }
-}
-
-template <int BPW, bool TWO>
-__device__ __forceinline__ void mma_frag(const PFrag<BPW, TWO> &f, const uint4 (&xr)[kMaxBpw], float (&acc)[4]) {
-#pragma unroll
-    for (int j = 0; j < BPW; ++j) {
-        uint32_t g01, g23, g45, g67, h01 = 0u, h23 = 0u, h45 = 0u, h67 = 0u;
-        codes4_to_bf16x2(f.cg[j].x, g01, g23);
-        codes4_to_bf16x2(f.cg[j].y, g45, g67);
+        uint32_t a01, a23, a45, a67, b01 = 0u, b23 = 0u, b45 = 0u, b67 = 0u;
+        codes4_to_bf16x2(wa.x, a01, a23);
+        codes4_to_bf16x2(wa.y, a45, a67);
         if constexpr (TWO) {
-            codes4_to_bf16x2(f.ch[j].x, h01, h23);
-            codes4_to_bf16x2(f.ch[j].y, h45, h67);
+            codes4_to_bf16x2(wb.x, b01, b23);
+            codes4_to_bf16x2(wb.y, b45, b67);
         }
         float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-        mma_bf16_16816(d0, d1, d2, d3, g01, h01, g23, h23, xr[j].x, xr[j].y);
-        mma_bf16_16816(d0, d1, d2, d3, g45, h45, g67, h67, xr[j].z, xr[j].w);
-        const float sg = f16_bits_to_f32(f.sg[j]);
-        acc[0] = fmaf(sg, d0, acc[0]);
-        acc[1] = fmaf(sg, d1, acc[1]);
+        mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xr[j].x, xr[j].y);
+        mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xr[j].z, xr[j].w);
+        const float s_a = f16_bits_to_f32(ha);
+        acc[0] = fmaf(s_a, d0, acc[0]);
+        acc[1] = fmaf(s_a, d1, acc[1]);
         if constexpr (TWO) {
-            const float sh = f16_bits_to_f32(f.sh[j]);
-            acc[2] = fmaf(sh, d2, acc[2]);
-            acc[3] = fmaf(sh, d3, acc[3]);
+            const float s_b = f16_bits_to_f32(hb);
+            acc[2] = fmaf(s_b, d2, acc[2]);
+            acc[3] = fmaf(s_b, d3, acc[3]);
         }
-    }
-}
-
-// 8-row stages (TWO false): copy this warp's share of the stage into
-// registers, hand the slot back to the producer (the release orders every
-// lane's reads before any refill), then do the arithmetic.  16-row stages
-// hold twice the registers, so they compute block by block straight from
-// shared memory and release the slot afterwards.
-template <int BPW, bool TWO>
-__device__ __forceinline__ void stage_mma(const uint8_t *codes, const uint16_t *scales, int RS, int nb, int kb0,
-                                          int kb1, int g, int t, const uint4 (&xr)[kMaxBpw],
-                                          uint64_t *empty_bar, int lane, float (&acc)[4]) {
-    if constexpr (TWO) {
-#pragma unroll
-        for (int j = 0; j < BPW; ++j) {
-            const int kb = kb0 + j;
-            if (kb < kb1) {
-                PFrag<1, true> f;
-                f.cg[0] = *reinterpret_cast<const uint2 *>(codes + g * RS + kb * 32 + 8 * t);
-                f.ch[0] = *reinterpret_cast<const uint2 *>(codes + (g + 8) * RS + kb * 32 + 8 * t);
-                f.sg[0] = scales[g * nb + kb];
-                f.sh[0] = scales[(g + 8) * nb + kb];
-                const uint4 xj[kMaxBpw] = {xr[j]};
-                mma_frag<1, true>(f, xj, acc);
-            }
-        }
-        __syncwarp();
-        if (lane == 0)
-            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
-    } else {
-        PFrag<BPW, TWO> f;
-        load_frag<BPW, TWO>(f, codes, scales, RS, nb, kb0, kb1, g, t);
-        __syncwarp();
-        if (lane == 0)
-            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
-        mma_frag<BPW, TWO>(f, xr, acc);
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant__ PParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    PSmem &sm = *reinterpret_cast<PSmem *>(smem_raw);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -203,184 +152,300 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
     const int begin = p.cta_begin[blockIdx.x];
     const int end = p.cta_begin[blockIdx.x + 1];
     const int M = p.M;
+    const int S = p.S;
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(smem_raw + p.ctl_off);     // [S][8 tiles]
+    uint32_t *rel = cnt + kMaxSlots * 8;                                     // [S] release counts
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + p.ctl_off + kMaxSlots * 9 * 4 + 4);
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], kWarps);
-        }
-        for (int i = 0; i < kRed; ++i) sm.cnt[i] = 0u;
+        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < kMaxSlots * 9; ++i) cnt[i] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
     if (end <= begin) return;
 
-    // ---- producer (lane 0 of warp 0, between its own stages) ------------------
+    // ---- refills ------------------------------------------------------------------
+    // Thread 0 issues the first S stages; afterwards the warp that releases a
+    // slot last issues the stage S later into it at once, so a free slot never
+    // waits for a particular warp to come round.
     const int nstages = end - begin;
-    int pi = 0;
-    int pd = find_pdesc(p, begin);
-    bool prod_ok = true;
-    auto produce = [&](int upto) {
-        while (prod_ok && pi < nstages && pi <= upto) {
-            const int slot = pi % kStages;
-            if (pi >= kStages) {
-                const uint32_t par = ((pi / kStages) - 1) & 1;
-                if (pi <= upto - (kStages - 1)) {
-                    if (!mbar_wait_bounded(&sm.empty[slot], par)) {
-                        prod_ok = false;
-                        if (p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
-                        return;
-                    }
-                } else if (!test_wait(&sm.empty[slot], par)) {
-                    return;
-                }
-            }
-            const int i = begin + pi;
-            while (i >= p.d[pd].stage_begin + p.d[pd].stages) ++pd;
-            const PDesc &D = p.d[pd];
-            const int r0 = (i - D.stage_begin) * D.RT;
-            const int rows = min(D.RT, D.N - r0);
-            uint8_t *dst = sm.slot[slot];
-            // scales: same offset mod 16 as in global memory; unaligned head
-            // and tail by plain copies, published by the arrive below
-            const uint32_t sbytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(D.nb) * 2u;
-            const int64_t sstart = static_cast<int64_t>(r0) * D.nb * 2;
-            const uint32_t a = static_cast<uint32_t>(sstart & 15);
-            const uint8_t *gs = reinterpret_cast<const uint8_t *>(D.s) + sstart;
-            uint8_t *sdst = dst + kCodeCap + a;
-            const uint32_t head = min(sbytes, a ? 16u - a : 0u);
-            const uint32_t body = (sbytes - head) & ~15u;
-            for (uint32_t b = 0; b < head; b += 2)
-                *reinterpret_cast<uint16_t *>(sdst + b) = *reinterpret_cast<const uint16_t *>(gs + b);
-            for (uint32_t b = head + body; b < sbytes; b += 2)
-                *reinterpret_cast<uint16_t *>(sdst + b) = *reinterpret_cast<const uint16_t *>(gs + b);
-            mbar_arrive_expect_tx(&sm.full[slot], static_cast<uint32_t>(rows) * static_cast<uint32_t>(D.K) + body);
-            for (int r = 0; r < rows; ++r)
-                bulk_g2s(dst + r * D.RS, D.q + static_cast<int64_t>(r0 + r) * D.K, static_cast<uint32_t>(D.K),
-                         &sm.full[slot]);
-            if (body) bulk_g2s(sdst + head, gs + head, body, &sm.full[slot]);
-            ++pi;
-        }
+    auto issue = [&](int pi, int pd) {
+        const int slot = pi % S;
+        const int i = begin + pi;
+        while (i >= p.d[pd].stage_begin + p.d[pd].stages) ++pd;
+        const PDesc &D = p.d[pd];
+        const int r0 = (i - D.stage_begin) * D.RT;
+        const int rows = min(D.RT, D.N - r0);
+        uint8_t *dst = smem_raw + static_cast<size_t>(slot) * p.slot_bytes;
+        // scales: same offset mod 16 as in global memory; the unaligned head
+        // and tail go by plain copies, published by the arrive below
+        const uint32_t sbytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(D.nb) * 2u;
+        const int64_t sstart = static_cast<int64_t>(r0) * D.nb * 2;
+        const uint32_t a = static_cast<uint32_t>(sstart & 15);
+        const uint8_t *gs = reinterpret_cast<const uint8_t *>(D.s) + sstart;
+        uint8_t *sdst = dst + D.scale_off + a;
+        const uint32_t head = min(sbytes, a ? 16u - a : 0u);
+        const uint32_t body = (sbytes - head) & ~15u;
+        for (uint32_t b = 0; b < head; b += 2)
+            *reinterpret_cast<uint16_t *>(sdst + b) = *reinterpret_cast<const uint16_t *>(gs + b);
+        for (uint32_t b = head + body; b < sbytes; b += 2)
+            *reinterpret_cast<uint16_t *>(sdst + b) = *reinterpret_cast<const uint16_t *>(gs + b);
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows) * static_cast<uint32_t>(D.K) + body);
+        const int8_t *src = D.q + static_cast<int64_t>(r0) * D.K;
+        for (int r = 0; r < rows; ++r)
+            bulk_g2s(dst + r * D.RS, src + static_cast<int64_t>(r) * D.K, static_cast<uint32_t>(D.K), &full[slot]);
+        if (body) bulk_g2s(sdst + head, gs + head, body, &full[slot]);
     };
+    if (tid == 0) {
+        const int d0 = find_pdesc(p, begin);
+        for (int pi = 0; pi < min(S, nstages); ++pi) issue(pi, d0);
+    }
 
     // ---- consumers --------------------------------------------------------------
     int d = find_pdesc(p, begin);
     int cur_d = -1;
     uint4 xr[kMaxBpw];
-    int kb0 = 0, kb1 = 0;
+    int kb0 = 0, nblk = 0;
     for (int i = begin, k = 0; i < end; ++i, ++k) {
-        if (warp == 0 && lane == 0) produce(k + kStages - 1);
-        __syncwarp();
         while (i >= p.d[d].stage_begin + p.d[d].stages) ++d;
         const PDesc &D = p.d[d];
+        const int lp = D.lp;
+        const int P = 1 << lp;
         if (d != cur_d) {
-            // this warp's x fragments: x[m = g][block kb][8t .. 8t+8), zero past M
+            // this warp's x fragments: x[m = g][block kb0 + j][8t .. 8t+8), zero past M
             cur_d = d;
-            kb0 = warp * D.bpw;
-            kb1 = min(D.nb, kb0 + D.bpw);
+            kb0 = (warp & (P - 1)) * D.bps;
+            nblk = max(0, min(D.nb - kb0, D.bps));
 #pragma unroll
             for (int j = 0; j < kMaxBpw; ++j) {
-                const int kb = kb0 + j;
                 xr[j] = make_uint4(0u, 0u, 0u, 0u);
-                if (g < M && kb < kb1) xr[j] = __ldg(reinterpret_cast<const uint4 *>(D.x + g * D.ldx + kb * 32 + 8 * t));
+                if (g < M && j < nblk)
+                    xr[j] = __ldg(reinterpret_cast<const uint4 *>(D.x + g * D.ldx + (kb0 + j) * 32 + 8 * t));
             }
         }
-        const int slot = k % kStages;
-        if (!mbar_wait_bounded(&sm.full[slot], (k / kStages) & 1)) {
+        const int slot = k % S;
+        if (!mbar_wait_bounded(&full[slot], (k / S) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
             return;
         }
+        const uint8_t *codes = smem_raw + static_cast<size_t>(slot) * p.slot_bytes;
         const int r0 = (i - D.stage_begin) * D.RT;
         const int rows = min(D.RT, D.N - r0);
-        const uint8_t *codes = sm.slot[slot];
         const uint16_t *scales = reinterpret_cast<const uint16_t *>(
-            sm.slot[slot] + kCodeCap + ((static_cast<int64_t>(r0) * D.nb * 2) & 15));
-        const bool two = D.RT == 16;
+            codes + D.scale_off + ((static_cast<int64_t>(r0) * D.nb * 2) & 15));
+        // this warp's rows: row g of group ga (lower half of the tile) and, for
+        // full tiles, row g of group ga + 8/P (upper half)
+        const int ga = warp >> lp;
+        const int ra = 8 * ga + g;
+        const int rb = ra + (64 >> lp);
+        const bool two = D.half == 0;
+        const bool va = ra < rows;
+        const bool vb = two && rb < rows;
+        const uint8_t *ca = codes + ra * D.RS + kb0 * 32;
+        const uint8_t *cb = codes + rb * D.RS + kb0 * 32;
+        const uint16_t *sa = scales + ra * D.nb + kb0;
+        const uint16_t *sb = scales + rb * D.nb + kb0;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int bpw = D.bpw;
-        uint64_t *eb = &sm.empty[slot];
-        // 16-row stages have K <= 2048 (bpw <= 8); 8-row stages have K > 1984 (bpw >= 8)
+        const bool full_tile = rows == D.RT && nblk == D.bps;
         if (two) {
-            if (bpw <= 2) stage_mma<2, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
-            else if (bpw <= 4) stage_mma<4, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
-            else if (bpw <= 6) stage_mma<6, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
-            else stage_mma<8, true>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            if (full_tile && nblk == 12)
+                tile_mma<12, true, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+            else if (full_tile && nblk == 8)
+                tile_mma<8, true, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+            else if (full_tile && nblk == 4)
+                tile_mma<4, true, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+            else
+                tile_mma<12, true, false>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
         } else {
-            if (bpw <= 8) stage_mma<8, false>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
-            else if (bpw <= 12) stage_mma<12, false>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
-            else stage_mma<16, false>(codes, scales, D.RS, D.nb, kb0, kb1, g, t, xr, eb, lane, acc);
+            if (full_tile && nblk == 16)
+                tile_mma<16, false, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+            else if (full_tile && nblk == 8)
+                tile_mma<8, false, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+            else
+                tile_mma<16, false, false>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
         }
-        const int rs = k % kRed;
 
-        // publish this warp's partials; the last warp adds all 8 in warp order
-        *reinterpret_cast<float4 *>(&sm.red[rs][warp][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        // publish this warp's partial tile; the last of the tile's P warps adds
+        // them in slice order and writes y
+        const int tile = warp >> lp;
+        uint8_t *rs = smem_raw + p.red_off + slot * p.red_entry;
+        if (two)
+            reinterpret_cast<float4 *>(rs)[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        else
+            reinterpret_cast<float2 *>(rs)[warp * 32 + lane] = make_float2(acc[0], acc[1]);
         __threadfence_block();
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = atomicAdd(&sm.cnt[rs], 1u);
+        if (lane == 0) prev = atomicAdd(&cnt[slot * 8 + tile], 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == kWarps - 1) {
+        if (prev == static_cast<uint32_t>(P - 1)) {
             __threadfence_block();
-            float4 v = *reinterpret_cast<const float4 *>(&sm.red[rs][0][lane][0]);
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) {
-                const float4 u = *reinterpret_cast<const float4 *>(&sm.red[rs][w][lane][0]);
-                v.x += u.x;
-                v.y += u.y;
-                v.z += u.z;
-                v.w += u.w;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sl = 0; sl < P; ++sl) {
+                const int src = ((tile << lp) + sl) * 32 + lane;
+                if (two) {
+                    const float4 u = reinterpret_cast<const float4 *>(rs)[src];
+                    if (sl == 0) {
+                        v = u;
+                    } else {
+                        v.x += u.x;
+                        v.y += u.y;
+                        v.z += u.z;
+                        v.w += u.w;
+                    }
+                } else {
+                    const float2 u = reinterpret_cast<const float2 *>(rs)[src];
+                    if (sl == 0) {
+                        v.x = u.x;
+                        v.y = u.y;
+                    } else {
+                        v.x += u.x;
+                        v.y += u.y;
+                    }
+                }
             }
             const int m0 = 2 * t;
-            const int ng = r0 + g;
-            const int nh = r0 + g + 8;
-            if (g < rows) {
-                if (m0 < M) D.y[m0 * D.ldy + ng] = v.x;
-                if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + ng] = v.y;
+            if (va) {
+                if (m0 < M) D.y[m0 * D.ldy + r0 + ra] = v.x;
+                if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + r0 + ra] = v.y;
             }
-            if (two && g + 8 < rows) {
-                if (m0 < M) D.y[m0 * D.ldy + nh] = v.z;
-                if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + nh] = v.w;
+            if (vb) {
+                if (m0 < M) D.y[m0 * D.ldy + r0 + rb] = v.z;
+                if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + r0 + rb] = v.w;
             }
-            if (lane == 0) sm.cnt[rs] = 0u;
+            if (lane == 0) cnt[slot * 8 + tile] = 0u;
         }
+        // release the slot: this warp's reads of the slot and of the partial
+        // buffer are ordered (fence, counter, fence) before the refill that
+        // the last of the 8 warps issues
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const uint32_t done = atomicAdd(&rel[slot], 1u);
+            if (done == kWarps - 1) {
+                __threadfence_block();
+                rel[slot] = 0u;
+                fence_proxy_async_smem();
+                if (k + S < nstages) issue(k + S, d);
+            }
+        }
+        __syncwarp();
     }
 }
 
 int g_configured_dev = -1;
 int g_occ = 0;
 
+struct Shape {
+    int P, lp, half, RT, RS, bps, scale_off, stage_bytes;
+};
+
+// Partial-tile buffer per slot: 8 warps x 32 lanes x float4 (full tiles) or
+// float2 (half tiles).
+constexpr int red_entry_bytes(bool any_full) { return kWarps * 32 * (any_full ? 16 : 8); }
+
+Shape make_shape(int K, int half, int P) {
+    Shape h{};
+    const int nb = K / 32;
+    h.P = P;
+    h.lp = __builtin_ctz(static_cast<unsigned>(P));
+    h.half = half;
+    h.RT = (half ? 64 : 128) / P;
+    h.RS = K + kPad;
+    h.bps = (nb + P - 1) / P;
+    h.scale_off = h.RT * h.RS;
+    h.stage_bytes = h.scale_off + h.RT * nb * 2 + 16;
+    return h;
+}
+
+// Slots of a ring of stages of `stage_bytes` (0 if fewer than 2 fit).
+int slots_for(int stage_bytes, bool any_full) {
+    const int slot = (stage_bytes + 127) / 128 * 128;
+    for (int S = kMaxSlots; S >= 2; --S)
+        if (S * slot + S * red_entry_bytes(any_full) + kCtlBytes <= kSmemBudget) return S;
+    return 0;
+}
+
+// The stage shape of a matrix: full tiles (slices of at most 384, 128/P
+// rows) or half tiles (slices of at most 512, 64/P rows), P the fewest slices
+// that respect the slice width and fit two slots; of the two, the one with
+// more bytes in flight when the matrix is alone in a launch.
+Shape shape_of(int K) {
+    Shape best{};
+    long best_score = -1;
+    for (int half = 0; half <= 1; ++half) {
+        const int width = half ? kHalfSliceK : kSliceK;
+        int P = 1;
+        while (P * width < K && P < 8) P *= 2;
+        if (P * width < K) continue;
+        Shape h = make_shape(K, half, P);
+        while (slots_for(h.stage_bytes, !half) == 0 && P < 8) {
+            P *= 2;
+            h = make_shape(K, half, P);
+        }
+        const int S = slots_for(h.stage_bytes, !half);
+        if (S == 0) continue;
+        const long score = static_cast<long>(S) * h.stage_bytes;
+        if (score > best_score) {
+            best = h;
+            best_score = score;
+        }
+    }
+    return best;  // RT == 0 if no shape fits
+}
+
+// Ring layout of a launch: slot size, slot count, offsets.  Returns false if
+// some matrix has no shape or two slots do not fit.
+bool layout_for(const q8_linear_desc *descs, int count, int &S, int &slot_bytes, int &red_off, int &ctl_off,
+                int &red_entry) {
+    int mx = 0;
+    bool any_full = false;
+    for (int i = 0; i < count; ++i) {
+        const Shape h = shape_of(static_cast<int>(descs[i].K));
+        if (h.RT == 0) return false;
+        mx = std::max(mx, h.stage_bytes);
+        any_full = any_full || !h.half;
+    }
+    S = slots_for(mx, any_full);
+    if (S < 2) return false;
+    slot_bytes = (mx + 127) / 128 * 128;
+    red_entry = red_entry_bytes(any_full);
+    red_off = S * slot_bytes;
+    ctl_off = red_off + S * red_entry;
+    return true;
+}
+
 }  // namespace
 
 bool pipe_supported(const q8_linear_desc *descs, int count, int M) {
     if (M < 1 || M > 8) return false;
-    for (int i = 0; i < count; ++i) {
-        const int64_t K = descs[i].K;
-        if (K > kPipeMaxK) return false;
-        const int RT = (16 * (K + 16) <= kCodeCap) ? 16 : 8;
-        if (RT * (K + 16) > kCodeCap || RT * (K / 32) * 2 + 16 > kScaleCap) return false;
-    }
-    return true;
+    for (int i = 0; i < count; ++i)
+        if (descs[i].K > kPipeMaxK) return false;
+    int S, sb, ro, co, re;
+    return layout_for(descs, count, S, sb, ro, co, re);
 }
 
 q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (g_configured_dev != di->device) {
-        if (cudaFuncSetAttribute(pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sizeof(PSmem))) != cudaSuccess)
+        if (cudaFuncSetAttribute(pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget) != cudaSuccess)
             return Q8_ERR_CUDA;
         int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, pipe_kernel, kThreads, sizeof(PSmem)) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, pipe_kernel, kThreads, kSmemBudget) != cudaSuccess)
             return Q8_ERR_CUDA;
         g_occ = std::max(o, 1);
         g_configured_dev = di->device;
     }
     static thread_local PParams p;
+    if (!layout_for(descs, count, p.S, p.slot_bytes, p.red_off, p.ctl_off, p.red_entry)) return Q8_ERR_UNSUPPORTED;
     double total_bytes = 0.0;
     int stages = 0;
     for (int i = 0; i < count; ++i) {
         PDesc &D = p.d[i];
         const int K = static_cast<int>(descs[i].K);
+        const Shape h = shape_of(K);
         D.q = descs[i].q;
         D.s = descs[i].s;
         D.x = descs[i].x;
@@ -390,9 +455,13 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
         D.N = static_cast<int32_t>(descs[i].N);
         D.K = K;
         D.nb = K / 32;
-        D.RT = (16 * (K + 16) <= kCodeCap) ? 16 : 8;
-        D.RS = K + 16;
-        D.bpw = (D.nb + kWarps - 1) / kWarps;
+        D.RT = h.RT;
+        D.RS = h.RS;
+        D.P = h.P;
+        D.lp = h.lp;
+        D.half = h.half;
+        D.bps = h.bps;
+        D.scale_off = h.scale_off;
         D.stage_begin = stages;
         D.stages = (D.N + D.RT - 1) / D.RT;
         stages += D.stages;
@@ -403,6 +472,7 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
     p.M = M;
     if (stages == 0) return Q8_OK;
     const int grid = std::min(std::min(stages, di->sm_count * g_occ), kMaxGrid);
+    // cut the stage list into `grid` ranges of (nearly) equal bytes
     int c = 0;
     double acc = 0.0;
     p.cta_begin[0] = 0;
@@ -416,7 +486,8 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
         }
     }
     while (c < grid) p.cta_begin[++c] = stages;
-    pipe_kernel<<<grid, kThreads, sizeof(PSmem), stream>>>(p);
+    const size_t smem = static_cast<size_t>(p.ctl_off) + kCtlBytes;
+    pipe_kernel<<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 
