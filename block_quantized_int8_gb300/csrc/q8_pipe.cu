@@ -51,7 +51,6 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPad = 32;               // bytes after each shared-memory row
 constexpr int kSliceK = 384;           // widest slice of a full-tile stage
 constexpr int kHalfSliceK = 512;       // widest slice of a half-tile stage
-constexpr int kMaxBpw = 16;            // x blocks per warp (half tiles: 512 / 32)
 constexpr int kPipeMaxK = 4096;
 constexpr int kMaxSlots = 3;
 constexpr int kMaxGrid = 1024;
@@ -102,10 +101,11 @@ __device__ __forceinline__ int find_pdesc(const PParams &p, int stage) {
 // of the mma tile) and, if TWO, row rb (upper half), straight from shared
 // memory.  FULL: both rows exist and the slice has BPW blocks, so nothing is
 // predicated.  acc[0..1]: row ra, activation rows 2t, 2t+1; acc[2..3]: rb.
-template <int BPW, bool TWO, bool FULL>
+template <int BPW, bool TWO, bool FULL, int KJ>
 __device__ __forceinline__ void tile_mma(const uint8_t *ca, const uint8_t *cb, const uint16_t *sa,
                                          const uint16_t *sb, bool va, bool vb, int nblk, int t,
-                                         const uint4 (&xr)[kMaxBpw], float (&acc)[4]) {
+                                         const uint4 (&xr)[KJ], float (&acc)[4]) {
+    static_assert(BPW <= KJ, "x fragment out of range");
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
         if (!FULL && j >= nblk) break;
@@ -142,6 +142,8 @@ __device__ __forceinline__ void tile_mma(const uint8_t *ca, const uint8_t *cb, c
     }
 }
 
+// KJ: x blocks a warp keeps in registers (12: full tiles only; 16: any).
+template <int KJ>
 __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant__ PParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x;
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
     // ---- consumers --------------------------------------------------------------
     int d = find_pdesc(p, begin);
     int cur_d = -1;
-    uint4 xr[kMaxBpw];
+    uint4 xr[KJ];
     int kb0 = 0, nblk = 0;
     for (int i = begin, k = 0; i < end; ++i, ++k) {
         while (i >= p.d[d].stage_begin + p.d[d].stages) ++d;
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
             kb0 = (warp & (P - 1)) * D.bps;
             nblk = max(0, min(D.nb - kb0, D.bps));
 #pragma unroll
-            for (int j = 0; j < kMaxBpw; ++j) {
+            for (int j = 0; j < KJ; ++j) {
                 xr[j] = make_uint4(0u, 0u, 0u, 0u);
                 if (g < M && j < nblk)
                     xr[j] = __ldg(reinterpret_cast<const uint4 *>(D.x + g * D.ldx + (kb0 + j) * 32 + 8 * t));
@@ -250,20 +252,20 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         const bool full_tile = rows == D.RT && nblk == D.bps;
         if (two) {
             if (full_tile && nblk == 12)
-                tile_mma<12, true, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+                tile_mma<12, true, true, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
             else if (full_tile && nblk == 8)
-                tile_mma<8, true, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+                tile_mma<8, true, true, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
             else if (full_tile && nblk == 4)
-                tile_mma<4, true, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+                tile_mma<4, true, true, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
             else
-                tile_mma<12, true, false>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
-        } else {
+                tile_mma<12, true, false, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+        } else if constexpr (KJ >= 16) {
             if (full_tile && nblk == 16)
-                tile_mma<16, false, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+                tile_mma<16, false, true, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
             else if (full_tile && nblk == 8)
-                tile_mma<8, false, true>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+                tile_mma<8, false, true, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
             else
-                tile_mma<16, false, false>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
+                tile_mma<16, false, false, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
         }
 
         // publish this warp's partial tile; the last of the tile's P warps adds
@@ -336,6 +338,17 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
 
 int g_configured_dev = -1;
 int g_occ = 0;
+
+template <int KJ>
+bool configure_kernel(int &occ) {
+    if (cudaFuncSetAttribute(pipe_kernel<KJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget) != cudaSuccess)
+        return false;
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, pipe_kernel<KJ>, kThreads, kSmemBudget) != cudaSuccess)
+        return false;
+    occ = std::min(occ, std::max(o, 1));
+    return true;
+}
 
 struct Shape {
     int P, lp, half, RT, RS, bps, scale_off, stage_bytes;
@@ -430,18 +443,16 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (g_configured_dev != di->device) {
-        if (cudaFuncSetAttribute(pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget) != cudaSuccess)
-            return Q8_ERR_CUDA;
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, pipe_kernel, kThreads, kSmemBudget) != cudaSuccess)
-            return Q8_ERR_CUDA;
-        g_occ = std::max(o, 1);
+        int o = 1 << 30;
+        if (!configure_kernel<12>(o) || !configure_kernel<16>(o)) return Q8_ERR_CUDA;
+        g_occ = o;
         g_configured_dev = di->device;
     }
     static thread_local PParams p;
     if (!layout_for(descs, count, p.S, p.slot_bytes, p.red_off, p.ctl_off, p.red_entry)) return Q8_ERR_UNSUPPORTED;
     double total_bytes = 0.0;
     int stages = 0;
+    bool wide_x = false;  // some matrix needs more than 12 x blocks per warp
     for (int i = 0; i < count; ++i) {
         PDesc &D = p.d[i];
         const int K = static_cast<int>(descs[i].K);
@@ -462,6 +473,7 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
         D.half = h.half;
         D.bps = h.bps;
         D.scale_off = h.scale_off;
+        wide_x = wide_x || h.half || h.bps > 12;
         D.stage_begin = stages;
         D.stages = (D.N + D.RT - 1) / D.RT;
         stages += D.stages;
@@ -487,7 +499,10 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
     }
     while (c < grid) p.cta_begin[++c] = stages;
     const size_t smem = static_cast<size_t>(p.ctl_off) + kCtlBytes;
-    pipe_kernel<<<grid, kThreads, smem, stream>>>(p);
+    if (wide_x)
+        pipe_kernel<16><<<grid, kThreads, smem, stream>>>(p);
+    else
+        pipe_kernel<12><<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 
