@@ -122,6 +122,24 @@ __device__ __forceinline__ void codes4_to_bf16x2(uint32_t w, uint32_t &lo, uint3
     hi = bf16x2_sub(ahi, bhi);
 }
 
+// Four int8 codes -> two f16x2 words, exactly.  binary16 has 10 fraction
+// bits, so 0x6400 | u is 1024 + u for a byte u = c ^ 0x80 = c + 128, and one
+// packed subtraction of 1152 (0x6480) leaves c.
+__device__ __forceinline__ void codes4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t plo = __byte_perm(u, 0x64646464u, 0x4140);   // [64 u1 64 u0]
+    const uint32_t phi = __byte_perm(u, 0x64646464u, 0x4342);   // [64 u3 64 u2]
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(plo), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(phi), "r"(0x64806480u));
+}
+
+// Two floats -> f16x2 (a in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
 // Four int8 codes -> four floats, exactly: 0x4B000000 | u is 2^23 + u for a
 // byte u, and u = c ^ 0x80 = c + 128.
 __device__ __forceinline__ void codes4_to_f32(uint32_t w, float &f0, float &f1, float &f2, float &f3) {
@@ -152,6 +170,17 @@ __device__ __forceinline__ void mma_bf16_16816(float &d0, float &d1, float &d2, 
                                                uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, binary16 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float &d0, float &d1, float &d2, float &d3,
+                                              uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

@@ -26,11 +26,16 @@
 //    8-row half tiles, three slots).  A warp's x slice stays in registers in
 //    the mma B-fragment layout (at most 16 blocks), reloaded only when the
 //    matrix changes.
-//  * Per 32-code block two mma.sync.m16n8k16 (bf16 in, fp32 out) with the
-//    weights as the 16-row A operand (lane (g, t) holds bytes [8t, 8t+8) of
-//    its rows) and x^T as B (columns = activation rows, zero past M).  Codes
-//    become bf16 exactly (|q| <= 127); each block's fp32 result is scaled by
-//    its binary16 scale.  The warps compute straight from shared memory.
+//  * Per 32-code block two mma.sync.m16n8k16 (binary16 in, fp32 out) with
+//    the weights as the 16-row A operand (lane (g, t) holds bytes [8t, 8t+8)
+//    of its rows) and x^T as B (columns = activation rows, zero past M).
+//    Codes become binary16 exactly (|q| <= 127) in three operations per pair;
+//    x is converted once per matrix: bf16 has 8 significant bits, so a value
+//    that is zero or of magnitude in [2^-17, 65504] is exact in binary16.  A
+//    block holding any other x value (tiny, huge, inf, nan) takes an exact
+//    bf16 path instead (codes -> bf16 by a sign split, x from global memory).
+//    Each block's fp32 result is scaled by its binary16 scale.  The warps
+//    compute straight from shared memory.
 //  * The P partial tiles of a stage are added in slice order by whichever of
 //    the P warps finishes last (shared-memory counter, nobody waits), so the
 //    results are deterministic and independent of batching.  A warp releases
@@ -101,6 +106,8 @@ __device__ __forceinline__ int find_pdesc(const PParams &p, int stage) {
 // of the mma tile) and, if TWO, row rb (upper half), straight from shared
 // memory.  FULL: both rows exist and the slice has BPW blocks, so nothing is
 // predicated.  acc[0..1]: row ra, activation rows 2t, 2t+1; acc[2..3]: rb.
+// x is binary16 (xr); blocks that binary16 cannot hold are zero there and
+// done by slow_blocks.
 template <int BPW, bool TWO, bool FULL, int KJ>
 __device__ __forceinline__ void tile_mma(const uint8_t *ca, const uint8_t *cb, const uint16_t *sa,
                                          const uint16_t *sb, bool va, bool vb, int nblk, int t,
@@ -122,15 +129,15 @@ __device__ __forceinline__ void tile_mma(const uint8_t *ca, const uint8_t *cb, c
             }
         }
         uint32_t a01, a23, a45, a67, b01 = 0u, b23 = 0u, b45 = 0u, b67 = 0u;
-        codes4_to_bf16x2(wa.x, a01, a23);
-        codes4_to_bf16x2(wa.y, a45, a67);
+        codes4_to_f16x2(wa.x, a01, a23);
+        codes4_to_f16x2(wa.y, a45, a67);
         if constexpr (TWO) {
-            codes4_to_bf16x2(wb.x, b01, b23);
-            codes4_to_bf16x2(wb.y, b45, b67);
+            codes4_to_f16x2(wb.x, b01, b23);
+            codes4_to_f16x2(wb.y, b45, b67);
         }
         float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-        mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xr[j].x, xr[j].y);
-        mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xr[j].z, xr[j].w);
+        mma_f16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xr[j].x, xr[j].y);
+        mma_f16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xr[j].z, xr[j].w);
         const float s_a = f16_bits_to_f32(ha);
         acc[0] = fmaf(s_a, d0, acc[0]);
         acc[1] = fmaf(s_a, d1, acc[1]);
@@ -138,6 +145,77 @@ __device__ __forceinline__ void tile_mma(const uint8_t *ca, const uint8_t *cb, c
             const float s_b = f16_bits_to_f32(hb);
             acc[2] = fmaf(s_b, d2, acc[2]);
             acc[3] = fmaf(s_b, d3, acc[3]);
+        }
+    }
+}
+
+// The blocks of a warp's slice whose x binary16 cannot hold (bits of
+// `slow`): exact bf16 products with x from global memory (xg, null past M).
+// Rare for activations, so kept out of line.
+__device__ __noinline__ float4 slow_blocks(const uint8_t *ca, const uint8_t *cb, const uint16_t *sa,
+                                           const uint16_t *sb, bool va, bool vb, int t, uint32_t slow,
+                                           const uint16_t *xg, float4 acc) {
+    while (slow) {
+        const int j = __ffs(slow) - 1;
+        slow &= slow - 1u;
+        uint2 wa = make_uint2(0u, 0u), wb = wa;
+        uint32_t ha = 0u, hb = 0u;
+        if (va) {
+            wa = *reinterpret_cast<const uint2 *>(ca + 32 * j + 8 * t);
+            ha = sa[j];
+        }
+        if (vb) {
+            wb = *reinterpret_cast<const uint2 *>(cb + 32 * j + 8 * t);
+            hb = sb[j];
+        }
+        uint4 xb = make_uint4(0u, 0u, 0u, 0u);
+        if (xg) xb = __ldg(reinterpret_cast<const uint4 *>(xg + 32 * j));
+        uint32_t a01, a23, a45, a67, b01, b23, b45, b67;
+        codes4_to_bf16x2(wa.x, a01, a23);
+        codes4_to_bf16x2(wa.y, a45, a67);
+        codes4_to_bf16x2(wb.x, b01, b23);
+        codes4_to_bf16x2(wb.y, b45, b67);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xb.x, xb.y);
+        mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xb.z, xb.w);
+        const float s_a = f16_bits_to_f32(ha), s_b = f16_bits_to_f32(hb);
+        acc.x = fmaf(s_a, d0, acc.x);
+        acc.y = fmaf(s_a, d1, acc.y);
+        acc.z = fmaf(s_b, d2, acc.z);
+        acc.w = fmaf(s_b, d3, acc.w);
+    }
+    return acc;
+}
+
+// x slice of activation row g (xg, null past M) as binary16 for the mma B
+// operand.  bf16 has 8 significant bits, so binary16 holds a bf16 value
+// exactly when it is zero or its magnitude lies in [2^-17, 65504] (below
+// 2^-14 as a subnormal that is still a multiple of 2^-24).  A block with any
+// other value (tiny, huge, inf, nan) is left zero and flagged in `slow` for
+// the exact bf16 path.
+template <int KJ>
+__device__ __forceinline__ void prep_x(const uint16_t *xg, int nblk, uint4 (&xr)[KJ], uint32_t &slow) {
+    slow = 0u;
+#pragma unroll
+    for (int j = 0; j < KJ; ++j) {
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        bool inexact = false;
+        if (xg && j < nblk) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xg + 32 * j));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float lo = bf16lo_f32(w4[q]);
+                const float hi = bf16hi_f32(w4[q]);
+                h[q] = f32x2_to_f16x2(lo, hi);
+                inexact = inexact || (lo != 0.f && !(fabsf(lo) >= 0x1p-17f && fabsf(lo) <= 65504.f)) ||
+                          (hi != 0.f && !(fabsf(hi) >= 0x1p-17f && fabsf(hi) <= 65504.f));
+            }
+        }
+        xr[j] = make_uint4(h[0], h[1], h[2], h[3]);
+        if (__any_sync(0xffffffffu, inexact)) {
+            slow |= 1u << j;
+            xr[j] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
 }
@@ -207,24 +285,25 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
     // ---- consumers --------------------------------------------------------------
     int d = find_pdesc(p, begin);
     int cur_d = -1;
-    uint4 xr[KJ];
+    uint4 xr[KJ];          // x slice of activation row g, binary16
     int kb0 = 0, nblk = 0;
+    uint32_t slow = 0u;    // blocks that take the exact bf16 path
     for (int i = begin, k = 0; i < end; ++i, ++k) {
         while (i >= p.d[d].stage_begin + p.d[d].stages) ++d;
         const PDesc &D = p.d[d];
         const int lp = D.lp;
         const int P = 1 << lp;
         if (d != cur_d) {
-            // this warp's x fragments: x[m = g][block kb0 + j][8t .. 8t+8), zero past M
+            // this warp's x fragments: x[m = g][block kb0 + j][8t .. 8t+8), zero
+            // past M; kept when the next matrix reads the same x slice
+            const int nkb0 = (warp & (P - 1)) * D.bps;
+            const int nnblk = max(0, min(D.nb - nkb0, D.bps));
+            const bool same = cur_d >= 0 && D.x == p.d[cur_d].x && D.ldx == p.d[cur_d].ldx && nkb0 == kb0 &&
+                              nnblk == nblk;
             cur_d = d;
-            kb0 = (warp & (P - 1)) * D.bps;
-            nblk = max(0, min(D.nb - kb0, D.bps));
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) {
-                xr[j] = make_uint4(0u, 0u, 0u, 0u);
-                if (g < M && j < nblk)
-                    xr[j] = __ldg(reinterpret_cast<const uint4 *>(D.x + g * D.ldx + (kb0 + j) * 32 + 8 * t));
-            }
+            kb0 = nkb0;
+            nblk = nnblk;
+            if (!same) prep_x<KJ>(g < M ? D.x + g * D.ldx + kb0 * 32 + 8 * t : nullptr, nblk, xr, slow);
         }
         const int slot = k % S;
         if (!mbar_wait_bounded(&full[slot], (k / S) & 1)) {
@@ -267,7 +346,15 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
             else
                 tile_mma<16, false, false, KJ>(ca, cb, sa, sb, va, vb, nblk, t, xr, acc);
         }
-
+        if (slow != 0u) {
+            const float4 r = slow_blocks(ca, cb, sa, sb, va, vb, t, slow,
+                                         g < M ? D.x + g * D.ldx + kb0 * 32 + 8 * t : nullptr,
+                                         make_float4(acc[0], acc[1], acc[2], acc[3]));
+            acc[0] = r.x;
+            acc[1] = r.y;
+            acc[2] = r.z;
+            acc[3] = r.w;
+        }
         // publish this warp's partial tile; the last of the tile's P warps adds
         // them in slice order and writes y
         const int tile = warp >> lp;

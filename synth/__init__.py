@@ -80,6 +80,25 @@ def activations(M: int, K: int, seed: int = 0, tag: str = "x") -> np.ndarray:
     return f32_to_bf16_bits(normal_f32((M, K), seed, tag))
 
 
+def wide_range_activations(M: int, K: int, seed: int = 0, tag: str = "xwide") -> np.ndarray:
+    """bf16 bits [M][K] of N(0, 1) draws times magnitudes spread over the whole
+    bf16 range: per element one of 2^-130 (bf16 subnormal), 2^-60, 2^-20, 1,
+    2^20, 2^60; every 7th element zero; row 0 keeps only the tiny magnitudes
+    and row 1 holds one huge element (2^100) among values near 1."""
+    r = rng(seed, tag)
+    g = normal_f32((M, K), seed, tag)
+    mags = np.array([2.0 ** -130, 2.0 ** -60, 2.0 ** -20, 1.0, 2.0 ** 20, 2.0 ** 60])
+    pick = r.integers(0, len(mags), size=(M, K))
+    x = g.astype(np.float64) * mags[pick]
+    x[:, ::7] = 0.0
+    if M > 0:
+        x[0] = g[0] * mags[r.integers(0, 2, size=K)]
+    if M > 1:
+        x[1] = g[1]
+        x[1, K // 3] = 2.0 ** 100
+    return f32_to_bf16_bits(x.astype(np.float32))
+
+
 def unit_activation(K: int, seed: int = 0, tag: str = "x_vocab") -> np.ndarray:
     """bf16 bits [1][K] of g/||g||_2, g ~ N(0,1)^K (RMS-normalised, times 1/sqrt(K))."""
     g = rng(seed, tag).standard_normal(size=K, dtype=np.float64)

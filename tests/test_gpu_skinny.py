@@ -69,6 +69,20 @@ def test_random_tolerance(oracle, variant, N, K, M):
     check_tol(y, y_ref, B, f"N={N} K={K} M={M} variant={variant}")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("N,K", [(300, 1536), (77, 4096), (130, 2048)])
+@pytest.mark.parametrize("M", [1, 2, 8, 16])
+def test_wide_range_activations(oracle, variant, N, K, M):
+    """Activations spanning the whole bf16 range, subnormals and zeros: the
+    binary16 fast path of the M <= 8 kernel has to hand such blocks to its
+    exact bf16 path, and every kernel stays within the tolerance."""
+    q, s, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"wr{N}.{K}"))
+    x = synth.wide_range_activations(M, K, 0, f"wrx{M}.{K}")
+    y_ref, B = oracle.matmul(q, s, x, threads=8)
+    (y,) = run_batch([(q, s, x)], M, variant)
+    check_tol(y, y_ref, B, f"wide range N={N} K={K} M={M} variant={variant}")
+
+
 def test_gemv_and_skinny_entry_points(oracle):
     from block_quantized_int8_gb300 import q8
     N, K = 1536, 4096
