@@ -21,9 +21,9 @@
 //    owns one slice (w % P) of two groups, one whole m16n8k16 tile.  A
 //    half-tile stage has 8/P groups and slices of at most 512: each warp owns
 //    one slice of one group, half a tile (the upper rows of the mma operand
-//    are zero and never converted).  Per K the host takes the shape with more
-//    bytes in flight (e.g. K = 1536: 32-row full tiles, two slots; K = 4096:
-//    8-row half tiles, three slots).  A warp's x slice stays in registers in
+//    are zero and never converted).  Full tiles are used whenever their
+//    slices fit (K <= 3072: e.g. K = 1536, 32 rows, two slots); otherwise
+//    half tiles (K = 4096: 8 rows, three slots).  A warp's x slice stays in registers in
 //    the mma B-fragment layout (at most 16 blocks), reloaded only when the
 //    matrix changes.
 //  * Per 32-code block two mma.sync.m16n8k16 (binary16 in, fp32 out) with
@@ -469,8 +469,10 @@ int slots_for(int stage_bytes, bool any_full) {
 
 // The stage shape of a matrix: full tiles (slices of at most 384, 128/P
 // rows) or half tiles (slices of at most 512, 64/P rows), P the fewest slices
-// that respect the slice width and fit two slots; of the two, the one with
-// more bytes in flight when the matrix is alone in a launch.
+// that respect the slice width and fit two slots; full tiles if they fit,
+// else (between half-tile shapes) the most bytes in flight.
+// The shape depends on K alone, so a matrix is summed in the same order
+// whatever else shares its launch (batched == separate calls, bit for bit).
 Shape shape_of(int K) {
     Shape best{};
     long best_score = -1;
@@ -486,7 +488,9 @@ Shape shape_of(int K) {
         }
         const int S = slots_for(h.stage_bytes, !half);
         if (S == 0) continue;
-        const long score = static_cast<long>(S) * h.stage_bytes;
+        // full tiles (12 x blocks per warp, two rows per lane) win whenever
+        // they fit: measured faster than half tiles with more slots
+        const long score = static_cast<long>(S) * h.stage_bytes + (half ? 0L : (1L << 40));
         if (score > best_score) {
             best = h;
             best_score = score;
