@@ -10,8 +10,8 @@
 //  * A "stage" is RT consecutive weight rows with their full K.  Rows of the
 //    row-major codes q[N][K] and scales s[N][K/32] are contiguous, so a stage
 //    is ONE bulk async copy of RT*K code bytes plus one of RT*K/16 scale bytes.
-//  * Each CTA owns a contiguous, byte-balanced range of the stages of all
-//    matrices (the host cuts the list so every CTA streams the same bytes).
+//  * Each CTA owns a contiguous range of the stages of all matrices, cut so
+//    every CTA gets the same work (bytes, weighted up for split rows).
 //  * Lane 0 of warp 0 also produces: it keeps kStages copies in flight
 //    (cp.async.bulk -> shared memory, completion on a "full" mbarrier) and
 //    refills a slot once every warp has released it ("empty" mbarrier).  A
@@ -53,6 +53,11 @@ constexpr int kScaleBytes = kCodeBytes / 16 + 16;  // RT * K / 16, plus up to 14
 constexpr int kStageBytes = kCodeBytes + kScaleBytes;
 constexpr int kMaxK = 8 * kSliceK;             // P <= 8
 constexpr int kMaxGrid = 1024;
+// Work of a stage for the partition, relative to its bytes: a matrix whose
+// rows are split over warps (P > 1) costs more per byte (narrower slices,
+// cross-warp combine).  1.2 measured best on the decode layer set
+// (K = 1536 and K = 4096 matrices in one launch: +3 % over byte balance).
+constexpr double kSplitCost = 1.2;
 constexpr int kJMax = 3;                       // 16-code chunks per lane per slice (1536 k)
 
 struct GDesc {
@@ -502,20 +507,20 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_stat
         D.stage_begin = stages;
         D.stages = (D.N + D.RT - 1) / D.RT;
         stages += D.stages;
-        total_bytes += static_cast<double>(D.N) * K * 1.0625;
+        total_bytes += static_cast<double>(D.N) * K * 1.0625 * (D.P > 1 ? kSplitCost : 1.0);
     }
     p.status = dev_status;
     p.count = count;
     p.total_stages = stages;
     if (stages == 0) return Q8_OK;
     const int grid = std::min(std::min(stages, di->sm_count * g_occ), kMaxGrid);
-    // cut the stage list into `grid` ranges of (nearly) equal bytes
+    // cut the stage list into `grid` ranges of (nearly) equal work
     int c = 0;
     double acc = 0.0;
     p.cta_begin[0] = 0;
     for (int i = 0; i < count && c < grid - 1; ++i) {
         const GDesc &D = p.d[i];
-        const double full = static_cast<double>(D.RT) * D.K * 1.0625;
+        const double full = static_cast<double>(D.RT) * D.K * 1.0625 * (D.P > 1 ? kSplitCost : 1.0);
         for (int st = 0; st < D.stages && c < grid - 1; ++st) {
             const int rows = std::min(D.RT, D.N - st * D.RT);
             acc += full * rows / D.RT;
