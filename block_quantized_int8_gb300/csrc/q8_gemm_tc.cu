@@ -7,21 +7,26 @@
 // "Parity lane" item 2; the weight tile is dequantised to bf16 in shared
 // memory so the tensor cores see a plain bf16 x bf16 product.
 //
-// One CTA computes a 128 (m) x 128 (n) tile of Y over all of K, in k-tiles of
-// 64, through a kStages-deep ring of shared-memory stages:
-//   warp 0, lane 0  TMA producer: for each k-tile, the x tile (bf16, 128 rows
-//                   x 128 bytes, 128-byte swizzle = the tensor core's K-major
-//                   layout) and the raw code tile (int8, 128 rows x 64 bytes)
-//                   via cp.async.bulk.tensor, completion on full_tma.
-//   warp 1, lane 0  MMA issuer: 4 x tcgen05.mma.kind::f16 (M=128, N=128,
-//                   K=16) per k-tile into a 128-column fp32 TMEM accumulator;
-//                   tcgen05.commit releases the stage (empty) and, after the
-//                   last k-tile, signals acc_full.
-//   warps 4-11      dequantisers: code tile (shared) x block scale (shared,
-//                   loaded once per CTA) -> bf16(s*q) written in the swizzled
-//                   K-major layout, fence.proxy.async, arrive on full_w; then
+// One CTA (one per SM) computes BMP x 128 rows (m) by BN columns (n) of Y over
+// all of K, in k-tiles of 64, through a ring of up to 8 shared-memory stages
+// (x tiles, raw code tile, dequantised weight tile):
+//   warp 0, lane 0  TMA producer: for each k-tile the BMP x tiles (bf16,
+//                   128 rows x 128 bytes each, 128-byte swizzle = the tensor
+//                   core's K-major layout) and the raw code tile (int8, BN
+//                   rows x 64 bytes) via cp.async.bulk.tensor, once the MMAs
+//                   of the stage's previous k-tile are done.
+//   warps 4-11      dequantisers: code tile x block scale (scales loaded once
+//                   per CTA) -> bf16(s*q) in the swizzled K-major layout of
+//                   the stage's weight tile, fence.proxy.async, arrive; then
 //                   the epilogue: tcgen05.ld of their 32 TMEM lanes (warp % 4)
 //                   and half of the columns each, fp32 -> bf16, store Y.
+//   warp 1, lane 0  MMA issuer: per k-tile and m-tile, 4 x tcgen05.mma.kind::f16
+//                   (M=128, N=BN, K=16) into fp32 TMEM accumulators; the BMP
+//                   m-tiles share the dequantised weight tile, so each weight
+//                   is converted once per BMP x 128 rows of x.  One
+//                   tcgen05.commit per k-tile frees the stage; a last one
+//                   signals acc_full.
+// The host picks (BMP, BN) = (2, 128), (1, 128) or (1, 64) to fill the SMs.
 // All waits are bounded; on expiry the CTA reports Q8_DEV_TIMEOUT, stops
 // issuing work, lets its copies and MMAs drain (bounded) and frees its TMEM.
 #include <cuda.h>
@@ -35,51 +40,47 @@ namespace q8 {
 
 namespace {
 
-constexpr int kBM = 128;          // rows of x / Y per tile (MMA M)
-constexpr int kBN = 128;          // weight rows per tile (MMA N)
+constexpr int kBM = 128;          // rows of x / Y per m-tile (MMA M)
 constexpr int kBK = 64;           // k per stage (128 bytes of bf16)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kThreads = 384;           // warps 0-1 roles, 2-3 idle, 4-11 dequantise + epilogue
 constexpr int kDeqThreads = 256;
-constexpr int kMaxScaleBytes = 48 * 1024;  // kBN * (K/32) * 2 -> K <= 6144
-constexpr int kTmemCols = kBN;             // fp32 accumulator columns
-constexpr size_t kTwoCtaSmem = 115712;      // (228 KB - 2 x 1 KB reserved) / 2
+constexpr int kMaxScaleBytes = 48 * 1024;  // 128 rows * (K/32) * 2 -> K <= 6144
+constexpr int kSmemMax = 232448;           // dynamic shared memory of one CTA per SM
+constexpr int kXTile = kBM * 128;          // one m-tile of x per stage
 
-constexpr int kXBytes = kBM * 128;
-constexpr int kWBytes = kBN * 128;
-constexpr int kCBytes = kBN * 64;
-constexpr int kStageBytes = kXBytes + kWBytes + kCBytes;
-
-// Shared memory: [x tiles][w tiles][code tiles] for S stages (S chosen at
-// launch: 2 when two CTAs fit on an SM, else kStages), then the scales, then
-// this control block.  Tiles start on 1024-byte boundaries.
+// Shared memory: [stages: BMP x tiles, weight tile, code tile][scales][ctl],
+// tiles on 1024-byte boundaries.
 struct GemmCtl {
-    uint64_t full_tma[kStages];
-    uint64_t full_w[kStages];
-    uint64_t empty[kStages];
+    uint64_t full_tma[kMaxStages];   // x and codes landed (TMA bytes)
+    uint64_t full_w[kMaxStages];     // weight tile dequantised (8 warps)
+    uint64_t empty[kMaxStages];      // MMAs reading the stage done (commit)
     uint64_t scales_full;
     uint64_t acc_full;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
 
+template <int BMP, int BN>
 struct GemmSmem {
+    static constexpr int kW = BN * 128;
+    static constexpr int kStage = BMP * kXTile + kW + BN * 64;
     uint8_t *base;
-    int S;
-    __device__ __forceinline__ uint8_t *x(int s) const { return base + s * kXBytes; }
-    __device__ __forceinline__ uint8_t *w(int s) const { return base + S * kXBytes + s * kWBytes; }
-    __device__ __forceinline__ uint8_t *codes(int s) const { return base + S * (kXBytes + kWBytes) + s * kCBytes; }
-    __device__ __forceinline__ uint8_t *scales() const { return base + S * kStageBytes; }
+    int ST;
+    __device__ __forceinline__ uint8_t *x(int s, int i) const { return base + s * kStage + i * kXTile; }
+    __device__ __forceinline__ uint8_t *w(int s) const { return base + s * kStage + BMP * kXTile; }
+    __device__ __forceinline__ uint8_t *codes(int s) const { return base + s * kStage + BMP * kXTile + kW; }
+    __device__ __forceinline__ uint8_t *scales() const { return base + ST * kStage; }
 };
 
 struct GemmParams {
     CUtensorMap tm_x;      // bf16 [M][ldx], box {64, 128}, 128-byte swizzle
-    CUtensorMap tm_q;      // int8 [N][K],   box {64, 128}, no swizzle
+    CUtensorMap tm_q;      // int8 [N][K],   box {64, BN}, no swizzle
     const uint16_t *s;     // binary16 scales [N][K/32]
     uint16_t *y;           // bf16 [M][ldy]
     uint32_t *status;
     int32_t M, N, K, nb;
-    int32_t S;             // pipeline stages
+    int32_t ST;            // ring stages
     int32_t ctl_off;       // byte offset of the control block from the aligned base
     int64_t ldy;
 };
@@ -106,16 +107,20 @@ __device__ __forceinline__ uint64_t sw128_desc(const void *tile) {
 }
 
 // Instruction descriptor, kind::f16: D f32, A bf16, B bf16, both K-major,
-// N = kBN, M = kBM.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+// N = BN, M = kBM.
+template <int BN>
+constexpr uint32_t idesc_for() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+           (static_cast<uint32_t>(kBM >> 4) << 24);
+}
 
+template <int BN>
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        :: "r"(tmem_d), "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
+        :: "r"(tmem_d), "l"(da), "l"(db), "r"(idesc_for<BN>()), "r"(accumulate));
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -158,26 +163,28 @@ __device__ __forceinline__ bool wait_or_abort(GemmCtl &sm, uint64_t *bar, uint32
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+template <int BMP, int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // the tiles need 1024-byte alignment (128-byte swizzle atoms)
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const GemmSmem L{base, p.S};
+    const GemmSmem<BMP, BN> L{base, p.ST};
     GemmCtl &sm = *reinterpret_cast<GemmCtl *>(base + p.ctl_off);
-    const int S = p.S;
+    constexpr int kTmemCols = BMP * BN;
+    const int ST = p.ST;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int n0 = blockIdx.x * kBN;
-    const int m0 = blockIdx.y * kBM;
+    const int n0 = blockIdx.x * BN;
+    const int m0 = blockIdx.y * (BMP * kBM);
     const int KT = (p.K + kBK - 1) / kBK;
-    const int rows_n = min(kBN, p.N - n0);
+    const int rows_n = min(BN, p.N - n0);
 
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(&sm.full_tma[i], 1);
-            mbar_init(&sm.full_w[i], kDeqThreads / 32);
+            mbar_init(&sm.full_w[i], kDeqThreads / 64);  // the 4 warps of one group
             mbar_init(&sm.empty[i], 1);
         }
         mbar_init(&sm.scales_full, 1);
@@ -205,47 +212,57 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
             *reinterpret_cast<uint16_t *>(L.scales() + b) = *reinterpret_cast<const uint16_t *>(ssrc + b);
         mbar_arrive_expect_tx(&sm.scales_full, sb16);
         if (sb16) bulk_g2s(L.scales(), ssrc, sb16, &sm.scales_full);
+        // an m-tile wholly past M is not loaded (its rows are never stored)
+        const int mtiles = min(BMP, (p.M - m0 + kBM - 1) / kBM);
         for (int kt = 0; kt < KT; ++kt) {
-            const int st = kt % S;
-            if (kt >= S && !wait_or_abort(sm, &sm.empty[st], ((kt / S) - 1) & 1, p.status)) break;
-            mbar_arrive_expect_tx(&sm.full_tma[st], kBM * 128 + kBN * 64);
-            tma_load_2d(L.x(st), &p.tm_x, kt * kBK, m0, &sm.full_tma[st]);
+            const int st = kt % ST;
+            if (kt >= ST && !wait_or_abort(sm, &sm.empty[st], ((kt / ST) - 1) & 1, p.status)) break;
+            mbar_arrive_expect_tx(&sm.full_tma[st], mtiles * kXTile + BN * 64);
+            for (int i = 0; i < mtiles; ++i) tma_load_2d(L.x(st, i), &p.tm_x, kt * kBK, m0 + i * kBM, &sm.full_tma[st]);
             tma_load_2d(L.codes(st), &p.tm_q, kt * kBK, n0, &sm.full_tma[st]);
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------- MMA issuer
+        // full_w implies full_tma: the dequantisers waited for the stage's
+        // TMA bytes (x included) before they arrived
         for (int kt = 0; kt < KT; ++kt) {
-            const int st = kt % S;
-            const uint32_t par = (kt / S) & 1;
-            if (!wait_or_abort(sm, &sm.full_tma[st], par, p.status)) break;
-            if (!wait_or_abort(sm, &sm.full_w[st], par, p.status)) break;
+            const int st = kt % ST;
+            if (!wait_or_abort(sm, &sm.full_w[st], (kt / ST) & 1, p.status)) break;
             tc_fence_after();
-            const uint64_t da = sw128_desc(L.x(st));
             const uint64_t db = sw128_desc(L.w(st));
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                // advance 16 elements (32 bytes) along K inside the swizzled rows
-                umma_bf16(tmem, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2),
-                          (kt > 0 || kk > 0) ? 1u : 0u);
+            for (int i = 0; i < BMP; ++i) {
+                const uint64_t da = sw128_desc(L.x(st, i));
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    // advance 16 elements (32 bytes) along K inside the swizzled rows
+                    umma_bf16<BN>(tmem + static_cast<uint32_t>(i * BN), da + static_cast<uint64_t>(kk * 2),
+                                  db + static_cast<uint64_t>(kk * 2), (kt > 0 || kk > 0) ? 1u : 0u);
+                }
             }
             umma_commit(&sm.empty[st]);
         }
         umma_commit(&sm.acc_full);
     } else if (warp >= 4) {
         // ------------------------------------------------ dequantise, epilogue
-        const int t = tid - 128;  // 0..255
+        // two groups of 4 warps take alternate k-tiles (more independent work
+        // per warp, and the groups overlap)
+        const int grp = (warp - 4) >> 2;
+        const int t = tid - 128 - 128 * grp;  // 0..127
         bool ok = wait_or_abort(sm, &sm.scales_full, 0, p.status);
         const uint16_t *sc = reinterpret_cast<const uint16_t *>(L.scales());
-        for (int kt = 0; ok && kt < KT; ++kt) {
-            const int st = kt % S;
-            if (!wait_or_abort(sm, &sm.full_tma[st], (kt / S) & 1, p.status)) {
+        for (int kt = grp; ok && kt < KT; kt += 2) {
+            const int st = kt % ST;
+            // the stage (and its weight tile) is free again: the producer
+            // waited for the MMAs of k-tile kt - ST before refilling it
+            if (!wait_or_abort(sm, &sm.full_tma[st], (kt / ST) & 1, p.status)) {
                 ok = false;
                 break;
             }
-            // 128 rows x 4 chunks of 16 codes; task j -> row j/4, chunk j%4
+            // BN rows x 4 chunks of 16 codes; task j -> row j/4, chunk j%4
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int j = t + kDeqThreads * i;
+            for (int i = 0; i < BN * 4 / (kDeqThreads / 2); ++i) {
+                const int j = t + (kDeqThreads / 2) * i;
                 const int row = j >> 2;
                 const int c = j & 3;  // 16-code chunk within the 64-code k-tile
                 const int kb = kt * 2 + (c >> 1);  // block index along K
@@ -269,35 +286,42 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
             }
             fence_proxy_async_smem();  // generic writes -> visible to the tensor core
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.full_w[st])) : "memory");
+            if (lane == 0)
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.full_w[st])) : "memory");
         }
-        // epilogue: TMEM lanes 32*(warp%4) .. +31 hold rows m0 + 32*(warp%4) + lane;
-        // warps 4-7 drain columns [0, 64), warps 8-11 columns [64, 128)
+        // epilogue: TMEM lanes 32*(warp%4) .. +31 hold rows 32*(warp%4) + lane
+        // of each m-tile; warps 4-7 drain columns [0, BN/2), warps 8-11 the rest
         if (ok && wait_or_abort(sm, &sm.acc_full, 0, p.status)) {
             tc_fence_after();
-            const int r = 32 * (warp & 3) + lane;
-            const int m = m0 + r;
-            const int cbeg = warp < 8 ? 0 : kBN / 2;
+            const int cbeg = warp < 8 ? 0 : BN / 2;
 #pragma unroll 1
-            for (int c0 = cbeg; c0 < cbeg + kBN / 2; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(c0), v);
-                if (m < p.M) {
-                    uint16_t *yrow = p.y + static_cast<int64_t>(m) * p.ldy + n0 + c0;
-                    if (n0 + c0 + 32 <= p.N) {
+            for (int i = 0; i < BMP; ++i) {
+                const int m = m0 + i * kBM + 32 * (warp & 3) + lane;
+#pragma unroll 1
+                for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                                  static_cast<uint32_t>(i * BN + c0), v);
+                    if (m < p.M) {
+                        uint16_t *yrow = p.y + static_cast<int64_t>(m) * p.ldy + n0 + c0;
+                        if (n0 + c0 + 32 <= p.N) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const uint4 o = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7])));
-                            *reinterpret_cast<uint4 *>(yrow + 8 * q4) = o;
-                        }
-                    } else {
-                        for (int e = 0; e < 32 && n0 + c0 + e < p.N; ++e) {
-                            const uint32_t h = pack_bf16x2(__uint_as_float(v[e]), 0.f);
-                            yrow[e] = static_cast<uint16_t>(h & 0xFFFFu);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const uint4 o = make_uint4(
+                                    pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7])));
+                                *reinterpret_cast<uint4 *>(yrow + 8 * q4) = o;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                if (n0 + c0 + e < p.N) {
+                                    const uint32_t h = pack_bf16x2(__uint_as_float(v[e]), 0.f);
+                                    yrow[e] = static_cast<uint16_t>(h & 0xFFFFu);
+                                }
+                            }
                         }
                     }
                 }
@@ -308,9 +332,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
     // ------------------------------------------------------------- teardown
     // If a role gave up, let in-flight copies and MMAs land (bounded) first.
     if (tid == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort_flag)) {
-        for (int i = 0; i < S; ++i) {
-            (void)mbar_try_wait(&sm.full_tma[i], 0);
-        }
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 1000000ull) {
         }
@@ -343,7 +364,7 @@ EncodeTiledFn encode_tiled() {
 }
 
 bool encode_maps(GemmParams &p, const int8_t *q, const uint16_t *x, int64_t N, int64_t K, int64_t M,
-                 int64_t ldx) {
+                 int64_t ldx, int BN) {
     const EncodeTiledFn cuTensorMapEncodeTiled = encode_tiled();
     if (!cuTensorMapEncodeTiled) return false;
     {
@@ -360,7 +381,7 @@ bool encode_maps(GemmParams &p, const int8_t *q, const uint16_t *x, int64_t N, i
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-        const cuuint32_t box[2] = {kBK, kBN};
+        const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
         const cuuint32_t estr[2] = {1, 1};
         if (cuTensorMapEncodeTiled(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(q), dims, strides,
                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -373,33 +394,53 @@ bool encode_maps(GemmParams &p, const int8_t *q, const uint16_t *x, int64_t N, i
 
 int g_configured_dev = -1;
 
+template <int BMP, int BN>
+bool configure() {
+    return cudaFuncSetAttribute(gemm_tc_kernel<BMP, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) ==
+           cudaSuccess;
+}
+
+// Shared memory of a (BMP, BN) launch with ST TMA stages, or 0 if even two do
+// not fit; sets ST and the control block offset.
+template <int BMP, int BN>
+size_t smem_for(int64_t nb, int &ST, int &ctl_off) {
+    using L = GemmSmem<BMP, BN>;
+    const int scale_bytes = static_cast<int>((static_cast<int64_t>(BN) * nb * 2 + 1023) / 1024 * 1024);
+    const int fixed = 1024 + scale_bytes + static_cast<int>(sizeof(GemmCtl));
+    ST = std::min(kMaxStages, (kSmemMax - fixed) / L::kStage);
+    if (ST < 2) return 0;
+    ctl_off = ST * L::kStage + scale_bytes;
+    return static_cast<size_t>(1024 + ctl_off + sizeof(GemmCtl));
+}
+
+template <int BMP, int BN>
+q8_status run(GemmParams &p, const int8_t *q, const uint16_t *x, int64_t N, int64_t K, int64_t M, int64_t ldx,
+              cudaStream_t stream) {
+    int ST = 0, ctl_off = 0;
+    const size_t smem = smem_for<BMP, BN>(p.nb, ST, ctl_off);
+    if (smem == 0) return Q8_ERR_UNSUPPORTED;
+    if (!encode_maps(p, q, x, N, K, M, ldx, BN)) return Q8_ERR_CUDA;
+    p.ST = ST;
+    p.ctl_off = ctl_off;
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BMP * kBM - 1) / (BMP * kBM)));
+    gemm_tc_kernel<BMP, BN><<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+}
+
 }  // namespace
 
 q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
-                         int32_t M, uint16_t *y, int64_t ldy, uint32_t *dev_status, cudaStream_t stream) {
+                         int32_t M, uint16_t *y, int64_t ldy, int32_t tile, uint32_t *dev_status,
+                         cudaStream_t stream) {
     const int64_t nb = K / 32;
-    if (static_cast<int64_t>(kBN) * nb * 2 > kMaxScaleBytes) return Q8_ERR_UNSUPPORTED;  // K > 6144
+    if (static_cast<int64_t>(kBM) * nb * 2 > kMaxScaleBytes) return Q8_ERR_UNSUPPORTED;  // K > 6144
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
-    // two CTAs per SM (2 stages each) when they fit, so one CTA's prologue and
-    // epilogue overlap the other's main loop; else one CTA with kStages stages
-    const int scale_bytes = static_cast<int>((static_cast<int64_t>(kBN) * nb * 2 + 1023) / 1024 * 1024);
-    auto smem_for = [&](int S) {
-        return static_cast<size_t>(1008 + S * kStageBytes + scale_bytes) + sizeof(GemmCtl);
-    };
-    int S = 2;
-    if (smem_for(2) > kTwoCtaSmem) S = kStages;
-    const size_t smem = smem_for(S);
     if (g_configured_dev != di->device) {
-        // the largest layout any supported K can need
-        const size_t smem_max = 1008 + static_cast<size_t>(kStages) * kStageBytes + kMaxScaleBytes + sizeof(GemmCtl);
-        if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_max)) != cudaSuccess)
-            return Q8_ERR_CUDA;
+        if (!configure<2, 128>() || !configure<1, 128>() || !configure<1, 64>()) return Q8_ERR_CUDA;
         g_configured_dev = di->device;
     }
     GemmParams p;
-    if (!encode_maps(p, q, x, N, K, M, ldx)) return Q8_ERR_CUDA;
     p.s = s;
     p.y = y;
     p.status = dev_status;
@@ -408,11 +449,21 @@ q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t 
     p.K = static_cast<int32_t>(K);
     p.nb = static_cast<int32_t>(nb);
     p.ldy = ldy;
-    p.S = S;
-    p.ctl_off = S * kStageBytes + scale_bytes;
-    const dim3 grid(static_cast<unsigned>((N + kBN - 1) / kBN), static_cast<unsigned>((M + kBM - 1) / kBM));
-    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+    // tile shape: two m-tiles per weight tile if that still gives most SMs a
+    // CTA, else one; 64-wide n-tiles for short N
+    if (tile == Q8_GEMM_TILE_AUTO) {
+        auto ctas = [&](int bmp, int bn) { return ((N + bn - 1) / bn) * ((M + bmp * kBM - 1) / (bmp * kBM)); };
+        const int64_t want = static_cast<int64_t>(di->sm_count) * 4 / 5;
+        if (ctas(2, 128) >= want)
+            tile = Q8_GEMM_TILE_256x128;
+        else if (ctas(1, 128) >= want || ctas(1, 128) >= ctas(1, 64))
+            tile = Q8_GEMM_TILE_128x128;
+        else
+            tile = Q8_GEMM_TILE_128x64;
+    }
+    if (tile == Q8_GEMM_TILE_256x128) return run<2, 128>(p, q, x, N, K, M, ldx, stream);
+    if (tile == Q8_GEMM_TILE_128x128) return run<1, 128>(p, q, x, N, K, M, ldx, stream);
+    return run<1, 64>(p, q, x, N, K, M, ldx, stream);
 }
 
 }  // namespace q8

@@ -30,10 +30,11 @@ Q8_DEV_TIMEOUT = 0x4
 Q8_SKINNY_MAX_M = 32
 Q8_MAX_BATCH = 64
 Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA = 0, 1, 2
+Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_128x64 = 0, 1, 2, 3
 
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
            "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
-           "q8_abi_version", "q8_gemm_skinny_noalloc")
+           "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex")
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -70,12 +71,13 @@ def lib():
         L.q8_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32, I32]
         L.q8_linear_batch_workspace_size.restype = SZ
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
+        L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, U32P, P]
         L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_status_str.argtypes = [ctypes.c_int]
         L.q8_status_str.restype = ctypes.c_char_p
         L.q8_abi_version.restype = I32
         for name in ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
-                     "q8_linear_batch_ex", "q8_gemm", "q8_gemm_skinny_noalloc"):
+                     "q8_linear_batch_ex", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -232,15 +234,16 @@ def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None
     _check(st, "q8_linear_batch")
 
 
-def q8_gemm(q, s, x, y=None, dev_status=None, stream=None):
-    """y[M, N] (bf16) = x[M, K] @ dequant(q, s)^T for M > 32 (tcgen05 path)."""
+def q8_gemm(q, s, x, y=None, dev_status=None, stream=None, tile=0):
+    """y[M, N] (bf16) = x[M, K] @ dequant(q, s)^T for M > 32 (tcgen05 path);
+    `tile` is one of the Q8_GEMM_TILE_* shapes (0: automatic)."""
     _cuda(q, "q", (torch.int8,), 2)
     _cuda(x, "x", _B16, 2)
     N, K = q.shape
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
-    st = lib().q8_gemm(_p(q), _p(s), N, K, _p(x), x.stride(0), M, _p(y), y.stride(0), _p(dev_status),
-                       _stream(stream))
+    st = lib().q8_gemm_ex(_p(q), _p(s), N, K, _p(x), x.stride(0), M, _p(y), y.stride(0), int(tile),
+                          _p(dev_status), _stream(stream))
     _check(st, "q8_gemm")
     return y

@@ -179,6 +179,25 @@ q8_status q8_gemm(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                   uint16_t *y, int64_t ldy,
                   uint32_t *dev_status, q8_stream_t stream);
 
+/* Tile shapes of q8_gemm (the _ex entry point): one CTA per SM computes
+ * 2 x 128 rows of x against 128 weight rows (each dequantised weight tile
+ * serves both 128-row halves), 128 x 128, or 128 x 64 (short N). */
+#define Q8_GEMM_TILE_AUTO     0   /* the first of the three that fills most SMs */
+#define Q8_GEMM_TILE_256x128  1
+#define Q8_GEMM_TILE_128x128  2
+#define Q8_GEMM_TILE_128x64   3
+
+/*
+ * q8_gemm_ex -- q8_gemm with an explicit tile shape (Q8_GEMM_TILE_*).  Every
+ * shape computes the same values bit for bit (each output is one fp32 sum
+ * over K in k order); the choice only changes speed.  Unknown `tile`:
+ * Q8_ERR_ARG.
+ */
+q8_status q8_gemm_ex(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                     const uint16_t *x, int64_t ldx, int32_t M,
+                     uint16_t *y, int64_t ldy, int32_t tile,
+                     uint32_t *dev_status, q8_stream_t stream);
+
 /*
  * q8_gemm_skinny_noalloc -- q8_gemm_skinny for callers that cannot allocate
  * device memory when they run the matmul (a fixed memory pool, a loop that

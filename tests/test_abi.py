@@ -114,6 +114,10 @@ def test_gemm_validation(L):
     assert f(A, A, 64, 48, A, 64, 64, A, 64, None, None) == q8.Q8_ERR_SHAPE
     assert f(A, A, 64, 64, A, 64, 64, A, 60, None, None) == q8.Q8_ERR_SHAPE
     assert f(A, A, 64, 64, A, 64, 64, A + 8, 64, None, None) == q8.Q8_ERR_ALIGN
+    g = L.q8_gemm_ex
+    for tile in (-1, 4, 99):
+        assert g(A, A, 64, 64, A, 64, 64, A, 64, tile, None, None) == q8.Q8_ERR_ARG
+    assert g(A, A, 64, 48, A, 64, 64, A, 64, q8.Q8_GEMM_TILE_128x64, None, None) == q8.Q8_ERR_SHAPE
 
 
 def test_workspace_sizes(L):

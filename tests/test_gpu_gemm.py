@@ -22,7 +22,10 @@ def bf16_to_f64(b: np.ndarray) -> np.ndarray:
     return synth.bf16_bits_to_f32(b).astype(np.float64)
 
 
-def run_gemm(qn, sn, xn):
+TILES = [0, 1, 2, 3]  # Q8_GEMM_TILE_AUTO, 256x128, 128x128, 128x64
+
+
+def run_gemm(qn, sn, xn, tile=0):
     from block_quantized_int8_gb300 import q8
     q, s = weights_dev(qn, sn)
     x = x_dev(xn)
@@ -32,20 +35,21 @@ def run_gemm(qn, sn, xn):
     ldy = (N + 7) // 8 * 8
     ybuf = torch.full((M, ldy), float("nan"), dtype=torch.bfloat16, device="cuda")
     y = ybuf[:, :N]
-    q8.q8_gemm(q, s, x, y, dev_status=st)
+    q8.q8_gemm(q, s, x, y, dev_status=st, tile=tile)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return ybuf.cpu().view(torch.int16).numpy().view(np.uint16)[:, :N]
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (256, 384, 1536), (200, 300, 96), (33, 129, 4096),
-                                   (512, 1536, 4096)])
-def test_gemm_exact_cases(oracle, M, N, K):
+                                   (512, 1536, 4096), (300, 520, 160)])
+def test_gemm_exact_cases(oracle, M, N, K, tile):
     q, s, x = synth.exact_case(N, K, M, 0, f"gx{M}.{N}.{K}")
     y_ref, _ = oracle.matmul(q, s, x, threads=8)
     # exact sums are small integers times powers of two: fp32 holds them exactly,
     # so the only rounding is the final bf16 one
-    got = run_gemm(q, s, x)
+    got = run_gemm(q, s, x, tile)
     assert np.array_equal(got, bf16_rn_bits(y_ref))
 
 
@@ -64,14 +68,25 @@ def test_gemm_prefill_full_size_sampled(oracle, K, N):
     assert np.all(err <= lim), f"max err {err.max()}, max (err - ulp/2)/B {ratio:.3e}"
 
 
-@pytest.mark.parametrize("M,N,K", [(40, 520, 1536), (300, 77, 160), (129, 1000, 4096)])
-def test_gemm_ragged_tolerance(oracle, M, N, K):
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("M,N,K", [(40, 520, 1536), (300, 77, 160), (129, 1000, 4096), (257, 130, 6144)])
+def test_gemm_ragged_tolerance(oracle, M, N, K, tile):
     qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"gr{M}.{N}.{K}"))
     xn = synth.activations(M, K, 0, f"grx{M}.{K}")
-    got = bf16_to_f64(run_gemm(qn, sn, xn))
+    got = bf16_to_f64(run_gemm(qn, sn, xn, tile))
     y_ref, B = oracle.matmul(qn, sn, xn, threads=16)
     half_ulp = np.abs(bf16_to_f64(bf16_rn_bits(y_ref))) * 2.0 ** -8
     assert np.all(np.abs(got - y_ref) <= TOL_REL * B + TOL_ABS + half_ulp)
+
+
+def test_gemm_tiles_agree_bitwise(oracle):
+    """Every tile shape sums each output over K in the same order."""
+    N, K, M = 520, 1536, 300
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, "gtile"))
+    xn = synth.activations(M, K, 0, "gtilex")
+    outs = [run_gemm(qn, sn, xn, t) for t in TILES]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
 
 
 def test_gemm_deterministic(oracle):
