@@ -1,6 +1,7 @@
 // q8_internal.h -- host-side declarations shared by the libq8 translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -50,6 +51,15 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_stat
 // 1 <= M <= 8 bulk-copy pipeline with warp MMA (q8_pipe.cu): K <= 4096.
 bool pipe_supported(const q8_linear_desc *descs, int count, int M);
 q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
+
+// 9 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256, <= 8192.
+bool tile_supported(const q8_linear_desc *descs, int count, int M);
+q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
+
+// 2-D TMA tensor map over a row-major [outer][inner] array of 1- or 2-byte
+// elements (q8_tmap.cu; cached by parameters).  false if encoding fails.
+bool encode_2d(CUtensorMap *map, int elem_bytes, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);

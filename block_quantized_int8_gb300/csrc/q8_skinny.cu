@@ -388,8 +388,9 @@ q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int varia
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     // M = 1: the CUDA-core bulk-copy GEMV (AUTO, SIMT); M <= 8: the warp-MMA
-    // bulk-copy pipeline (AUTO for M >= 2, MMA for any M <= 8); otherwise the
-    // general tile kernel below
+    // bulk-copy pipeline (AUTO for M >= 2, MMA for any M <= 8); M = 9..32:
+    // the TMA-fed chunked tile kernel (K % 256 == 0); otherwise the general
+    // kernel below
     if (M == 1 && variant != Q8_VARIANT_MMA && gemv_supported(descs, count))
         return launch_gemv(descs, count, dev_status, stream);
     if (M <= 8 && variant != Q8_VARIANT_SIMT && pipe_supported(descs, count, M))
@@ -398,6 +399,10 @@ q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int varia
     const size_t need = plan_skinny(descs, count, M, plans);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return Q8_ERR_ALIGN;
+    // 9 <= M <= 32 with K a multiple of 256: the chunked tile kernel (needs
+    // no workspace, but the call keeps the documented workspace contract)
+    if (M > 8 && variant != Q8_VARIANT_SIMT && tile_supported(descs, count, M))
+        return launch_tile(descs, count, M, dev_status, stream);
 
     BatchParams p;
     int items = 0;

@@ -67,7 +67,7 @@ typedef enum q8_status {
 #define Q8_MAX_BATCH 64      /* most descriptors per q8_linear_batch call */
 
 /* Kernel variants for the M <= 32 path (the _ex entry points). */
-#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: warp-MMA pipeline; M > 8: warp-MMA tiles */
+#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: warp-MMA pipeline; M > 8: TMA-fed warp-MMA tiles */
 #define Q8_VARIANT_SIMT 1    /* CUDA-core FFMA: codes dequantised in registers, one FMA per weight per row */
 #define Q8_VARIANT_MMA  2    /* warp mma.sync bf16 on exact bf16 codes, block scale applied in fp32 */
 

@@ -182,10 +182,10 @@ def test_layer_set_batch_sampled(oracle):
 # ---------------------------------------------------------------------------
 # determinism, graph replay, batch == separate calls
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [3, 20])
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_batch_equals_separate_calls_bitwise(oracle, variant):
-    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 64)]
-    M = 3
+def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
+    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 256)]
     mats_np = []
     for i, (N, K) in enumerate(shapes):
         qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"bs{i}"))
