@@ -463,11 +463,7 @@ int g_occ = 0;
 
 }  // namespace
 
-bool gemv_supported(const q8_linear_desc *descs, int count) {
-    for (int i = 0; i < count; ++i)
-        if (descs[i].K > kMaxK) return false;
-    return true;
-}
+bool gemv_k_supported(int64_t K) { return K <= kMaxK; }
 
 q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();

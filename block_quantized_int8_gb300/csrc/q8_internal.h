@@ -44,22 +44,26 @@ struct SplitPlan {
 // Plans every descriptor and returns the workspace bytes needed.
 size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans);
 
-// M = 1 bulk-copy pipeline (q8_gemv.cu): matrices with K <= 16384.
-bool gemv_supported(const q8_linear_desc *descs, int count);
+// M = 1 bulk-copy pipeline (q8_gemv.cu): matrices with K <= 12288.
+bool gemv_k_supported(int64_t K);
 q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_status, cudaStream_t stream);
 
 // 1 <= M <= 8 bulk-copy pipeline with warp MMA (q8_pipe.cu): K <= 4096.
-bool pipe_supported(const q8_linear_desc *descs, int count, int M);
+bool pipe_k_supported(int64_t K);
 q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
 
-// 9 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256, <= 8192.
-bool tile_supported(const q8_linear_desc *descs, int count, int M);
+// 2 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256.
+bool tile_k_supported(int64_t K);
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
 
 // 2-D TMA tensor map over a row-major [outer][inner] array of 1- or 2-byte
 // elements (q8_tmap.cu; cached by parameters).  false if encoding fails.
 bool encode_2d(CUtensorMap *map, int elem_bytes, const void *base, uint64_t inner, uint64_t outer,
                uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+// Rank-2 or rank-3 map: dims[0] innermost, stride_bytes[i] the byte stride of
+// dims[i + 1], box[] the box extent per dimension.
+bool encode_tmap(CUtensorMap *map, int elem_bytes, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *stride_bytes, const uint32_t *box, bool swizzle128);
 
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);

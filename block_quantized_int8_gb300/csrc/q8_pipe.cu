@@ -191,6 +191,16 @@ __device__ __noinline__ float4 slow_blocks(const uint8_t *ca, const uint8_t *cb,
     return acc;
 }
 
+// bf16 bits b that binary16 holds exactly: zero, or |b| in [2^-17, 65504]
+// (biased exponent >= 110 and magnitude bits <= 0x477F = 65280, the largest
+// bf16 not above 65504); NaN and infinity fail the second test.  Integer
+// compares only (measured: the same test on floats made the x preparation
+// at the head of each CTA several times slower).
+__device__ __forceinline__ bool bf16_fits_f16(uint32_t b) {
+    const uint32_t m = b & 0x7FFFu;
+    return m == 0u || m - 0x3700u <= 0x477Fu - 0x3700u;
+}
+
 // x slice of activation row g (xg, null past M) as binary16 for the mma B
 // operand.  bf16 has 8 significant bits, so binary16 holds a bf16 value
 // exactly when it is zero or its magnitude lies in [2^-17, 65504] (below
@@ -200,20 +210,21 @@ __device__ __noinline__ float4 slow_blocks(const uint8_t *ca, const uint8_t *cb,
 template <int KJ>
 __device__ __forceinline__ void prep_x(const uint16_t *xg, int nblk, uint4 (&xr)[KJ], uint32_t &slow) {
     slow = 0u;
+    // all loads first (independent, so they overlap), then the conversions
+#pragma unroll
+    for (int j = 0; j < KJ; ++j)
+        xr[j] = (xg && j < nblk) ? __ldg(reinterpret_cast<const uint4 *>(xg + 32 * j)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < KJ; ++j) {
         uint32_t h[4] = {0u, 0u, 0u, 0u};
         bool inexact = false;
-        if (xg && j < nblk) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xg + 32 * j));
+        {
+            const uint4 v = xr[j];
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float lo = bf16lo_f32(w4[q]);
-                const float hi = bf16hi_f32(w4[q]);
-                h[q] = f32x2_to_f16x2(lo, hi);
-                inexact = inexact || (lo != 0.f && !(fabsf(lo) >= 0x1p-17f && fabsf(lo) <= 65504.f)) ||
-                          (hi != 0.f && !(fabsf(hi) >= 0x1p-17f && fabsf(hi) <= 65504.f));
+                h[q] = f32x2_to_f16x2(bf16lo_f32(w4[q]), bf16hi_f32(w4[q]));
+                inexact |= !bf16_fits_f16(w4[q] & 0xFFFFu) || !bf16_fits_f16(w4[q] >> 16);
             }
         }
         xr[j] = make_uint4(h[0], h[1], h[2], h[3]);
@@ -526,15 +537,11 @@ bool layout_for(const q8_linear_desc *descs, int count, int &S, int &slot_bytes,
 
 }  // namespace
 
-bool pipe_supported(const q8_linear_desc *descs, int count, int M) {
-    if (M < 1 || M > 8) return false;
-    for (int i = 0; i < count; ++i)
-        if (descs[i].K > kPipeMaxK) return false;
-    int S, sb, ro, co, re;
-    return layout_for(descs, count, S, sb, ro, co, re);
-}
+bool pipe_k_supported(int64_t K) { return K <= kPipeMaxK && shape_of(static_cast<int>(K)).RT != 0; }
 
-q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
+namespace {
+
+q8_status launch_set(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (g_configured_dev != di->device) {
@@ -599,6 +606,18 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
     else
         pipe_kernel<12><<<grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+}
+
+}  // namespace
+
+q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
+    if (M < 1 || M > 8) return Q8_ERR_UNSUPPORTED;
+    for (int i = 0; i < count; ++i)
+        if (!pipe_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
+    // every mix of K <= 4096 fits one ring (the largest half-tile stage
+    // with a full tile's reduction entries still leaves two slots), so the
+    // launch never depends on which matrices share it
+    return launch_set(descs, count, M, dev_status, stream);
 }
 
 }  // namespace q8

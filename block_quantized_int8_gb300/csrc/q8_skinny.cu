@@ -383,26 +383,59 @@ size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *pla
     return off;
 }
 
-q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
+namespace {
+
+enum Route { kRouteGemv, kRoutePipe, kRouteTile, kRouteGeneral, kRoutes };
+
+// The kernel that serves one matrix, from its own K, M and the variant only,
+// so a matrix gets the same kernel -- hence the same bits -- whatever else
+// shares its call.  M = 1: the CUDA-core bulk-copy GEMV (AUTO, SIMT);
+// M = 2..8: the TMA-fed chunked tile kernel for K > 1536 (K % 256 == 0), the
+// warp-MMA bulk-copy pipeline otherwise (also M = 1 with MMA); M = 9..32:
+// the tile kernel (K % 256 == 0); everything else: the general kernel below.
+Route route_of(int64_t K, int M, int variant) {
+    if (M == 1 && variant != Q8_VARIANT_MMA && gemv_k_supported(K)) return kRouteGemv;
+    if (variant == Q8_VARIANT_SIMT) return kRouteGeneral;
+    if (M >= 2 && tile_k_supported(K) && (M > 8 || K > 1536)) return kRouteTile;
+    if (M <= 8 && pipe_k_supported(K)) return kRoutePipe;
+    return kRouteGeneral;
+}
+
+}  // namespace
+
+q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
-    // M = 1: the CUDA-core bulk-copy GEMV (AUTO, SIMT); M <= 8: the warp-MMA
-    // bulk-copy pipeline (AUTO for M >= 2, MMA for any M <= 8); M = 9..32:
-    // the TMA-fed chunked tile kernel (K % 256 == 0); otherwise the general
-    // kernel below
-    if (M == 1 && variant != Q8_VARIANT_MMA && gemv_supported(descs, count))
-        return launch_gemv(descs, count, dev_status, stream);
-    if (M <= 8 && variant != Q8_VARIANT_SIMT && pipe_supported(descs, count, M))
-        return launch_pipe(descs, count, M, dev_status, stream);
+    static thread_local q8_linear_desc part[kRoutes][Q8_MAX_BATCH];
+    int n[kRoutes] = {0, 0, 0, 0};
+    for (int i = 0; i < all_count; ++i) {
+        const Route r = route_of(all[i].K, M, variant);
+        part[r][n[r]++] = all[i];
+    }
+    // the documented workspace (the plan of every matrix, whatever kernel
+    // serves it) is checked before anything is enqueued; the general kernel
+    // uses the front of it
     SplitPlan plans[Q8_MAX_BATCH];
-    const size_t need = plan_skinny(descs, count, M, plans);
+    const size_t need = plan_skinny(all, all_count, M, plans);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return Q8_ERR_ALIGN;
-    // 9 <= M <= 32 with K a multiple of 256: the chunked tile kernel (needs
-    // no workspace, but the call keeps the documented workspace contract)
-    if (M > 8 && variant != Q8_VARIANT_SIMT && tile_supported(descs, count, M))
-        return launch_tile(descs, count, M, dev_status, stream);
+    const q8_linear_desc *descs = part[kRouteGeneral];
+    const int count = n[kRouteGeneral];
+    if (count > 0) plan_skinny(descs, count, M, plans);
+    if (n[kRouteGemv] > 0) {
+        const q8_status st = launch_gemv(part[kRouteGemv], n[kRouteGemv], dev_status, stream);
+        if (st != Q8_OK) return st;
+    }
+    if (n[kRoutePipe] > 0) {
+        const q8_status st = launch_pipe(part[kRoutePipe], n[kRoutePipe], M, dev_status, stream);
+        if (st != Q8_OK) return st;
+    }
+    if (n[kRouteTile] > 0) {
+        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, dev_status, stream);
+        if (st != Q8_OK) return st;
+    }
+    if (count == 0) return Q8_OK;
 
     BatchParams p;
     int items = 0;

@@ -1,27 +1,33 @@
-// q8_tile.cu -- Q8_0 W8A16 matmul for 9 <= M <= 32 activation rows over one or
-// several matrices in one persistent launch (K a multiple of 256).
+// q8_tile.cu -- Q8_0 W8A16 matmul for 2 <= M <= 32 activation rows over one or
+// several matrices in one persistent launch (K a multiple of 256).  Serves
+// M = 9..32, and M = 2..8 when a matrix has K > 1536 (q8_pipe.cu is faster on
+// the shorter rows, the chunked tiles on the longer ones).
 //
 // Y[m][n] = sum_k s[n][k/32] * q[n][k] * x[m][k]; "Frigg" README, Finding 8
 // (a batched W8A16 kernel reads each weight once for the whole batch of rows)
 // and Finding 3 (one launch for the many small matrices of a decode step).
 //
 // Design (TMA fed, tensor cores through warp mma):
-//  * An item is 128 consecutive weight rows of one matrix; CTAs own
-//    contiguous, byte-balanced ranges of items.  Each of the 8 warps owns a
-//    16-row tile of the item over all of K, so a row's sum never leaves its
-//    warp (no cross-warp reduction, no workspace).
-//  * K is streamed in chunks of 256 through a 2-slot ring per CTA (two CTAs
-//    per SM).  A stage is one chunk of one item: the codes (128 rows x 256
-//    bytes as two 128-byte-wide boxes), the x chunk (M rows x 256 bf16 as
-//    four boxes) and the block scales (128 rows x 8), all by
-//    cp.async.bulk.tensor; codes and x land in the 128-byte swizzled layout,
-//    so the lanes' fragment reads (rows g and g+8, or x rows 8j+g) fall on
-//    distinct banks.  No producer warp: thread 0 issues the first stages and
-//    the warp that releases a slot last issues the next one into it.
-//  * Per 32-code block the warp converts its codes to bf16 exactly (a sign
-//    split, |q| <= 127) and runs two mma.sync.m16n8k16 per 8 activation rows
-//    (weights as A, x^T as B), then scales the fp32 result by the binary16
-//    block scales of its two rows.  Products are exact; fp32 sums in k order.
+//  * K is cut into chunks of 256.  A stage is S consecutive chunks of
+//    R = 128 / S weight rows (32 KB of codes), with the x chunks and block
+//    scales that go with them, each loaded by one cp.async.bulk.tensor (codes
+//    and x in the 128-byte swizzled layout, so the lanes' fragment reads fall
+//    on distinct banks).  An item is R rows of one matrix over all of K; CTAs
+//    own contiguous, byte-balanced ranges of items and stream them through a
+//    2-slot ring (two CTAs per SM).  No producer warp: thread 0 issues the
+//    first stages and the warp that releases a slot last issues the next one.
+//  * The 8 warps split a stage as 8 / S row tiles of 16 x S chunks.  S (1, 2
+//    or 4) is chosen per launch so that a small launch still fills the GPU.
+//  * Per 32-code block a warp converts its codes to bf16 exactly (a sign
+//    split, |q| <= 127), runs two mma.sync.m16n8k16 per 8 activation rows
+//    (weights as A, x^T as B) and adds the result times the binary16 block
+//    scale of each row to an fp32 accumulator.  Products are exact.
+//  * fp32 sums are kept in C = 4 / (row-tiles of 8 x rows) classes: chunk c
+//    goes to class c mod C, summed in chunk order; at the end of an item the
+//    classes are added in class order.  A class is never split between
+//    warps (S divides C), so the bits do not depend on S: a matrix gives the
+//    same result alone or in any batch.  With S > 1 the warps publish their
+//    classes in shared memory and the last warp of the row tile adds them.
 // Every wait is bounded (Q8_DEV_TIMEOUT on expiry).
 #include <cuda.h>
 
@@ -36,25 +42,35 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kRows = 128;              // weight rows per item
-constexpr int kChunk = 256;             // K per stage
+constexpr int kChunk = 256;             // K per chunk
 constexpr int kSlots = 2;
-constexpr int kMaxGrid = 320;              // >= SMs x 2 on GB300 (the parameter block is near its limit)
-constexpr int kCodeBox = kRows * 128;   // one 128-byte-wide box of codes
+constexpr int kMaxGrid = 320;           // >= SMs x 2 on GB300 (the parameter block is near its limit)
+constexpr int kCodeBytes = 32768;       // codes of a stage: (128 / S) rows x 256 S
+constexpr int kXBytes = 16384;          // x of a stage: MP rows x 256 S bf16, MP S <= 32
+constexpr int kScaleBytes = 2048;       // block scales of a stage: (128 / S) rows x 8 S
+constexpr int kStage = kCodeBytes + kXBytes + kScaleBytes;  // a multiple of 1024
+constexpr int kRedBytes = 8192;         // class partials of one item: (8 / S) x C x 32 lanes x 4 MT floats
+// shared memory of tile_kernel<MT>: alignment slack, ring, class partials
+// (only where K can be split: MT < 4), barriers and counters
+template <int MT>
+constexpr int smem_bytes() { return 1024 + kSlots * kStage + (MT < 4 ? kRedBytes : 0) + 128; }
+static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
 
 struct TMaps {
-    CUtensorMap q;      // int8 [N][K], box {128, 128}, 128-byte swizzle
-    CUtensorMap x;      // bf16 [M][ldx], box {64, MP}, 128-byte swizzle
-    CUtensorMap s;      // binary16 [N][K/32], box {8, 128}
+    CUtensorMap q;      // int8 [N][K] as {128, N, K/128}, box {128, R, 2S}, 128-byte swizzle
+    CUtensorMap x;      // bf16 [M][ldx] as {64, M, K/64}, box {64, MP, 4S}, 128-byte swizzle
+    CUtensorMap s;      // binary16 [N][K/32], box {8S, R}
 };
 
 struct TDesc {
     float *y;
     int64_t ldy;
     int32_t N;
-    int32_t KC;          // chunks per item, K / 256
+    int32_t KC;          // chunks per row, K / 256
     int32_t item_begin;  // first global item of this matrix
-    int32_t items;       // ceil(N / 128)
+    int32_t items;       // ceil(N / R)
+    int32_t lgS;         // log2 of S, the chunks per stage (0, 1 or 2)
+    int32_t R;           // rows per item, 128 / S
 };
 
 struct TParams {
@@ -67,18 +83,19 @@ struct TParams {
 };
 static_assert(sizeof(TParams) <= 32764, "kernel parameters exceed the 32764-byte limit");
 
-template <int MP>
-struct TLayout {
-    static constexpr int kXBox = MP * 128;                       // one 64-element-wide box of x
-    static constexpr int kScales = kCodeBox * 2 + 4 * kXBox;      // offset of the scales
-    static constexpr int kStage = kScales + kRows * 16;
-    static constexpr int kSmem = 1024 + kSlots * kStage + 64;
-};
-
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *tm, int c0, int c1, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *tm, int c0, int c1, int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];"
+        :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2),
+           "r"(smem_addr(bar))
         : "memory");
 }
 
@@ -88,11 +105,12 @@ __device__ __forceinline__ int find_tdesc(const TParams &p, int item) {
     return d;
 }
 
-// Position (descriptor, item, chunk) in a CTA's sequence of stages.
+// Position (descriptor, item, first chunk) in a CTA's sequence of stages.
 struct Pos {
     int d, item, chunk;
     __device__ __forceinline__ void next(const TParams &p) {
-        if (++chunk == p.d[d].KC) {
+        chunk += 1 << p.d[d].lgS;
+        if (chunk == p.d[d].KC) {
             chunk = 0;
             ++item;
             while (d + 1 < p.count && item >= p.d[d + 1].item_begin) ++d;
@@ -100,15 +118,70 @@ struct Pos {
     }
 };
 
+// One chunk (8 blocks of 32) of a warp's 16-row tile into the accumulators a.
+//   cb: the chunk's first code box (128 K-bytes x R rows, swizzled), rb = R x 128
+//   xb: the chunk's first x box (64 K x MP rows, swizzled)
+//   sa, sb: the block scales of rows ra and ra + 8
+template <int MT>
+__device__ __forceinline__ void chunk_mma(float (&a)[MT][4], const uint8_t *cb, int rb, const uint8_t *xb,
+                                          const uint16_t *sa, const uint16_t *sb, int ra, const uint32_t (&offq)[4],
+                                          const uint32_t (&offx)[2], int g) {
+    constexpr int MP = MT * 8;
+#pragma unroll
+    for (int bl = 0; bl < kChunk / 32; ++bl) {
+        const uint8_t *cbox = cb + (bl >> 2) * rb;
+        const uint2 wa = *reinterpret_cast<const uint2 *>(cbox + ra * 128 + offq[bl & 3]);
+        const uint2 wb = *reinterpret_cast<const uint2 *>(cbox + (ra + 8) * 128 + offq[bl & 3]);
+        const float s_a = f16_bits_to_f32(sa[bl]);
+        const float s_b = f16_bits_to_f32(sb[bl]);
+        uint32_t a01, a23, a45, a67, b01, b23, b45, b67;
+        codes4_to_bf16x2(wa.x, a01, a23);
+        codes4_to_bf16x2(wa.y, a45, a67);
+        codes4_to_bf16x2(wb.x, b01, b23);
+        codes4_to_bf16x2(wb.y, b45, b67);
+        const uint8_t *xbox = xb + (bl >> 1) * (MP * 128);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            const uint4 xj = *reinterpret_cast<const uint4 *>(xbox + (8 * j + g) * 128 + offx[bl & 1]);
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+            mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xj.x, xj.y);
+            mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xj.z, xj.w);
+            a[j][0] = fmaf(s_a, d0, a[j][0]);
+            a[j][1] = fmaf(s_a, d1, a[j][1]);
+            a[j][2] = fmaf(s_b, d2, a[j][2]);
+            a[j][3] = fmaf(s_b, d3, a[j][3]);
+        }
+    }
+}
+
+template <int MT>
+__device__ __forceinline__ void store_tile(const TDesc &D, int row0, int ra, int t, int M, const float (&v)[MT][4]) {
+    const int na = row0 + ra, nbr = row0 + ra + 8;
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+        const int m0 = 8 * j + 2 * t;
+        if (na < D.N) {
+            if (m0 < M) D.y[m0 * D.ldy + na] = v[j][0];
+            if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + na] = v[j][1];
+        }
+        if (nbr < D.N) {
+            if (m0 < M) D.y[m0 * D.ldy + nbr] = v[j][2];
+            if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + nbr] = v[j][3];
+        }
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant__ TParams p) {
     constexpr int MP = MT * 8;
-    using L = TLayout<MP>;
+    constexpr int C = 4 / MT;  // accumulator classes
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + kSlots * L::kStage);
-    uint32_t *rel = reinterpret_cast<uint32_t *>(full + kSlots);
+    float4 *red = reinterpret_cast<float4 *>(base + kSlots * kStage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + kSlots * kStage + (MT < 4 ? kRedBytes : 0));
+    uint32_t *rel = reinterpret_cast<uint32_t *>(full + kSlots);  // per slot: warps done with it
+    uint32_t *cnt = rel + kSlots;                                 // per row tile: warps that published
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -123,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             mbar_init(&full[i], 1);
             rel[i] = 0u;
         }
+        for (int i = 0; i < kWarps; ++i) cnt[i] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
@@ -134,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         int d = find_tdesc(p, ib);
         for (int it = ib; it < ie; ++it) {
             while (d + 1 < p.count && it >= p.d[d + 1].item_begin) ++d;
-            nstages += p.d[d].KC;
+            nstages += p.d[d].KC >> p.d[d].lgS;
         }
     }
 
@@ -142,15 +216,12 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
         const TMaps &T = p.m[pos.d];
-        uint8_t *st = base + slot * L::kStage;
-        const int row0 = (pos.item - D.item_begin) * kRows;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(L::kStage));
-        tma_2d(st, &T.q, pos.chunk * kChunk, row0, &full[slot]);
-        tma_2d(st + kCodeBox, &T.q, pos.chunk * kChunk + 128, row0, &full[slot]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            tma_2d(st + 2 * kCodeBox + j * L::kXBox, &T.x, pos.chunk * kChunk + 64 * j, 0, &full[slot]);
-        tma_2d(st + L::kScales, &T.s, pos.chunk * (kChunk / 32), row0, &full[slot]);
+        uint8_t *st = base + slot * kStage;
+        const int row0 = (pos.item - D.item_begin) * D.R;
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + (MP * 512 << D.lgS) + kScaleBytes));
+        tma_3d(st, &T.q, 0, row0, 2 * pos.chunk, &full[slot]);
+        tma_3d(st + kCodeBytes, &T.x, 0, 0, 4 * pos.chunk, &full[slot]);
+        tma_2d(st + kCodeBytes + kXBytes, &T.s, 8 * pos.chunk, row0, &full[slot]);
     };
     Pos pos{find_tdesc(p, ib), ib, 0};
     if (tid == 0) {
@@ -162,53 +233,117 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     }
 
     // per-lane swizzled offsets: codes block b' (0..3) within a 128-byte box
-    // for rows with (row & 7) == g; x 32-element half kbb (0..1) of a box
+    // for rows with (row & 7) == g; x 32-element half (0..1) of a box
     uint32_t offq[4], offx[2];
 #pragma unroll
     for (int b = 0; b < 4; ++b) offq[b] = ((((2 * b + (t >> 1)) ^ g)) << 4) + 8 * (t & 1);
 #pragma unroll
     for (int h = 0; h < 2; ++h) offx[h] = (((4 * h + t) ^ g)) << 4;
-    const int ra = 16 * warp + g;  // item-local rows of this lane: ra, ra + 8
 
-    float acc[MT][4];
+    float acc[C][MT][4];
 #pragma unroll
-    for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int c = 0; c < C; ++c)
+#pragma unroll
+        for (int j = 0; j < MT; ++j) acc[c][j][0] = acc[c][j][1] = acc[c][j][2] = acc[c][j][3] = 0.f;
 
     for (int k = 0; k < nstages; ++k) {
         const int slot = k % kSlots;
+        const TDesc &D = p.d[pos.d];
+        const int lgS = C == 1 ? 0 : D.lgS;  // C == 1: never split
+        const int S = 1 << lgS;
+        const int rt = warp & ((kWarps >> lgS) - 1);  // row tile
+        const int ks = warp >> (3 - lgS);             // chunk of the stage
+        const int ra = 16 * rt + g;                   // item-local rows of this lane: ra, ra + 8
+        const int cls = (pos.chunk + ks) & (C - 1);
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
             return;
         }
-        const uint8_t *st = base + slot * L::kStage;
-        const uint16_t *sc = reinterpret_cast<const uint16_t *>(st + L::kScales);
-#pragma unroll
-        for (int bl = 0; bl < kChunk / 32; ++bl) {
-            const uint8_t *cbox = st + (bl >> 2) * kCodeBox;
-            const uint2 wa = *reinterpret_cast<const uint2 *>(cbox + ra * 128 + offq[bl & 3]);
-            const uint2 wb = *reinterpret_cast<const uint2 *>(cbox + (ra + 8) * 128 + offq[bl & 3]);
-            const float s_a = f16_bits_to_f32(sc[ra * 8 + bl]);
-            const float s_b = f16_bits_to_f32(sc[(ra + 8) * 8 + bl]);
-            uint32_t a01, a23, a45, a67, b01, b23, b45, b67;
-            codes4_to_bf16x2(wa.x, a01, a23);
-            codes4_to_bf16x2(wa.y, a45, a67);
-            codes4_to_bf16x2(wb.x, b01, b23);
-            codes4_to_bf16x2(wb.y, b45, b67);
-            const uint8_t *xbox = st + 2 * kCodeBox + (bl >> 1) * L::kXBox;
-#pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                const uint4 xj = *reinterpret_cast<const uint4 *>(xbox + (8 * j + g) * 128 + offx[bl & 1]);
-                float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-                mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xj.x, xj.y);
-                mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xj.z, xj.w);
-                acc[j][0] = fmaf(s_a, d0, acc[j][0]);
-                acc[j][1] = fmaf(s_a, d1, acc[j][1]);
-                acc[j][2] = fmaf(s_b, d2, acc[j][2]);
-                acc[j][3] = fmaf(s_b, d3, acc[j][3]);
+        {
+            const uint8_t *st = base + slot * kStage;
+            const int rb = D.R * 128;
+            const uint8_t *cb = st + 2 * ks * rb;
+            const uint8_t *xb = st + kCodeBytes + 4 * ks * (MP * 128);
+            const uint16_t *sa = reinterpret_cast<const uint16_t *>(st + kCodeBytes + kXBytes) + (ra << (3 + lgS)) + 8 * ks;
+            const uint16_t *sb = sa + (8 << (3 + lgS));
+            if constexpr (C == 4) {
+                switch (cls) {
+                    case 0: chunk_mma<MT>(acc[0], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
+                    case 1: chunk_mma<MT>(acc[1 % C], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
+                    case 2: chunk_mma<MT>(acc[2 % C], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
+                    default: chunk_mma<MT>(acc[3 % C], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
+                }
+            } else if constexpr (C == 2) {
+                if (cls == 0)
+                    chunk_mma<MT>(acc[0], cb, rb, xb, sa, sb, ra, offq, offx, g);
+                else
+                    chunk_mma<MT>(acc[1 % C], cb, rb, xb, sa, sb, ra, offq, offx, g);
+            } else {
+                chunk_mma<MT>(acc[0], cb, rb, xb, sa, sb, ra, offq, offx, g);
             }
         }
-        // release the slot: reads ordered (fence, counter, fence) before the
-        // refill that the last of the 8 warps issues
+        // the item's last stage: add the classes in class order and store y
+        if (pos.chunk + S == D.KC) {
+            const int row0 = (pos.item - D.item_begin) * D.R;
+            float v[MT][4];
+            if (C == 1 || S == 1) {
+#pragma unroll
+                for (int j = 0; j < MT; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float x = acc[0][j][e];
+#pragma unroll
+                        for (int c = 1; c < C; ++c) x += acc[c][j][e];
+                        v[j][e] = x;
+                    }
+                store_tile<MT>(D, row0, ra, t, M, v);
+            } else {
+                // publish the classes this warp owns (c mod S == ks); the last
+                // of the row tile's S warps adds all of them
+#pragma unroll
+                for (int c = 0; c < C; ++c)
+                    if ((c & (S - 1)) == ks)
+#pragma unroll
+                        for (int j = 0; j < MT; ++j)
+                            red[((rt * C + c) * 32 + lane) * MT + j] =
+                                make_float4(acc[c][j][0], acc[c][j][1], acc[c][j][2], acc[c][j][3]);
+                __threadfence_block();
+                __syncwarp();
+                uint32_t prev = 0;
+                if (lane == 0) prev = atomicAdd(&cnt[rt], 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == static_cast<uint32_t>(S - 1)) {
+                    __threadfence_block();
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) {
+                        float4 u = red[(rt * C * 32 + lane) * MT + j];
+#pragma unroll
+                        for (int c = 1; c < C; ++c) {
+                            const float4 w = red[((rt * C + c) * 32 + lane) * MT + j];
+                            u.x += w.x;
+                            u.y += w.y;
+                            u.z += w.z;
+                            u.w += w.w;
+                        }
+                        v[j][0] = u.x;
+                        v[j][1] = u.y;
+                        v[j][2] = u.z;
+                        v[j][3] = u.w;
+                    }
+                    store_tile<MT>(D, row0, ra, t, M, v);
+                    __syncwarp();
+                    if (lane == 0) cnt[rt] = 0u;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < C; ++c)
+#pragma unroll
+                for (int j = 0; j < MT; ++j) acc[c][j][0] = acc[c][j][1] = acc[c][j][2] = acc[c][j][3] = 0.f;
+        }
+        // release the slot (after the item's partials are read, so that the
+        // next item's cannot overwrite them: items have one stage if S == 1,
+        // at least two otherwise): reads ordered (fence, counter, fence)
+        // before the refill that the last of the 8 warps issues
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
@@ -219,31 +354,12 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
                 fence_proxy_async_smem();
                 if (k + kSlots < nstages) {
                     Pos q = pos;
-                    for (int s = 0; s < kSlots; ++s) q.next(p);
+                    for (int s2 = 0; s2 < kSlots; ++s2) q.next(p);
                     issue(k + kSlots, q);
                 }
             }
         }
         __syncwarp();
-        // the item's last chunk: store y and start the next item
-        const TDesc &D = p.d[pos.d];
-        if (pos.chunk == D.KC - 1) {
-            const int row0 = (pos.item - D.item_begin) * kRows;
-            const int na = row0 + ra, nbr = row0 + ra + 8;
-#pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                const int m0 = 8 * j + 2 * t;
-                if (na < D.N) {
-                    if (m0 < M) D.y[m0 * D.ldy + na] = acc[j][0];
-                    if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + na] = acc[j][1];
-                }
-                if (nbr < D.N) {
-                    if (m0 < M) D.y[m0 * D.ldy + nbr] = acc[j][2];
-                    if (m0 + 1 < M) D.y[(m0 + 1) * D.ldy + nbr] = acc[j][3];
-                }
-                acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-            }
-        }
         pos.next(p);
     }
 }
@@ -253,12 +369,10 @@ int g_occ = 0;
 
 template <int MT>
 bool configure(int &occ) {
-    if (cudaFuncSetAttribute(tile_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TLayout<MT * 8>::kSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(tile_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<MT>()) != cudaSuccess)
         return false;
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT>, kThreads, TLayout<MT * 8>::kSmem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT>, kThreads, smem_bytes<MT>()) != cudaSuccess)
         return false;
     occ = std::min(occ, std::max(o, 1));
     return true;
@@ -275,55 +389,88 @@ q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, c
         const TDesc &D = p.d[i];
         const double per_row = static_cast<double>(D.KC) * kChunk * 1.0625;
         for (int it = 0; it < D.items && c < grid - 1; ++it) {
-            acc += per_row * std::min(kRows, D.N - it * kRows);
+            acc += per_row * std::min(D.R, D.N - it * D.R);
             while (c < grid - 1 && acc >= total_bytes * (c + 1) / grid) p.cta_begin[++c] = D.item_begin + it + 1;
         }
     }
     while (c < grid) p.cta_begin[++c] = items;
-    tile_kernel<MT><<<grid, kThreads, TLayout<MT * 8>::kSmem, stream>>>(p);
+    tile_kernel<MT><<<grid, kThreads, smem_bytes<MT>(), stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 
+// Chunks per stage of a matrix with KC chunks in a launch that asks for S:
+// the largest power of two <= S that divides KC and leaves an item at least
+// two stages (the class partials of an item are read before the slot of its
+// last stage is released; two stages keep the next item's from landing first).
+int split_for(int64_t KC, int S) {
+    while (S > 1 && (KC % S != 0 || KC < 2 * S)) S >>= 1;
+    return S;
+}
+
+int log2_of(int S) { return S >= 4 ? 2 : (S >= 2 ? 1 : 0); }
+
 }  // namespace
 
-bool tile_supported(const q8_linear_desc *descs, int count, int M) {
-    if (M < 9 || M > 32 || count > Q8_MAX_BATCH) return false;
-    for (int i = 0; i < count; ++i)
-        if (descs[i].K % kChunk != 0) return false;
-    return true;
-}
+bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
 
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
+    if (M < 2 || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
+    for (int i = 0; i < count; ++i)
+        if (!tile_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
     if (g_configured_dev != di->device) {
         int o = 1 << 30;
-        if (!configure<2>(o) || !configure<4>(o)) return Q8_ERR_CUDA;
+        if (!configure<1>(o) || !configure<2>(o) || !configure<4>(o)) return Q8_ERR_CUDA;
         g_occ = o;
         g_configured_dev = di->device;
     }
     static thread_local TParams p;
-    const int MP = M <= 16 ? 16 : 32;
+    const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+    const int MP = 8 * MT;
+    const int C = 4 / MT;
+    // the fewest chunks per stage that give every SM an item (measured: a
+    // split costs more than the second CTA per SM gains); the results do not
+    // depend on it
+    int S = 1;
+    for (;;) {
+        int64_t n_items = 0;
+        for (int i = 0; i < count; ++i) {
+            const int R = 128 / split_for(descs[i].K / kChunk, S);
+            n_items += (descs[i].N + R - 1) / R;
+        }
+        if (S >= C || n_items >= di->sm_count) break;
+        S *= 2;
+    }
     int items = 0;
     double total_bytes = 0.0;
     for (int i = 0; i < count; ++i) {
         TDesc &D = p.d[i];
         TMaps &T = p.m[i];
         const q8_linear_desc &d = descs[i];
+        const int64_t KC = d.K / kChunk;
+        const int Sd = split_for(KC, S);
+        const uint32_t R = static_cast<uint32_t>(128 / Sd);
+        const uint64_t qdims[3] = {128, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K / 128)};
+        const uint64_t qstr[2] = {static_cast<uint64_t>(d.K), 128};
+        const uint32_t qbox[3] = {128, R, static_cast<uint32_t>(2 * Sd)};
+        const uint64_t xdims[3] = {64, static_cast<uint64_t>(M), static_cast<uint64_t>(d.K / 64)};
+        const uint64_t xstr[2] = {static_cast<uint64_t>(d.ldx) * 2, 128};
+        const uint32_t xbox[3] = {64, static_cast<uint32_t>(MP), static_cast<uint32_t>(4 * Sd)};
         const int64_t nb = d.K / 32;
-        if (!encode_2d(&T.q, 1, d.q, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N),
-                       static_cast<uint64_t>(d.K), 128, kRows, true) ||
-            !encode_2d(&T.x, 2, d.x, static_cast<uint64_t>(d.K), static_cast<uint64_t>(M),
-                       static_cast<uint64_t>(d.ldx) * 2, 64, static_cast<uint32_t>(MP), true) ||
+        if (!encode_tmap(&T.q, 1, d.q, 3, qdims, qstr, qbox, true) ||
+            !encode_tmap(&T.x, 2, d.x, 3, xdims, xstr, xbox, true) ||
             !encode_2d(&T.s, 2, d.s, static_cast<uint64_t>(nb), static_cast<uint64_t>(d.N),
-                       static_cast<uint64_t>(nb) * 2, 8, kRows, false))
+                       static_cast<uint64_t>(nb) * 2, static_cast<uint32_t>(8 * Sd), R, false))
             return Q8_ERR_CUDA;
         D.y = d.y;
         D.ldy = d.ldy;
         D.N = static_cast<int32_t>(d.N);
-        D.KC = static_cast<int32_t>(d.K / kChunk);
+        D.KC = static_cast<int32_t>(KC);
+        D.lgS = log2_of(Sd);
+        D.R = static_cast<int32_t>(R);
         D.item_begin = items;
-        D.items = static_cast<int32_t>((d.N + kRows - 1) / kRows);
+        D.items = static_cast<int32_t>((d.N + R - 1) / R);
         items += D.items;
         total_bytes += static_cast<double>(d.N) * d.K * 1.0625;
     }
@@ -331,7 +478,8 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
     p.count = count;
     p.M = M;
     if (items == 0) return Q8_OK;
-    return M <= 16 ? run<2>(p, di, items, total_bytes, stream) : run<4>(p, di, items, total_bytes, stream);
+    if (MT == 1) return run<1>(p, di, items, total_bytes, stream);
+    return MT == 2 ? run<2>(p, di, items, total_bytes, stream) : run<4>(p, di, items, total_bytes, stream);
 }
 
 }  // namespace q8

@@ -67,7 +67,7 @@ typedef enum q8_status {
 #define Q8_MAX_BATCH 64      /* most descriptors per q8_linear_batch call */
 
 /* Kernel variants for the M <= 32 path (the _ex entry points). */
-#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: warp-MMA pipeline; M > 8: TMA-fed warp-MMA tiles */
+#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: warp-MMA pipeline (K <= 1536) or TMA-fed warp-MMA tiles; M > 8: the tiles */
 #define Q8_VARIANT_SIMT 1    /* CUDA-core FFMA: codes dequantised in registers, one FMA per weight per row */
 #define Q8_VARIANT_MMA  2    /* warp mma.sync bf16 on exact bf16 codes, block scale applied in fp32 */
 
@@ -136,8 +136,9 @@ typedef struct q8_linear_desc {
 
 /*
  * q8_linear_batch -- several independent skinny matmuls (same M, any shapes)
- * in ONE persistent launch that walks a static list of (matrix, row tile,
- * K split) work items.  Source: "Frigg" README, Finding 3 and Finding 8 (a
+ * in one persistent launch per kernel family that walks a static list of
+ * (matrix, row tile, K split) work items; each matrix is routed on its own K
+ * and M, so a call whose matrices all share a family is one launch.  Source: "Frigg" README, Finding 3 and Finding 8 (a
  * decode step of many small matmuls is launch-bound before it is
  * bandwidth-bound).
  *   descs : HOST array of `count` descriptors, 1 <= count <= Q8_MAX_BATCH;

@@ -182,10 +182,14 @@ def test_layer_set_batch_sampled(oracle):
 # ---------------------------------------------------------------------------
 # determinism, graph replay, batch == separate calls
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("M", [3, 20])
+@pytest.mark.parametrize("M", [1, 3, 8, 20])
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
-    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 256)]
+    # shapes that the automatic routing sends to different kernels: K <= 1536
+    # and K % 256 != 0 (pipeline for M <= 8), K > 1536 with K % 256 == 0
+    # (tiles for M >= 2), K > 4096 off the 256 grid and K > 12288 (general)
+    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 256),
+              (130, 2080), (300, 4128), (96, 12800)]
     mats_np = []
     for i, (N, K) in enumerate(shapes):
         qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"bs{i}"))
@@ -194,6 +198,24 @@ def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
     for m_np, y_t in zip(mats_np, together):
         (y_s,) = run_batch([m_np], M, variant)
         assert np.array_equal(y_s, y_t)
+
+
+@pytest.mark.parametrize("M", [4, 12, 24])
+@pytest.mark.parametrize("K", [1536, 4096])
+def test_tile_k_split_keeps_bits(oracle, M, K):
+    """A lone small matrix gets its K split across warps (to fill the GPU);
+    in a launch with many rows it is not.  Its result must not change."""
+    if M <= 8 and K <= 1536:
+        pytest.skip("served by the pipeline kernel, not the tiles")
+    qn, sn, _ = oracle.quantize_rows(synth.weights(1536, K, 0, "ks"))
+    mat = (qn, sn, synth.activations(M, K, 0, "ksx"))
+    (alone,) = run_batch([mat], M, 0)
+    big_q, big_s, _ = oracle.quantize_rows(synth.weights(8192, K, 0, "ksb"))
+    big = (big_q, big_s, synth.activations(M, K, 0, "ksbx"))
+    together = run_batch([mat] + [big] * 6, M, 0)
+    assert np.array_equal(alone, together[0])
+    y_ref, B = oracle.matmul(qn, sn, mat[2], threads=8)
+    check_tol(alone, y_ref, B, f"K split N=1536 K={K} M={M}")
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
