@@ -101,7 +101,8 @@ size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {
     d.N = N;
     d.K = K;
     SplitPlan pl;
-    return plan_skinny(&d, 1, M, &pl);
+    size_t sched_off;
+    return skinny_workspace(&d, 1, M, &pl, &sched_off);
 }
 
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M) {
@@ -114,7 +115,8 @@ size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count
     }
     if (n == 0) return 0;
     SplitPlan pl[Q8_MAX_BATCH];
-    return plan_skinny(tmp, n, M, pl);
+    size_t sched_off;
+    return skinny_workspace(tmp, n, M, pl, &sched_off);
 }
 
 q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant,

@@ -52,13 +52,18 @@ constexpr int kMaxPairs = 4;                   // row pairs per warp per stage: 
 constexpr int kScaleBytes = kCodeBytes / 16 + 16;  // RT * K / 16, plus up to 14 bytes of alignment offset
 constexpr int kStageBytes = kCodeBytes + kScaleBytes;
 constexpr int kMaxK = 8 * kSliceK;             // P <= 8
-constexpr int kMaxGrid = 1024;
+constexpr int kMaxGrid = 512;
 // Work of a stage for the partition, relative to its bytes: a matrix whose
 // rows are split over warps (P > 1) costs more per byte (narrower slices,
 // cross-warp combine).  1.2 measured best on the decode layer set
 // (K = 1536 and K = 4096 matrices in one launch: +3 % over byte balance).
 constexpr double kSplitCost = 1.2;
 constexpr int kJMax = 3;                       // 16-code chunks per lane per slice (1536 k)
+// Share of a CTA's balanced stage range that it owns outright; the rest of
+// every range goes to a pool that CTAs draw from one stage at a time once
+// their own part is done (CTAs start up to a few microseconds apart and SMs
+// stream at different rates, so equal static shares finish unevenly).
+constexpr double kStaticShare = 0.95;
 
 struct GDesc {
     const int8_t *q;
@@ -79,9 +84,14 @@ struct GDesc {
 struct GParams {
     GDesc d[Q8_MAX_BATCH];
     uint32_t *status;
+    uint32_t *sched;        // pool counter, zero between launches (null: no pool)
     int32_t count;
     int32_t total_stages;
-    int32_t cta_begin[kMaxGrid + 1];  // CTA c owns stages [cta_begin[c], cta_begin[c+1])
+    int32_t grid;
+    int32_t pool_total;     // stages in the pool
+    int32_t cta_begin[kMaxGrid + 1];  // CTA c's balanced range [cta_begin[c], cta_begin[c+1])
+    int32_t cta_split[kMaxGrid];      // it owns [cta_begin[c], cta_split[c]); the rest is pooled
+    int32_t pool_off[kMaxGrid + 1];   // pool index of the first pooled stage of CTA c's range
 };
 
 struct Smem {
@@ -90,6 +100,8 @@ struct Smem {
     uint32_t cnt[2 * kStages][kRedRows];
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t named[kStages];               // the producer has written sidx of the slot
+    int32_t sidx[kStages];                 // stage in a slot drawn from the pool; -1: no more
 };
 
 __device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
@@ -303,34 +315,57 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Descriptor of a stage (binary search: pool stages come from anywhere).
 __device__ __forceinline__ int find_gdesc(const GParams &p, int stage) {
-    int d = 0;
-    while (d + 1 < p.count && stage >= p.d[d + 1].stage_begin) ++d;
-    return d;
+    int lo = 0, hi = p.count;  // d[lo].stage_begin <= stage < d[hi].stage_begin
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.d[mid].stage_begin <= stage) lo = mid; else hi = mid;
+    }
+    return lo;
 }
 
-// The work of one CTA over stages [begin, end); KJ is the number of 16-code
-// chunks per lane in a warp's K slice (3: slices up to 1536 wide).
-// `ring` counts the stages this CTA has already passed through its ring of
-// kStages slots; slot and mbarrier phase follow from it.
+// Stage of pool index j: the pooled part of CTA c's range holds pool indices
+// [pool_off[c], pool_off[c+1]).
+__device__ __forceinline__ int pool_stage(const GParams &p, int j) {
+    int lo = 0, hi = p.grid;  // pool_off[lo] <= j < pool_off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.pool_off[mid] <= j) lo = mid; else hi = mid;
+    }
+    return p.cta_split[lo] + (j - p.pool_off[lo]);
+}
+
+// The work of one CTA: its own stages [begin, split), then stages drawn from
+// the pool until it is empty; KJ is the number of 16-code chunks per lane in
+// a warp's K slice (3: slices up to 1536 wide).  Ring position k uses slot
+// k % kStages and mbarrier phase (k / kStages) & 1.
 template <int KJ>
-__device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, int end, int warp, int lane,
-                                         int ring) {
-    // Lane 0 of warp 0 is also the producer.  Before warp 0 consumes stage k it
-    // tops the ring up: stages up to k + kStages - 1 are issued as soon as their
-    // slot is free (non-blocking check); stage k itself is issued even if that
-    // means waiting for the slowest warp to release its slot, so no consumer can
-    // wait on a copy that nobody will start.
-    const int nstages = end - begin;
-    int pi = 0;                       // stages issued so far (producer lane only)
-    int pd = find_gdesc(p, begin);    // descriptor of the next stage to issue
-    bool prod_ok = true;
+__device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, int split, int warp, int lane) {
+    // Lane 0 of warp 0 is also the producer.  Before warp 0 consumes position
+    // k it tops the ring up: positions up to k + kStages - 1 are issued as soon
+    // as their slot is free (non-blocking check); position k itself is issued
+    // even if that means waiting for the slowest warp to release its slot, so
+    // no consumer can wait on a copy that nobody will start.  Positions past
+    // the CTA's own stages take pool indices from the counter, drawn one
+    // position ahead so that the atomic's latency hides behind a stage; the
+    // stage goes to sidx[slot] (announced on named[slot] at once, so that the
+    // consumers can load x for it while the copy is in flight), and once the
+    // pool is empty an end marker (-1) takes its place.  Every CTA draws exactly
+    // one index past the pool, so the CTA that draws the grid's last one
+    // leaves the counter zero for the next launch.
+    const int nown = split - begin;
+    int pi = 0;                         // positions issued so far (producer lane only)
+    int pd = nown > 0 ? find_gdesc(p, begin) : 0;  // descriptor of the stage being issued
+    bool prod_ok = true;                // false once timed out or past the end marker
+    uint32_t ahead = 0xFFFFFFFFu;       // pool index drawn for the next pool position
+    auto draw = [&]() { ahead = p.sched ? atomicAdd(p.sched, 1u) : 0xFFFFFFFFu; };
+    if (warp == 0 && lane == 0 && nown == 0) draw();
     auto produce = [&](int upto) {
-        while (prod_ok && pi < nstages && pi <= upto) {
-            const int q = ring + pi;  // ring position of the stage to issue
-            const int slot = q % kStages;
-            if (q >= kStages) {
-                const uint32_t par = ((q / kStages) - 1) & 1;
+        while (prod_ok && pi <= upto) {
+            const int slot = pi % kStages;
+            if (pi >= kStages) {
+                const uint32_t par = ((pi / kStages) - 1) & 1;
                 const bool must = pi <= upto - (kStages - 1);
                 if (must) {
                     if (!mbar_wait_bounded(&sm.empty[slot], par)) {
@@ -342,8 +377,26 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
                     return;
                 }
             }
-            const int i = begin + pi;
-            while (i >= p.d[pd].stage_begin + p.d[pd].stages) ++pd;
+            int i;
+            if (pi < nown) {
+                i = begin + pi;
+                while (i >= p.d[pd].stage_begin + p.d[pd].stages) ++pd;
+            } else {
+                const uint32_t j = ahead;
+                if (j >= static_cast<uint32_t>(p.pool_total)) {
+                    if (p.sched && j == static_cast<uint32_t>(p.pool_total + p.grid - 1)) atomicExch(p.sched, 0u);
+                    sm.sidx[slot] = -1;
+                    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];"
+                                 :: "r"(smem_addr(&sm.named[slot])) : "memory");
+                    prod_ok = false;
+                    return;
+                }
+                i = pool_stage(p, static_cast<int>(j));
+                pd = find_gdesc(p, i);
+                sm.sidx[slot] = i;
+                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];"
+                             :: "r"(smem_addr(&sm.named[slot])) : "memory");
+            }
             const GDesc &D = p.d[pd];
             const int r0 = (i - D.stage_begin) * D.RT;
             const int rows = min(D.RT, D.N - r0);
@@ -367,48 +420,77 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
             mbar_arrive_expect_tx(&sm.full[slot], cbytes + body);
             bulk_g2s(dst, D.q + static_cast<int64_t>(r0) * D.K, cbytes, &sm.full[slot]);
             if (body) bulk_g2s(sdst + head, gs + head, body, &sm.full[slot]);
+            if (pi >= nown - 1) draw();
             ++pi;
         }
     };
 
     // ---------------------------------------------------------------- consumers
-    int d = find_gdesc(p, begin);
-    int cur_d = -1;
+    int d = nown > 0 ? find_gdesc(p, begin) : 0;
     unsigned long long xr[KJ][8];  // this lane's x chunks as packed fp32 pairs
     int slice = 0, nj = 0, k0 = 0, chunks_slice = 0;
-    for (int i = begin, k = 0; i < end; ++i, ++k) {
+    // x in the registers: activation row and geometry (K, P) it was loaded for
+    const uint16_t *cur_x = nullptr;
+    int cur_K = 0, cur_P = 0;
+    // (re)load this warp's slice of x into registers as fp32 pairs, unless
+    // they already hold it (matrices of one launch often share their x)
+    auto load_x = [&](const GDesc &D) {
+        if (D.x == cur_x && D.K == cur_K && D.P == cur_P) return;
+        cur_x = D.x;
+        cur_K = D.K;
+        cur_P = D.P;
+        slice = warp & (D.P - 1);
+        const int kb0 = slice * D.bps;
+        const int kb1 = min(D.nb, kb0 + D.bps);
+        chunks_slice = (kb1 - kb0) * 2;  // 16-code chunks in the slice
+        k0 = kb0 * 32;
+        nj = (chunks_slice + 31) / 32;
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+            const int c = lane + 32 * j;
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+            if (c < chunks_slice) {
+                const uint4 *xp = reinterpret_cast<const uint4 *>(D.x + k0 + 16 * c);
+                a = __ldg(xp);
+                b = __ldg(xp + 1);
+            }
+            const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xr[j][e] = f2_pack(bf16lo_f32(v[e]), bf16hi_f32(v[e]));
+        }
+    };
+    for (int k = 0;; ++k) {
         if (warp == 0 && lane == 0) produce(k + kStages - 1);
         __syncwarp();
-        while (i >= p.d[d].stage_begin + p.d[d].stages) ++d;
-        const GDesc &D = p.d[d];
-        if (d != cur_d) {
-            // (re)load this warp's slice of x into registers as fp32 pairs
-            cur_d = d;
-            slice = warp & (D.P - 1);
-            const int kb0 = slice * D.bps;
-            const int kb1 = min(D.nb, kb0 + D.bps);
-            chunks_slice = (kb1 - kb0) * 2;  // 16-code chunks in the slice
-            k0 = kb0 * 32;
-            nj = (chunks_slice + 31) / 32;
-#pragma unroll
-            for (int j = 0; j < KJ; ++j) {
-                const int c = lane + 32 * j;
-                uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-                if (c < chunks_slice) {
-                    const uint4 *xp = reinterpret_cast<const uint4 *>(D.x + k0 + 16 * c);
-                    a = __ldg(xp);
-                    b = __ldg(xp + 1);
-                }
-                const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xr[j][e] = f2_pack(bf16lo_f32(v[e]), bf16hi_f32(v[e]));
+        const int slot = k % kStages;
+        int i;
+        if (k < nown) {
+            // own stage: x for it loads while its copy is in flight
+            i = begin + k;
+            while (i >= p.d[d].stage_begin + p.d[d].stages) ++d;
+            load_x(p.d[d]);
+            if (!mbar_wait_bounded(&sm.full[slot], (k / kStages) & 1)) {
+                if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+                return;
+            }
+        } else {
+            // pool stage: its index is published (named) when it is issued,
+            // so x for it loads while its copy is in flight
+            const int kp = k - nown;  // pool positions before this one
+            if (!mbar_wait_bounded(&sm.named[slot], (kp / kStages) & 1)) {
+                if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+                return;
+            }
+            i = *reinterpret_cast<volatile const int32_t *>(&sm.sidx[slot]);
+            if (i < 0) return;
+            d = find_gdesc(p, i);
+            load_x(p.d[d]);
+            if (!mbar_wait_bounded(&sm.full[slot], (k / kStages) & 1)) {
+                if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+                return;
             }
         }
-        const int slot = (ring + k) % kStages;
-        if (!mbar_wait_bounded(&sm.full[slot], ((ring + k) / kStages) & 1)) {
-            if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
-            return;
-        }
+        const GDesc &D = p.d[d];
         const uint8_t *codes = sm.stage[slot];
         const int r0 = (i - D.stage_begin) * D.RT;
         const uint16_t *scales = reinterpret_cast<const uint16_t *>(
@@ -426,7 +508,7 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
         const int wrow = warp >> D.lp;
         const uint8_t *cA = codes + wrow * D.K + k0;
         const uint16_t *sA = scales + wrow * D.nb + (k0 >> 5);
-        const int rs = (ring + k) % (2 * kStages);
+        const int rs = k % (2 * kStages);
         const bool full_slice = chunks_slice == 32 * nj;
         float *yrow = D.y + r0;
         switch (nj) {
@@ -444,18 +526,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int begin = p.cta_begin[blockIdx.x];
-    const int end = p.cta_begin[blockIdx.x + 1];
+    const int split = p.cta_split[blockIdx.x];
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], kConsumerWarps);
+            mbar_init(&sm.named[i], 1);
         }
         fence_mbar_init();
     }
     for (int i = tid; i < 2 * kStages * kRedRows; i += kThreads) (&sm.cnt[0][0])[i] = 0u;
     __syncthreads();
-    if (end > begin) cta_work<kJMax>(p, sm, begin, end, warp, lane, 0);
+    cta_work<kJMax>(p, sm, begin, split, warp, lane);
 }
 
 int g_configured_dev = -1;
@@ -465,7 +548,8 @@ int g_occ = 0;
 
 bool gemv_k_supported(int64_t K) { return K <= kMaxK; }
 
-q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_status, cudaStream_t stream) {
+q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, uint32_t *dev_status,
+                      cudaStream_t stream) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (g_configured_dev != di->device) {
@@ -524,8 +608,18 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_stat
         }
     }
     while (c < grid) p.cta_begin[++c] = stages;
-    const int launch = grid;
-    gemv_kernel<<<launch, kThreads, sizeof(Smem), stream>>>(p);
+    // each CTA keeps the first kStaticShare of its range; the rest is pooled
+    p.sched = sched;
+    p.grid = grid;
+    p.pool_off[0] = 0;
+    for (int b = 0; b < grid; ++b) {
+        const int len = p.cta_begin[b + 1] - p.cta_begin[b];
+        const int own = sched ? static_cast<int>(len * kStaticShare) : len;
+        p.cta_split[b] = p.cta_begin[b] + own;
+        p.pool_off[b + 1] = p.pool_off[b] + (len - own);
+    }
+    p.pool_total = p.pool_off[grid];
+    gemv_kernel<<<grid, kThreads, sizeof(Smem), stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 

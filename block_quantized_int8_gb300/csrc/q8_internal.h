@@ -44,9 +44,17 @@ struct SplitPlan {
 // Plans every descriptor and returns the workspace bytes needed.
 size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans);
 
+// Workspace of a skinny call: the general kernel's plan of every matrix, then
+// (when some matrix is served by the GEMV) a 256-byte block whose first word
+// is the GEMV's pool counter, at *sched_off (SIZE_MAX if none).
+size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off);
+
 // M = 1 bulk-copy pipeline (q8_gemv.cu): matrices with K <= 12288.
 bool gemv_k_supported(int64_t K);
-q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *dev_status, cudaStream_t stream);
+// sched: a zeroed device word the launch uses as its pool counter and leaves
+// zero again (null: every CTA keeps its whole static range).
+q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, uint32_t *dev_status,
+                      cudaStream_t stream);
 
 // 1 <= M <= 8 bulk-copy pipeline with warp MMA (q8_pipe.cu): K <= 4096.
 bool pipe_k_supported(int64_t K);

@@ -79,12 +79,18 @@ extern "C" q8_status q8_gemm_skinny_noalloc(const int8_t *q, const uint16_t *s, 
     if (ws == nullptr) return Q8_ERR_CUDA;
 
     if (need > 0) {
-        // the ticket words come first in the workspace layout; clear them
+        // clear the words the kernels count with: the ticket words (first in
+        // the layout) and the GEMV's pool counter block (last)
         SplitPlan pl;
-        (void)plan_skinny(&d, 1, M, &pl);
+        size_t sched_off;
+        (void)skinny_workspace(&d, 1, M, &pl, &sched_off);
         const size_t ticket_bytes = pl.part_off - pl.ticket_off;
         if (ticket_bytes > 0 &&
             cudaMemsetAsync(static_cast<unsigned char *>(ws) + pl.ticket_off, 0, ticket_bytes,
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return Q8_ERR_CUDA;
+        if (sched_off != SIZE_MAX &&
+            cudaMemsetAsync(static_cast<unsigned char *>(ws) + sched_off, 0, 256,
                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
             return Q8_ERR_CUDA;
     }

@@ -403,6 +403,18 @@ Route route_of(int64_t K, int M, int variant) {
 
 }  // namespace
 
+size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off) {
+    size_t need = count > 0 ? plan_skinny(descs, count, M, plans) : 0;
+    *sched_off = SIZE_MAX;
+    bool gemv = false;
+    for (int i = 0; i < count; ++i) gemv = gemv || route_of(descs[i].K, M, Q8_VARIANT_AUTO) == kRouteGemv;
+    if (gemv) {
+        *sched_off = (need + 255) / 256 * 256;
+        need = *sched_off + 256;
+    }
+    return need;
+}
+
 q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream) {
     const DeviceInfo *di = device_info();
@@ -414,17 +426,21 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
         part[r][n[r]++] = all[i];
     }
     // the documented workspace (the plan of every matrix, whatever kernel
-    // serves it) is checked before anything is enqueued; the general kernel
-    // uses the front of it
+    // serves it, and the GEMV's pool counter) is checked before anything is
+    // enqueued; the general kernel uses the front of it
     SplitPlan plans[Q8_MAX_BATCH];
-    const size_t need = plan_skinny(all, all_count, M, plans);
+    size_t sched_off;
+    const size_t need = skinny_workspace(all, all_count, M, plans, &sched_off);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return Q8_ERR_ALIGN;
     const q8_linear_desc *descs = part[kRouteGeneral];
     const int count = n[kRouteGeneral];
     if (count > 0) plan_skinny(descs, count, M, plans);
     if (n[kRouteGemv] > 0) {
-        const q8_status st = launch_gemv(part[kRouteGemv], n[kRouteGemv], dev_status, stream);
+        uint32_t *sched = sched_off == SIZE_MAX
+                              ? nullptr
+                              : reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + sched_off);
+        const q8_status st = launch_gemv(part[kRouteGemv], n[kRouteGemv], sched, dev_status, stream);
         if (st != Q8_OK) return st;
     }
     if (n[kRoutePipe] > 0) {

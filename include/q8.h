@@ -144,6 +144,10 @@ typedef struct q8_linear_desc {
  *   descs : HOST array of `count` descriptors, 1 <= count <= Q8_MAX_BATCH;
  *           copied into the launch, may be reused on return.
  *   ws    : q8_linear_batch_workspace_size(descs, count, M) bytes, zeroed once.
+ *           At M = 1 it ends with a 256-byte block whose first word the GEMV
+ *           uses as a work counter (it hands its last stages to whichever CTA
+ *           is free first) and leaves zero; after a Q8_DEV_TIMEOUT zero the
+ *           workspace again.
  * Each output equals, bit for bit, what q8_gemm_skinny returns for that matrix.
  * Outputs must not overlap each other or any input.
  */

@@ -126,11 +126,13 @@ def test_workspace_sizes(L):
     assert L.q8_workspace_size(0, 64, 1) == 0
     assert L.q8_workspace_size(64, 33, 1) == 0
     assert L.q8_workspace_size(64, 64, 33) == 0
-    # a huge N needs no split; a short-N, long-K matrix does
-    assert L.q8_workspace_size(262144, 1536, 1) == 0
+    # a huge N needs no split, only (at M = 1) the 256-byte block of the
+    # GEMV's pool counter; a short-N, long-K matrix splits K as well
+    assert L.q8_workspace_size(262144, 1536, 1) == 256
+    assert L.q8_workspace_size(262144, 1536, 2) == 0
     w = L.q8_workspace_size(1536, 4096, 1)
-    assert w > 0 and w % 256 == 0
-    # a batch needs the sum of its members' workspaces
+    assert w > 256 and w % 256 == 0
+    # a batch needs the sum of its members' split workspaces and one counter block
     d = (q8.LinearDesc * 2)()
     d[0] = q8.LinearDesc(A, A, A, A, 1536, 4096, 4096, 1536)
     d[1] = q8.LinearDesc(A, A, A, A, 262144, 1536, 1536, 262144)

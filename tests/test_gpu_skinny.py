@@ -218,6 +218,57 @@ def test_tile_k_split_keeps_bits(oracle, M, K):
     check_tol(alone, y_ref, B, f"K split N=1536 K={K} M={M}")
 
 
+def test_gemv_pool_counter_returns_to_zero(oracle):
+    """The M = 1 kernel hands out its last stages through a counter in the
+    workspace; every launch must leave it zero, or the next launch on the same
+    workspace would skip stages.  Repeated calls and graph replays on one
+    workspace give the same bits, and the counter block reads zero after."""
+    from block_quantized_int8_gb300 import q8
+    mats, ys, host = [], [], []
+    for i, (N, K) in enumerate([(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096)] * 4):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"pc{i % 4}"))
+        xn = synth.activations(1, K, 0, f"pcx{i}")
+        host.append((qn, sn, xn))
+        q, s = weights_dev(qn, sn)
+        x = x_dev(xn)
+        y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+        mats.append((q, s, x, y))
+        ys.append(y)
+    descs, M = q8.make_descs(mats)
+    need = q8.q8_linear_batch_workspace_size(descs, M)
+    assert need >= 256
+    ws = q8.workspace(need)
+    q8.q8_linear_batch(descs=descs, M=M, ws=ws)
+    torch.cuda.synchronize()
+    first = [y.clone() for y in ys]
+    assert int(ws.view(-1)[-256:].count_nonzero()) == 0
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        q8.q8_linear_batch(descs=descs, M=M, ws=ws)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(ys, first))
+        assert int(ws.view(-1)[-256:].count_nonzero()) == 0
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        q8.q8_linear_batch(descs=descs, M=M, ws=ws)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        q8.q8_linear_batch(descs=descs, M=M, ws=ws)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(ys, first))
+    assert int(ws.view(-1)[-256:].count_nonzero()) == 0
+    # and the result is right
+    for (qn, sn, xn), y in zip(host[:4], ys[:4]):
+        y_ref, B = oracle.matmul(qn, sn, xn, threads=8)
+        check_tol(y.cpu().numpy(), y_ref, B, "pooled GEMV")
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_deterministic_and_graph_replay(oracle, variant):
     from block_quantized_int8_gb300 import q8
