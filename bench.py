@@ -212,9 +212,10 @@ class LayerSet:
         self.ws = q8.workspace(ws_need, dev)
         self.launches_per_step = synth.PASSES
 
-    def step(self, variant=0, stream=None):
+    def step(self, variant=0, stream=None, chained=False):
         for p in range(synth.PASSES):
-            self.q8.q8_linear_batch(descs=self.descs[p], M=1, ws=self.ws, variant=variant, stream=stream)
+            self.q8.q8_linear_batch(descs=self.descs[p], M=1, ws=self.ws, variant=variant, stream=stream,
+                                    chained=chained)
 
     def check_sample(self, oracle_mod=None):
         """Cheap consistency check of pass 0 against the oracle on a few rows."""
@@ -255,7 +256,7 @@ def per_launch_ms(torch, ls, reps, variant=0):
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
-def e2e_gbs(torch, ls, steps, bytes_per_step):
+def e2e_gbs(torch, ls, steps, bytes_per_step, chained=False):
     """Whole step through the public API with host buffers: one pinned H2D copy
     of every pass's activations, the 8 batch launches, a D2H copy of each
     pass's outputs (issued on a second stream as soon as that pass is done, so
@@ -273,7 +274,7 @@ def e2e_gbs(torch, ls, steps, bytes_per_step):
         cs = torch.cuda.current_stream()
         ls.x_all.view(torch.int16).copy_(xh, non_blocking=True)
         for p in range(synth.PASSES):
-            ls.q8.q8_linear_batch(descs=ls.descs[p], M=1, ws=ls.ws)
+            ls.q8.q8_linear_batch(descs=ls.descs[p], M=1, ws=ls.ws, chained=chained)
             done[p].record(cs)
             copy_stream.wait_event(done[p])
             with torch.cuda.stream(copy_stream):
@@ -541,6 +542,8 @@ def main():
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 SIMT, 2 MMA")
     ap.add_argument("--no-rows", action="store_true", help="skip the context rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="launch the passes with q8_linear_batch instead of q8_linear_batch_chained")
     ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16"], default=None,
                     help="run a few launches of one workload and exit (for ncu captures)")
     args = ap.parse_args()
@@ -576,7 +579,8 @@ def main():
 
     log("building the layer set ...")
     ls = LayerSet(torch, q8)
-    fn = lambda: ls.step(args.variant)  # noqa: E731
+    chained = args.variant == 0 and not args.no_chain
+    fn = lambda: ls.step(args.variant, chained=chained)  # noqa: E731
 
     clk = ClockSampler(local_rank)
     clk.start()
@@ -604,7 +608,7 @@ def main():
     achieved = bytes_pass / (launch_ms / 1e3) / 1e9
     traffic, _ = profile_traffic()
 
-    e2e, h2d, d2h = e2e_gbs(torch, ls, max(20, min(200, args.steps // 10)), bytes_step)
+    e2e, h2d, d2h = e2e_gbs(torch, ls, max(20, min(200, args.steps // 10)), bytes_step, chained)
 
     rows = {} if (args.no_rows or rank != 0) else extra_rows(torch, q8, peak)
 
@@ -620,7 +624,10 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int8xbf16->f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": 1, "layers": synth.LAYERS, "passes": synth.PASSES,
-                       "bytes_per_step": bytes_step, "launch": "one q8_linear_batch per pass (64 matrices)",
+                       "bytes_per_step": bytes_step,
+                       "launch": ("one q8_linear_batch_chained per pass (64 matrices; weights fixed, so each "
+                                  "launch may start while the previous one finishes)") if chained
+                       else "one q8_linear_batch per pass (64 matrices)",
                        "variant": ["auto", "simt", "mma"][args.variant],
                        "l2": "no flush: 481 MB of weights per pass > 129 MB L2",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},

@@ -119,8 +119,10 @@ size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count
     return skinny_workspace(tmp, n, M, pl, &sched_off);
 }
 
-q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant,
-                             void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+namespace {
+
+q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant, void *ws,
+                       size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream, bool chained) {
     if (!descs || count < 0 || count > Q8_MAX_BATCH) return Q8_ERR_ARG;
     if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_MMA) return Q8_ERR_ARG;
     if (M < 0 || M > Q8_SKINNY_MAX_M) return Q8_ERR_SHAPE;
@@ -137,7 +139,20 @@ q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t
     const DeviceInfo *di;
     q8_status st = check_arch(&di);
     if (st != Q8_OK) return st;
-    return launch_skinny(live, n, M, variant, ws, ws_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
+    return launch_skinny(live, n, M, variant, ws, ws_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream),
+                         chained);
+}
+
+}  // namespace
+
+q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant,
+                             void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+    return linear_batch(descs, count, M, variant, ws, ws_bytes, dev_status, stream, false);
+}
+
+q8_status q8_linear_batch_chained(const q8_linear_desc *descs, int32_t count, int32_t M, void *ws,
+                                  size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
+    return linear_batch(descs, count, M, Q8_VARIANT_AUTO, ws, ws_bytes, dev_status, stream, true);
 }
 
 q8_status q8_linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M,

@@ -89,6 +89,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching (its CTAs take SM slots as ours exit), and wait until the
+// kernels before this one have completed and their writes are visible (a
+// no-op when this kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 1-D bulk copy global -> shared, completing `bytes` on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

@@ -89,6 +89,7 @@ struct GParams {
     int32_t total_stages;
     int32_t grid;
     int32_t pool_total;     // stages in the pool
+    int32_t chained;        // launched as a programmatic dependent: weights may be read early
     int32_t cta_begin[kMaxGrid + 1];  // CTA c's balanced range [cta_begin[c], cta_begin[c+1])
     int32_t cta_split[kMaxGrid];      // it owns [cta_begin[c], cta_split[c]); the rest is pooled
     int32_t pool_off[kMaxGrid + 1];   // pool index of the first pooled stage of CTA c's range
@@ -360,7 +361,6 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
     bool prod_ok = true;                // false once timed out or past the end marker
     uint32_t ahead = 0xFFFFFFFFu;       // pool index drawn for the next pool position
     auto draw = [&]() { ahead = p.sched ? atomicAdd(p.sched, 1u) : 0xFFFFFFFFu; };
-    if (warp == 0 && lane == 0 && nown == 0) draw();
     auto produce = [&](int upto) {
         while (prod_ok && pi <= upto) {
             const int slot = pi % kStages;
@@ -459,6 +459,12 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
             for (int e = 0; e < 8; ++e) xr[j][e] = f2_pack(bf16lo_f32(v[e]), bf16hi_f32(v[e]));
         }
     };
+    // Chained launch: the first own stages that need no draw (weights only) are
+    // issued before the previous kernel in the stream has completed; x, y and
+    // the counter are touched only after the wait below.
+    if (p.chained && warp == 0 && lane == 0) produce(min(kStages, nown - 1) - 1);
+    pdl_wait_prior();
+    if (warp == 0 && lane == 0 && nown == 0) draw();
     for (int k = 0;; ++k) {
         if (warp == 0 && lane == 0) produce(k + kStages - 1);
         __syncwarp();
@@ -538,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
     for (int i = tid; i < 2 * kStages * kRedRows; i += kThreads) (&sm.cnt[0][0])[i] = 0u;
     __syncthreads();
+    // a chained launch after this one may start as soon as SM slots free up
+    if (tid == 0) pdl_launch_dependents();
     cta_work<kJMax>(p, sm, begin, split, warp, lane);
 }
 
@@ -549,7 +557,7 @@ int g_occ = 0;
 bool gemv_k_supported(int64_t K) { return K <= kMaxK; }
 
 q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, uint32_t *dev_status,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool chained) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (g_configured_dev != di->device) {
@@ -619,6 +627,21 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, u
         p.pool_off[b + 1] = p.pool_off[b] + (len - own);
     }
     p.pool_total = p.pool_off[grid];
+    p.chained = chained ? 1 : 0;
+    if (chained) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = sizeof(Smem);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gemv_kernel, p) != cudaSuccess) return Q8_ERR_CUDA;
+        return Q8_OK;
+    }
     gemv_kernel<<<grid, kThreads, sizeof(Smem), stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }

@@ -53,8 +53,11 @@ size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan
 bool gemv_k_supported(int64_t K);
 // sched: a zeroed device word the launch uses as its pool counter and leaves
 // zero again (null: every CTA keeps its whole static range).
+// chained: launched as a programmatic dependent of the previous kernel in the
+// stream; the first weight stages are read before that kernel completes,
+// x, y and the counter only after.
 q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, uint32_t *dev_status,
-                      cudaStream_t stream);
+                      cudaStream_t stream, bool chained = false);
 
 // 1 <= M <= 8 bulk-copy pipeline with warp MMA (q8_pipe.cu): K <= 4096.
 bool pipe_k_supported(int64_t K);
@@ -74,7 +77,8 @@ bool encode_tmap(CUtensorMap *map, int elem_bytes, const void *base, int rank, c
                  const uint64_t *stride_bytes, const uint32_t *box, bool swizzle128);
 
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
-                        void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream);
+                        void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream,
+                        bool chained = false);
 
 // Host-only argument check of one skinny matmul, as q8_gemm_skinny does it.
 q8_status check_skinny_args(const q8_linear_desc &d, int32_t M);

@@ -416,7 +416,7 @@ size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan
 }
 
 q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int variant,
-                        void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream) {
+                        void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream, bool chained) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     static thread_local q8_linear_desc part[kRoutes][Q8_MAX_BATCH];
@@ -440,7 +440,7 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
         uint32_t *sched = sched_off == SIZE_MAX
                               ? nullptr
                               : reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + sched_off);
-        const q8_status st = launch_gemv(part[kRouteGemv], n[kRouteGemv], sched, dev_status, stream);
+        const q8_status st = launch_gemv(part[kRouteGemv], n[kRouteGemv], sched, dev_status, stream, chained);
         if (st != Q8_OK) return st;
     }
     if (n[kRoutePipe] > 0) {

@@ -33,7 +33,7 @@ Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA = 0, 1, 2
 Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_128x64 = 0, 1, 2, 3
 
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
-           "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
+           "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
            "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex")
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -66,6 +66,7 @@ def lib():
         L.q8_gemm_skinny.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, P, SZ, U32P, P]
         L.q8_linear_batch.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, P, SZ, U32P, P]
         L.q8_linear_batch_ex.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, I32, P, SZ, U32P, P]
+        L.q8_linear_batch_chained.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, P, SZ, U32P, P]
         L.q8_workspace_size.argtypes = [I64, I64, I32]
         L.q8_workspace_size.restype = SZ
         L.q8_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32, I32]
@@ -77,7 +78,7 @@ def lib():
         L.q8_status_str.restype = ctypes.c_char_p
         L.q8_abi_version.restype = I32
         for name in ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
-                     "q8_linear_batch_ex", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc"):
+                     "q8_linear_batch_ex", "q8_linear_batch_chained", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -221,16 +222,24 @@ def q8_linear_batch_workspace_size(descs, M: int) -> int:
 
 
 def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None, stream=None,
-                    descs=None, M=None):
+                    descs=None, M=None, chained=False):
     """Run several skinny matmuls in one launch.  ``mats`` = [(q, s, x, y), ...],
-    or pass prepared ``descs`` (from make_descs) and ``M``."""
+    or pass prepared ``descs`` (from make_descs) and ``M``.  ``chained=True``
+    calls q8_linear_batch_chained (no earlier work in the stream may write
+    the weights; the variant is then automatic)."""
     if descs is None:
         descs, M = make_descs(mats)
     need = q8_linear_batch_workspace_size(descs, M)
     if ws is None and need:
         ws = workspace(need)
-    st = lib().q8_linear_batch_ex(descs, len(descs), M, variant, _p(ws), 0 if ws is None else ws.numel(),
-                                  _p(dev_status), _stream(stream))
+    nbytes = 0 if ws is None else ws.numel()
+    if chained:
+        if variant != Q8_VARIANT_AUTO:
+            raise ValueError("a chained call uses the automatic variant")
+        st = lib().q8_linear_batch_chained(descs, len(descs), M, _p(ws), nbytes, _p(dev_status), _stream(stream))
+    else:
+        st = lib().q8_linear_batch_ex(descs, len(descs), M, variant, _p(ws), nbytes, _p(dev_status),
+                                      _stream(stream))
     _check(st, "q8_linear_batch")
 
 

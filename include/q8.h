@@ -155,6 +155,21 @@ q8_status q8_linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M,
                           void *ws, size_t ws_bytes,
                           uint32_t *dev_status, q8_stream_t stream);
 
+/*
+ * q8_linear_batch_chained -- as q8_linear_batch, for a stream of calls whose
+ * weights no earlier work in the stream writes (a decode loop over fixed
+ * model weights).  The launch may start while the previous kernel in the
+ * stream is finishing (programmatic dependent launch): it reads the first
+ * stages of weights (q, s) before that kernel completes, and x, y and ws only
+ * after it has completed and its writes are visible.  So the previous work
+ * may produce x, but must not write any q or s of this call.  Same results,
+ * bit for bit, as q8_linear_batch.  M = 1 matrices served by the GEMV start
+ * early; other kernels run as in q8_linear_batch.
+ */
+q8_status q8_linear_batch_chained(const q8_linear_desc *descs, int32_t count, int32_t M,
+                                  void *ws, size_t ws_bytes,
+                                  uint32_t *dev_status, q8_stream_t stream);
+
 /* As q8_linear_batch / q8_gemm_skinny with an explicit kernel variant
  * (Q8_VARIANT_*), for side-by-side measurement.  Variants agree within the
  * accuracy bound, not bit for bit. */

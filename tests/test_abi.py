@@ -96,6 +96,11 @@ def test_batch_validation(L):
     d[1].x = A + 2
     assert L.q8_linear_batch(d, 2, 1, None, 0, None, None) == q8.Q8_ERR_ALIGN
     assert L.q8_linear_batch(d, 0, 1, None, 0, None, None) == q8.Q8_OK
+    # the chained entry point checks the same way before anything is launched
+    assert L.q8_linear_batch_chained(d, 65, 1, None, 0, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_batch_chained(None, 1, 1, None, 0, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_batch_chained(d, 2, 1, None, 0, None, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_linear_batch_chained(d, 0, 1, None, 0, None, None) == q8.Q8_OK
 
 
 def test_quantize_validation(L):

@@ -269,6 +269,61 @@ def test_gemv_pool_counter_returns_to_zero(oracle):
         check_tol(y.cpu().numpy(), y_ref, B, "pooled GEMV")
 
 
+@pytest.mark.parametrize("M", [1, 4])
+def test_chained_calls_match_plain_calls(oracle, M):
+    """q8_linear_batch_chained over a stream of passes (new x each pass, one
+    workspace, weights fixed) gives the same bits as q8_linear_batch, also in
+    a CUDA graph, and leaves the M = 1 pool counter zero."""
+    from block_quantized_int8_gb300 import q8
+    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096)]
+    w = []
+    for i, (N, K) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"ch{i}"))
+        w.append(weights_dev(qn, sn))
+    passes = 6
+    xs = [[x_dev(synth.activations(M, K, 0, f"chx{p}.{i}")) for i, (N, K) in enumerate(shapes)]
+          for p in range(passes)]
+
+    def run(chained, graph=False):
+        ys = [[torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for (N, K) in shapes]
+              for _ in range(passes)]
+        descs = [q8.make_descs([(w[i][0], w[i][1], xs[p][i], ys[p][i]) for i in range(len(shapes))])[0]
+                 for p in range(passes)]
+        ws = q8.workspace(max(q8.q8_linear_batch_workspace_size(d, M) for d in descs))
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def step():
+            for d in descs:
+                q8.q8_linear_batch(descs=d, M=M, ws=ws, dev_status=st, chained=chained)
+        if graph:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                step()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            for _ in range(2):
+                g.replay()
+        else:
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        if ws is not None and M == 1:
+            assert int(ws.view(-1)[-256:].count_nonzero()) == 0
+        return [[y.cpu() for y in row] for row in ys]
+
+    plain = run(False)
+    for got in (run(True), run(True, graph=True)):
+        for p in range(passes):
+            for a, b in zip(plain[p], got[p]):
+                assert torch.equal(a, b)
+    qn, sn, _ = oracle.quantize_rows(synth.weights(1536, 4096, 0, "ch3"))
+    y_ref, B = oracle.matmul(qn, sn, synth.activations(M, 4096, 0, "chx5.3"), threads=8)
+    check_tol(plain[5][3].numpy(), y_ref, B, "chained pass 5")
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_deterministic_and_graph_replay(oracle, variant):
     from block_quantized_int8_gb300 import q8
