@@ -340,6 +340,16 @@ def extra_rows(torch, q8, peak):
     qbytes = N * K * 4 + N * K + N * K // 16
     rows["quantize_262144x1536"] = {"GB/s": round(qbytes / t / 1e9, 1), "frac": round(qbytes / t / 1e9 / peak, 3),
                                     "us": round(t * 1e6, 2)}
+    # GGUF Q8_0 ingest of that matrix (34 B in, 34 B out per block) and export
+    raw = q8.q8_planar_to_gguf(wq, ws_)
+    t = timed([lambda: q8.q8_gguf_to_planar(raw, N, K, qb, sb)], reps=5)
+    gbytes = 2 * raw.numel()
+    rows["gguf_ingest_262144x1536"] = {"GB/s": round(gbytes / t / 1e9, 1), "frac": round(gbytes / t / 1e9 / peak, 3),
+                                       "us": round(t * 1e6, 2)}
+    t = timed([lambda: q8.q8_planar_to_gguf(wq, ws_, raw)], reps=5)
+    rows["gguf_export_262144x1536"] = {"GB/s": round(gbytes / t / 1e9, 1), "frac": round(gbytes / t / 1e9 / peak, 3),
+                                       "us": round(t * 1e6, 2)}
+    del raw
     wsmall = torch.from_numpy(synth.quant_stress_rows()).to(dev)
     t = timed([lambda: q8.q8_quantize_rows(wsmall)], reps=50)
     rows["quantize_32x4096"] = {"us": round(t * 1e6, 2)}

@@ -84,6 +84,12 @@ const char *q8_status_str(q8_status st) {
 
 q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K, int8_t *q, uint16_t *s,
                            uint32_t *dev_status, q8_stream_t stream) {
+    return q8_quantize_rows_ex(w, rows, K, q, s, Q8_QUANT_EXACT, dev_status, stream);
+}
+
+q8_status q8_quantize_rows_ex(const float *w, int64_t rows, int64_t K, int8_t *q, uint16_t *s, int32_t mode,
+                              uint32_t *dev_status, q8_stream_t stream) {
+    if (mode != Q8_QUANT_EXACT && mode != Q8_QUANT_FL32) return Q8_ERR_ARG;
     if (rows < 0 || K <= 0 || (K % 32) != 0) return Q8_ERR_SHAPE;
     if (rows == 0) return Q8_OK;
     if (!w || !q || !s) return Q8_ERR_ARG;
@@ -92,7 +98,33 @@ q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K, int8_t *q, u
     const DeviceInfo *di;
     q8_status st = check_arch(&di);
     if (st != Q8_OK) return st;
-    return launch_quantize(w, rows, K, q, s, dev_status, reinterpret_cast<cudaStream_t>(stream));
+    return launch_quantize(w, rows, K, q, s, dev_status, reinterpret_cast<cudaStream_t>(stream), mode);
+}
+
+q8_status q8_gguf_to_planar(const void *blocks, int64_t rows, int64_t K, int8_t *q, uint16_t *s,
+                            q8_stream_t stream) {
+    if (rows < 0 || K <= 0 || (K % 32) != 0) return Q8_ERR_SHAPE;
+    if (rows == 0) return Q8_OK;
+    if (!blocks || !q || !s) return Q8_ERR_ARG;
+    if (!aligned(blocks, 16) || !aligned(q, 16) || !aligned(s, 16)) return Q8_ERR_ALIGN;
+    if (rows > INT64_MAX / K) return Q8_ERR_SHAPE;
+    const DeviceInfo *di;
+    q8_status st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_gguf_ingest(blocks, rows * (K / 32), q, s, reinterpret_cast<cudaStream_t>(stream));
+}
+
+q8_status q8_planar_to_gguf(const int8_t *q, const uint16_t *s, int64_t rows, int64_t K, void *blocks,
+                            q8_stream_t stream) {
+    if (rows < 0 || K <= 0 || (K % 32) != 0) return Q8_ERR_SHAPE;
+    if (rows == 0) return Q8_OK;
+    if (!blocks || !q || !s) return Q8_ERR_ARG;
+    if (!aligned(blocks, 16) || !aligned(q, 16) || !aligned(s, 16)) return Q8_ERR_ALIGN;
+    if (rows > INT64_MAX / K) return Q8_ERR_SHAPE;
+    const DeviceInfo *di;
+    q8_status st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_gguf_export(q, s, rows * (K / 32), blocks, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {

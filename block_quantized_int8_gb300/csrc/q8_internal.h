@@ -21,8 +21,9 @@ struct DeviceInfo {
 const DeviceInfo *device_info();
 
 // ---- quantizer --------------------------------------------------------------
+// mode: Q8_QUANT_EXACT (codes from the stored scale) or Q8_QUANT_FL32.
 q8_status launch_quantize(const float *w, int64_t rows, int64_t K, int8_t *q, uint16_t *s,
-                          uint32_t *dev_status, cudaStream_t stream);
+                          uint32_t *dev_status, cudaStream_t stream, int mode = Q8_QUANT_EXACT);
 
 // ---- skinny matmul (M <= 32) -------------------------------------------------
 constexpr int kSkinnyWarps = 8;
@@ -66,6 +67,11 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
 // 2 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256.
 bool tile_k_supported(int64_t K);
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
+
+// GGUF Q8_0 block repack (q8_gguf.cu): nblocks blocks of 34 bytes (binary16
+// scale, 32 int8 codes) <-> planar codes (32 bytes per block) and scales.
+q8_status launch_gguf_ingest(const void *blocks, int64_t nblocks, int8_t *q, uint16_t *s, cudaStream_t stream);
+q8_status launch_gguf_export(const int8_t *q, const uint16_t *s, int64_t nblocks, void *blocks, cudaStream_t stream);
 
 // 2-D TMA tensor map over a row-major [outer][inner] array of 1- or 2-byte
 // elements (q8_tmap.cu; cached by parameters).  false if encoding fails.

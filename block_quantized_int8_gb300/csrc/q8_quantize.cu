@@ -13,6 +13,12 @@
 // products (k +- 1/2)*s are exact in binary32 (9-bit times 11-bit
 // significands) and one compare in each direction fixes the estimate.
 //
+// Compatibility mode (Q8_QUANT_FL32): the code is the binary32 quotient
+// w / d32 (IEEE division, d32 = amax/127 before the binary16 rounding of the
+// stored scale) rounded half away from zero -- ACT 4's q8round applied to a
+// float32 value: truncate, recover the fraction exactly, step away from zero
+// when it is at least one half.
+//
 // Layout: 8 lanes own one block (a float4 each); a warp covers four blocks,
 // 512 contiguous bytes per load.  Bandwidth-bound: 4 B read + 1.0625 B written
 // per weight.
@@ -35,6 +41,16 @@ __device__ __forceinline__ int32_t code_of(float v, float sf, float rcp) {
     return v < 0.0f ? -ki : ki;
 }
 
+__device__ __forceinline__ int32_t code_fl32(float v, float d) {
+    const float t = __fdiv_rn(v, d);
+    const float k0 = truncf(t);
+    float k = fabsf(k0);
+    if (fabsf(__fsub_rn(t, k0)) >= 0.5f) k = __fadd_rn(k, 1.0f);  // t - trunc(t) is exact
+    const int32_t ki = static_cast<int32_t>(fminf(k, 127.0f));
+    return t < 0.0f ? -ki : ki;
+}
+
+template <bool FL32>
 __global__ void __launch_bounds__(256)
 quantize_kernel(const float *__restrict__ w, int64_t nblocks, uint32_t *__restrict__ q,
                 uint16_t *__restrict__ s, uint32_t *__restrict__ status) {
@@ -63,11 +79,19 @@ quantize_kernel(const float *__restrict__ w, int64_t nblocks, uint32_t *__restri
         if (flags) {
             sbits = 0;
         } else if (sf != 0.0f) {
-            const float rcp = __frcp_rn(sf);
-            const uint32_t c0 = static_cast<uint32_t>(code_of(v.x, sf, rcp)) & 0xFFu;
-            const uint32_t c1 = static_cast<uint32_t>(code_of(v.y, sf, rcp)) & 0xFFu;
-            const uint32_t c2 = static_cast<uint32_t>(code_of(v.z, sf, rcp)) & 0xFFu;
-            const uint32_t c3 = static_cast<uint32_t>(code_of(v.w, sf, rcp)) & 0xFFu;
+            uint32_t c0, c1, c2, c3;
+            if constexpr (FL32) {
+                c0 = static_cast<uint32_t>(code_fl32(v.x, d)) & 0xFFu;
+                c1 = static_cast<uint32_t>(code_fl32(v.y, d)) & 0xFFu;
+                c2 = static_cast<uint32_t>(code_fl32(v.z, d)) & 0xFFu;
+                c3 = static_cast<uint32_t>(code_fl32(v.w, d)) & 0xFFu;
+            } else {
+                const float rcp = __frcp_rn(sf);
+                c0 = static_cast<uint32_t>(code_of(v.x, sf, rcp)) & 0xFFu;
+                c1 = static_cast<uint32_t>(code_of(v.y, sf, rcp)) & 0xFFu;
+                c2 = static_cast<uint32_t>(code_of(v.z, sf, rcp)) & 0xFFu;
+                c3 = static_cast<uint32_t>(code_of(v.w, sf, rcp)) & 0xFFu;
+            }
             packed = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
         }
         if (valid) {
@@ -81,7 +105,7 @@ quantize_kernel(const float *__restrict__ w, int64_t nblocks, uint32_t *__restri
 }
 
 q8_status launch_quantize(const float *w, int64_t rows, int64_t K, int8_t *q, uint16_t *s,
-                          uint32_t *dev_status, cudaStream_t stream) {
+                          uint32_t *dev_status, cudaStream_t stream, int mode) {
     const int64_t nblocks = rows * (K / 32);
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
@@ -91,8 +115,12 @@ q8_status launch_quantize(const float *w, int64_t rows, int64_t K, int8_t *q, ui
     const int64_t cap = static_cast<int64_t>(di->sm_count) * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    quantize_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(
-        w, nblocks, reinterpret_cast<uint32_t *>(q), s, dev_status);
+    if (mode == Q8_QUANT_FL32)
+        quantize_kernel<true><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
+            w, nblocks, reinterpret_cast<uint32_t *>(q), s, dev_status);
+    else
+        quantize_kernel<false><<<static_cast<unsigned>(grid), threads, 0, stream>>>(
+            w, nblocks, reinterpret_cast<uint32_t *>(q), s, dev_status);
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 

@@ -31,10 +31,12 @@ Q8_SKINNY_MAX_M = 32
 Q8_MAX_BATCH = 64
 Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA = 0, 1, 2
 Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_128x64 = 0, 1, 2, 3
+Q8_QUANT_EXACT, Q8_QUANT_FL32 = 0, 1
 
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
            "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
-           "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex")
+           "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex", "q8_gguf_to_planar",
+           "q8_planar_to_gguf", "q8_quantize_rows_ex")
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -62,6 +64,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         P, I64, I32, SZ, U32P = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
         L.q8_quantize_rows.argtypes = [P, I64, I64, P, P, U32P, P]
+        L.q8_quantize_rows_ex.argtypes = [P, I64, I64, P, P, I32, U32P, P]
         L.q8_gemv.argtypes = [P, P, I64, I64, P, P, P, SZ, U32P, P]
         L.q8_gemm_skinny.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, P, SZ, U32P, P]
         L.q8_linear_batch.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, P, SZ, U32P, P]
@@ -74,11 +77,14 @@ def lib():
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, U32P, P]
         L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
+        L.q8_gguf_to_planar.argtypes = [P, I64, I64, P, P, P]
+        L.q8_planar_to_gguf.argtypes = [P, P, I64, I64, P, P]
         L.q8_status_str.argtypes = [ctypes.c_int]
         L.q8_status_str.restype = ctypes.c_char_p
         L.q8_abi_version.restype = I32
-        for name in ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
-                     "q8_linear_batch_ex", "q8_linear_batch_chained", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc"):
+        for name in ("q8_quantize_rows", "q8_quantize_rows_ex", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
+                     "q8_linear_batch_ex", "q8_linear_batch_chained", "q8_gguf_to_planar",
+                     "q8_planar_to_gguf", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -126,8 +132,9 @@ def workspace(nbytes: int, device=None) -> torch.Tensor | None:
 
 
 # ---------------------------------------------------------------------------
-def q8_quantize_rows(w, q=None, s=None, dev_status=None, stream=None):
-    """Q8_0-quantize float32 w[rows, K] -> (q int8 [rows, K], s float16 [rows, K/32])."""
+def q8_quantize_rows(w, q=None, s=None, dev_status=None, stream=None, mode=Q8_QUANT_EXACT):
+    """Q8_0-quantize float32 w[rows, K] -> (q int8 [rows, K], s float16 [rows, K/32]);
+    ``mode`` picks the code rule (Q8_QUANT_EXACT or Q8_QUANT_FL32)."""
     _cuda(w, "w", (torch.float32,), 2)
     if not w.is_contiguous():
         raise ValueError("w must be contiguous")
@@ -136,9 +143,36 @@ def q8_quantize_rows(w, q=None, s=None, dev_status=None, stream=None):
         q = torch.empty((rows, K), dtype=torch.int8, device=w.device)
     if s is None:
         s = torch.empty((rows, max(K // 32, 0)), dtype=torch.float16, device=w.device)
-    st = lib().q8_quantize_rows(_p(w), rows, K, _p(q), _p(s), _p(dev_status), _stream(stream))
+    st = lib().q8_quantize_rows_ex(_p(w), rows, K, _p(q), _p(s), int(mode), _p(dev_status), _stream(stream))
     _check(st, "q8_quantize_rows")
     return q, s
+
+
+def q8_gguf_to_planar(blocks, rows: int, K: int, q=None, s=None, stream=None):
+    """GGUF Q8_0 bytes (uint8, rows * K/32 blocks of 34 bytes) -> (q int8 [rows, K],
+    s float16 [rows, K/32])."""
+    _cuda(blocks, "blocks", (torch.uint8,))
+    if not blocks.is_contiguous() or blocks.numel() != rows * (K // 32) * 34:
+        raise ValueError("blocks must be contiguous and hold rows * K/32 blocks of 34 bytes")
+    if q is None:
+        q = torch.empty((rows, K), dtype=torch.int8, device=blocks.device)
+    if s is None:
+        s = torch.empty((rows, K // 32), dtype=torch.float16, device=blocks.device)
+    st = lib().q8_gguf_to_planar(_p(blocks), rows, K, _p(q), _p(s), _stream(stream))
+    _check(st, "q8_gguf_to_planar")
+    return q, s
+
+
+def q8_planar_to_gguf(q, s, blocks=None, stream=None):
+    """(q int8 [rows, K], s binary16 [rows, K/32]) -> GGUF Q8_0 bytes (uint8)."""
+    _cuda(q, "q", (torch.int8,), 2)
+    _cuda(s, "s", _B16, 2)
+    rows, K = q.shape
+    if blocks is None:
+        blocks = torch.empty(rows * (K // 32) * 34, dtype=torch.uint8, device=q.device)
+    st = lib().q8_planar_to_gguf(_p(q), _p(s), rows, K, _p(blocks), _stream(stream))
+    _check(st, "q8_planar_to_gguf")
+    return blocks
 
 
 def q8_workspace_size(N: int, K: int, M: int) -> int:

@@ -90,6 +90,44 @@ q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K,
                            int8_t *q, uint16_t *s,
                            uint32_t *dev_status, q8_stream_t stream);
 
+/* Code rules of q8_quantize_rows_ex. */
+#define Q8_QUANT_EXACT 0  /* as q8_quantize_rows: exact quotient by the stored binary16 scale */
+#define Q8_QUANT_FL32 1   /* compatibility: binary32 quotient w / d (d = amax/127 in binary32) */
+
+/*
+ * q8_quantize_rows_ex -- q8_quantize_rows with a choice of code rule.
+ * Q8_QUANT_FL32 rounds (half away from zero, clamp +-127) the binary32
+ * quotient w / d, IEEE division by the binary32 scale d = amax/127 before its
+ * rounding to the stored binary16 s -- the float32 value that
+ * "MODEL-BASELINE-RESULTS" (fak), ACT 4 "Correctness", rounds with q8round.
+ * Scales, flags and the zero-scale rule are those of Q8_QUANT_EXACT; codes
+ * can differ by one where s != d.  Bit-identical to that definition.
+ * An unknown mode returns Q8_ERR_ARG.
+ */
+q8_status q8_quantize_rows_ex(const float *w, int64_t rows, int64_t K,
+                              int8_t *q, uint16_t *s, int32_t mode,
+                              uint32_t *dev_status, q8_stream_t stream);
+
+/*
+ * q8_gguf_to_planar -- repack a GGUF Q8_0 tensor into this library's layout.
+ * Source: the GGUF model files of the "aubier" README ("Layout": the engine's
+ * GGUF loader) and the serverAppConfigs log; the block is the Q8_0 block of
+ * "MODEL-BASELINE-RESULTS" (fak), ACT 3 item 1.
+ *   blocks : rows * K/32 blocks of 34 bytes, consecutive (a [rows][K] tensor
+ *            in GGUF order): binary16 scale d, then 32 int8 codes;
+ *            16-byte aligned                                       (in)
+ *   q      : int8 [rows][K], 16-byte aligned                       (out)
+ *   s      : binary16 bits [rows][K/32], 16-byte aligned           (out)
+ * Block g (row g / (K/32), block g % (K/32)) becomes q[32g .. 32g+32) and
+ * s[g], bit for bit.  K must be a positive multiple of 32.
+ */
+q8_status q8_gguf_to_planar(const void *blocks, int64_t rows, int64_t K,
+                            int8_t *q, uint16_t *s, q8_stream_t stream);
+
+/* q8_planar_to_gguf -- the inverse of q8_gguf_to_planar (same alignment). */
+q8_status q8_planar_to_gguf(const int8_t *q, const uint16_t *s, int64_t rows, int64_t K,
+                            void *blocks, q8_stream_t stream);
+
 /*
  * q8_gemv -- y[n] = sum_k s[n][k/32]*q[n][k]*x[k] for one activation row (M = 1).
  * Source: "Frigg" README, "The machine" (at batch 1 every decode GEMM is this

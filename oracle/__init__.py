@@ -15,6 +15,14 @@ Functions and what they follow (page titles of the source pages):
   B = sum |w' x|.
 * ``f32_to_f16`` / ``f16_to_f64`` / ``code`` -- the binary16 rounding and the
   single-weight code rule, exposed for exhaustive pins.
+* ``quantize_rows_fl32`` / ``code_fl32`` -- the compatibility code rule: the
+  binary32 quotient w / d32 rounded half away from zero ("MODEL-BASELINE-
+  RESULTS" (fak), ACT 4 "Correctness": q8round of a float32 value), with the
+  same binary16 stored scale.
+* ``gguf_to_planar`` / ``planar_to_gguf`` -- the GGUF Q8_0 block (34 bytes:
+  binary16 scale, then 32 int8 codes; the model files of the "aubier" README,
+  "Layout") split into planar codes and scales, and back: a numpy view of
+  the byte array as records, no arithmetic.
 
 Every function is pinned by the CPU test suite (see tests/test_oracle_*.py);
 none is "parity unpinned".
@@ -71,6 +79,9 @@ def _load():
         lib.q8ref_f32_to_f16_array.argtypes = [P, P, I64]
         lib.q8ref_f16_to_f64_array.argtypes = [P, P, I64]
         lib.q8ref_code_array.argtypes = [P, I64, ctypes.c_uint16, P]
+        lib.q8ref_code_fl32_array.argtypes = [P, I64, ctypes.c_float, P]
+        lib.q8ref_quantize_rows_fl32.argtypes = [P, I64, I64, P, P, P]
+        lib.q8ref_quantize_rows_fl32.restype = ctypes.c_uint32
         _lib = lib
     return _lib
 
@@ -102,6 +113,29 @@ def code(w, s_bits: int) -> np.ndarray:
     return out
 
 
+def code_fl32(w, d32: float) -> np.ndarray:
+    """Compatibility codes of ``w`` against the binary32 scale ``d32``:
+    round half away from zero of the binary32 quotient w / d32."""
+    a = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.int8)
+    _load().q8ref_code_fl32_array(_ptr(a), a.size, ctypes.c_float(float(np.float32(d32))), _ptr(out))
+    return out
+
+
+def quantize_rows_fl32(w: np.ndarray, with_flags: bool = False):
+    """As ``quantize_rows``, with the compatibility codes (``code_fl32`` of
+    each weight against d32 = amax/127 in binary32); same scales and flags."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    if w.ndim != 2 or w.shape[1] % 32:
+        raise ValueError("w must be [rows][K] with K a multiple of 32")
+    rows, K = w.shape
+    q = np.empty((rows, K), dtype=np.int8)
+    s = np.empty((rows, K // 32), dtype=np.uint16)
+    fl = np.empty((rows, K // 32), dtype=np.uint32)
+    allf = _load().q8ref_quantize_rows_fl32(_ptr(w), rows, K, _ptr(q), _ptr(s), _ptr(fl))
+    return q, s, (fl if with_flags else int(allf))
+
+
 def quantize_rows(w: np.ndarray, with_flags: bool = False):
     """Q8_0-quantize a [rows][K] binary32 matrix along K.
 
@@ -118,6 +152,30 @@ def quantize_rows(w: np.ndarray, with_flags: bool = False):
     fl = np.empty((rows, K // 32), dtype=np.uint32)
     allf = _load().q8ref_quantize_rows(_ptr(w), rows, K, _ptr(q), _ptr(s), _ptr(fl))
     return q, s, (fl if with_flags else int(allf))
+
+
+_GGUF_Q8_0 = np.dtype([("d", "<u2"), ("qs", "i1", (32,))])  # 34 bytes, no padding
+
+
+def gguf_to_planar(blocks: np.ndarray, rows: int, K: int):
+    """Planar (q int8 [rows][K], s uint16 [rows][K/32]) of a GGUF Q8_0 byte
+    array holding rows * K/32 consecutive blocks."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    if b.size != rows * (K // 32) * 34:
+        raise ValueError("blocks must hold rows * K/32 blocks of 34 bytes")
+    rec = b.view(_GGUF_Q8_0)
+    return rec["qs"].reshape(rows, K).copy(), rec["d"].reshape(rows, K // 32).copy()
+
+
+def planar_to_gguf(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """GGUF Q8_0 bytes of planar codes q [rows][K] and scales s [rows][K/32]."""
+    rows, K = q.shape
+    rec = np.empty(rows * (K // 32), dtype=_GGUF_Q8_0)
+    rec["d"] = np.asarray(s, dtype=np.uint16).reshape(-1)
+    rec["qs"] = np.asarray(q, dtype=np.int8).reshape(-1, 32)
+    return rec.view(np.uint8).copy()
 
 
 def matmul(q: np.ndarray, s: np.ndarray, x_bf16: np.ndarray, rows=None, threads: int = 1):

@@ -136,6 +136,24 @@ int8_t q8ref_code(float w, double s)
 }
 
 /* ---------------------------------------------------------------------- */
+/* Compatibility codes: the binary32 quotient w / d32 (IEEE division,      */
+/* round to nearest even; d32 = amax/127 in binary32, before the binary16  */
+/* rounding of the stored scale) rounded half away from zero and clamped   */
+/* to 127 -- the binary32 quotient that "MODEL-BASELINE-RESULTS" (fak),    */
+/* ACT 4 "Correctness", rounds with q8round.  The half-away rounding of a  */
+/* binary32 value is exact in binary64 (24 significant bits + 0.5).        */
+/* ---------------------------------------------------------------------- */
+int8_t q8ref_code_fl32(float w, float d32)
+{
+    if (d32 == 0.0f) return 0;
+    volatile float t = w / d32;
+    double a = fabs((double)t);
+    double k = floor(a + 0.5);
+    if (k > 127.0) k = 127.0;
+    return (int8_t)(t < 0.0f ? -k : k);
+}
+
+/* ---------------------------------------------------------------------- */
 /* Quantize rows x K binary32 weights into Q8_0 blocks along K.            */
 /*   q      : int8  [rows][K]                                              */
 /*   s_bits : binary16 bits [rows][K/32]                                   */
@@ -190,6 +208,52 @@ uint32_t q8ref_quantize_rows(const float *w, int64_t rows, int64_t K,
 /* q int8 [N][K], s_bits binary16 [N][K/32], x_bf16 bf16 bits [M][ldx],    */
 /* y and bnd binary64 [M][ldy] (bnd may be NULL).                          */
 /* ---------------------------------------------------------------------- */
+/* ---------------------------------------------------------------------- */
+/* As q8ref_quantize_rows, with the compatibility codes: the same scale    */
+/* d32, the same stored binary16 scale and flags, but each code is         */
+/* q8ref_code_fl32(w, d32); a stored scale of zero still gives zero codes. */
+/* ---------------------------------------------------------------------- */
+uint32_t q8ref_quantize_rows_fl32(const float *w, int64_t rows, int64_t K,
+                                  int8_t *q, uint16_t *s_bits, uint32_t *flags)
+{
+    uint32_t all = 0;
+    int64_t nb = K / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *blk = w + r * K + b * 32;
+            int8_t *qb = q + r * K + b * 32;
+            uint32_t fl = 0;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                if (!isfinite(blk[i])) fl |= Q8REF_FLAG_NONFINITE;
+                else if (fabsf(blk[i]) > amax) amax = fabsf(blk[i]);
+            }
+            uint16_t sb = 0;
+            volatile float d32 = 0.0f;
+            if (!fl) {
+                d32 = amax / 127.0f;
+                sb = q8ref_f32_to_f16(d32);
+                if ((sb & 0x7c00u) == 0x7c00u) fl |= Q8REF_FLAG_SCALE_OVF;
+            }
+            if (fl || sb == 0) {
+                for (int i = 0; i < 32; ++i) qb[i] = 0;
+                s_bits[r * nb + b] = fl ? 0 : sb;
+            } else {
+                for (int i = 0; i < 32; ++i) qb[i] = q8ref_code_fl32(blk[i], d32);
+                s_bits[r * nb + b] = sb;
+            }
+            if (flags) flags[r * nb + b] = fl;
+            all |= fl;
+        }
+    }
+    return all;
+}
+
+void q8ref_code_fl32_array(const float *w, int64_t n, float d32, int8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = q8ref_code_fl32(w[i], d32);
+}
+
 void q8ref_matmul(const int8_t *q, const uint16_t *s_bits, int64_t N, int64_t K,
                   const uint16_t *x_bf16, int64_t ldx, int64_t M,
                   int64_t n_begin, int64_t n_end,

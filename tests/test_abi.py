@@ -125,6 +125,29 @@ def test_gemm_validation(L):
     assert g(A, A, 64, 48, A, 64, 64, A, 64, q8.Q8_GEMM_TILE_128x64, None, None) == q8.Q8_ERR_SHAPE
 
 
+def test_quantize_ex_validation(L):
+    from block_quantized_int8_gb300 import q8
+    assert L.q8_quantize_rows_ex(A, 1, 32, A, A, 2, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_quantize_rows_ex(A, 1, 32, A, A, -1, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_quantize_rows_ex(A, 1, 48, A, A, q8.Q8_QUANT_FL32, None, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_quantize_rows_ex(A + 4, 1, 32, A, A, q8.Q8_QUANT_FL32, None, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_quantize_rows_ex(A, 0, 32, A, A, q8.Q8_QUANT_FL32, None, None) == q8.Q8_OK
+
+
+def test_gguf_validation(L):
+    """Argument checks of the GGUF repack happen on the host, before any CUDA call."""
+    from block_quantized_int8_gb300 import q8
+    assert L.q8_gguf_to_planar(A, 2, 48, A, A, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_gguf_to_planar(A, -1, 64, A, A, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_gguf_to_planar(None, 2, 64, A, A, None) == q8.Q8_ERR_ARG
+    assert L.q8_gguf_to_planar(A + 2, 2, 64, A, A, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_gguf_to_planar(A, 2, 64, A + 8, A, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_gguf_to_planar(A, 0, 64, None, None, None) == q8.Q8_OK
+    assert L.q8_planar_to_gguf(A, A, 2, 64, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_planar_to_gguf(A, A, 2, 64, A + 2, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_planar_to_gguf(A, A, 2, 40, A, None) == q8.Q8_ERR_SHAPE
+
+
 def test_workspace_sizes(L):
     from block_quantized_int8_gb300 import q8
     # invalid shapes need nothing

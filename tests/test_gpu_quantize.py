@@ -90,3 +90,62 @@ def test_quantize_empty_is_noop():
     w = torch.empty((0, 64), dtype=torch.float32, device="cuda")
     q, s = q8.q8_quantize_rows(w)
     assert q.shape == (0, 64) and s.shape == (0, 2)
+
+
+# ---------------------------------------------------------------------------
+# compatibility mode: half-away rounding of the binary32 quotient w / d32
+# ---------------------------------------------------------------------------
+def gpu_quantize_fl32(w: np.ndarray):
+    from block_quantized_int8_gb300 import q8
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, s = q8.q8_quantize_rows(dev(w), dev_status=st, mode=q8.Q8_QUANT_FL32)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().view(torch.int16).numpy().view(np.uint16), int(st.item())
+
+
+def test_fl32_stress_rows_bit_exact(oracle):
+    w = synth.quant_stress_rows(32, 4096, 0)
+    q_ref, s_ref, fl = oracle.quantize_rows_fl32(w)
+    q, s, st = gpu_quantize_fl32(w)
+    assert fl == st == 0
+    assert np.array_equal(q, q_ref) and np.array_equal(s, s_ref)
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (3, 96), (257, 1536), (1000, 4096)])
+def test_fl32_random_bit_exact_and_close_to_exact_mode(oracle, rows, K):
+    w = synth.weights(rows, K, 0, f"qf{rows}.{K}")
+    q_ref, s_ref, _ = oracle.quantize_rows_fl32(w)
+    q, s, st = gpu_quantize_fl32(w)
+    assert st == 0
+    assert np.array_equal(q, q_ref) and np.array_equal(s, s_ref)
+    # same scales as the exact rule, codes at most one apart
+    q_e, s_e, _ = oracle.quantize_rows(w)
+    assert np.array_equal(s, s_e)
+    assert int(np.max(np.abs(q.astype(np.int32) - q_e.astype(np.int32)))) <= 1
+
+
+def test_fl32_exact_halves_and_flags(oracle):
+    g = synth.rng(0, "halves.fl32")
+    rows = []
+    for e in range(-14, 16):
+        for _ in range(4):
+            s = np.float32(np.ldexp(1.0 + int(g.integers(0, 1024)) / 1024.0, e))
+            if 127.0 * float(s) > 127 * 65504:
+                continue
+            rows.append(synth.exact_half_block(s, 1.0 if len(rows) % 2 else -1.0, g))
+    n = len(rows) // 8 * 8
+    w = np.stack(rows[:n]).reshape(-1, 32 * 8).copy()
+    w[0, 5] = np.nan
+    w[1, 40] = np.float32(127.0 * 65520.0)
+    q_ref, s_ref, fl = oracle.quantize_rows_fl32(w)
+    q, s, st = gpu_quantize_fl32(w)
+    assert np.array_equal(q, q_ref) and np.array_equal(s, s_ref)
+    assert st == fl == (oracle.FLAG_NONFINITE | oracle.FLAG_SCALE_OVF)
+
+
+def test_quantize_mode_argument():
+    from block_quantized_int8_gb300 import q8
+    w = torch.zeros((1, 32), dtype=torch.float32, device="cuda")
+    q = torch.empty((1, 32), dtype=torch.int8, device="cuda")
+    s = torch.empty((1, 1), dtype=torch.float16, device="cuda")
+    assert q8.lib().q8_quantize_rows_ex(q8._p(w), 1, 32, q8._p(q), q8._p(s), 2, None, None) == q8.Q8_ERR_ARG

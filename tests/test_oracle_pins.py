@@ -390,3 +390,147 @@ def test_matmul_transposition_sensitivity(oracle):
     xf[0, 0] = 1; xf[0, 33] = 5; xf[1, 63] = 7; xf[1, 0] = -1
     y, B = oracle.matmul(q, s, synth.f32_to_bf16_bits(xf))
     assert np.array_equal(y, np.array([[1.0, 20.0, 0.0], [-1.0, 0.0, -21.0]]))
+
+
+# ---------------------------------------------------------------------------
+# GGUF Q8_0 block repack
+# ---------------------------------------------------------------------------
+GGUF_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "gguf_q8_0_blocks.txt")
+
+
+def _gguf_golden():
+    blocks = []
+    for line in open(GGUF_GOLDEN):
+        line = line.split("#")[0].split()
+        if not line:
+            continue
+        assert line[0] == "block" and len(line) == 34
+        blocks.append((int(line[1], 16), [int(v) for v in line[2:]]))
+    return blocks
+
+
+def test_gguf_blocks_split_by_hand():
+    """Bytes built here by hand (scale little endian, then the codes) split
+    into the scales and codes the fixture lists."""
+    import oracle
+    blocks = _gguf_golden()
+    raw = b"".join(d.to_bytes(2, "little") + bytes(c & 0xFF for c in codes) for d, codes in blocks)
+    assert len(raw) == 34 * len(blocks)
+    q, s = oracle.gguf_to_planar(np.frombuffer(raw, dtype=np.uint8), 1, 32 * len(blocks))
+    assert s.tolist() == [[d for d, _ in blocks]]
+    assert q.reshape(-1).tolist() == [c for _, codes in blocks for c in codes]
+    # and back, byte for byte
+    assert oracle.planar_to_gguf(q, s).tobytes() == raw
+
+
+def test_gguf_round_trip_random_bytes():
+    """Any byte string of whole blocks survives split and merge, for several
+    row shapes of the same block run (the split does not depend on K)."""
+    import oracle
+    rng = np.random.default_rng(7)
+    raw = rng.integers(0, 256, size=34 * 96, dtype=np.uint8)
+    for rows, K in [(1, 3072), (3, 1024), (96, 32), (12, 256)]:
+        q, s = oracle.gguf_to_planar(raw, rows, K)
+        assert q.shape == (rows, K) and s.shape == (rows, K // 32)
+        # block g's scale is bytes 34g, 34g+1 (little endian); its codes the next 32
+        g = 37
+        assert int(s.reshape(-1)[g]) == int(raw[34 * g]) | (int(raw[34 * g + 1]) << 8)
+        assert q.reshape(-1)[32 * g:32 * g + 32].view(np.uint8).tolist() == raw[34 * g + 2:34 * g + 34].tolist()
+        assert np.array_equal(oracle.planar_to_gguf(q, s), raw)
+
+
+# ---------------------------------------------------------------------------
+# compatibility code rule: half-away rounding of the binary32 quotient w / d32
+# ---------------------------------------------------------------------------
+def _fl32_of_fraction(r):
+    """Round the rational r to the nearest binary32 value, ties to even, with
+    integer arithmetic only (an implementation independent of the oracle)."""
+    from fractions import Fraction
+    if r == 0:
+        return Fraction(0)
+    sign = -1 if r < 0 else 1
+    r = abs(r)
+    a, b = r.numerator, r.denominator
+    e = a.bit_length() - b.bit_length()
+    if (a < (b << e)) if e >= 0 else ((a << -e) < b):
+        e -= 1
+    # 2^e <= r < 2^(e+1); quantum 2^(e-23), or 2^-149 below the normal range
+    qe = max(e - 23, -149)
+    num, den = (a << -qe, b) if qe <= 0 else (a, b << qe)
+    m, rem = divmod(num, den)
+    if 2 * rem > den or (2 * rem == den and (m & 1)):
+        m += 1
+    return sign * Fraction(m) * (Fraction(2) ** qe)
+
+
+def _half_away_code(t):
+    from fractions import Fraction
+    k = int(abs(t) + Fraction(1, 2))  # floor of a non-negative rational
+    k = min(k, 127)
+    return -k if t < 0 else k
+
+
+def test_fl32_quotient_rule_by_exact_arithmetic():
+    """code_fl32 against an integer-exact re-derivation: the quotient w / d32
+    rounded to binary32 (ties to even), then half away from zero, clamped."""
+    import oracle
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    for amax in [1.0, 127.0, 0.02, 3.1, 1e-3, 7.75e-3, 250.0, 6.0e-5]:
+        d32 = np.float32(np.float32(amax) / np.float32(127.0))
+        w = (rng.uniform(-1.0, 1.0, size=4000) * amax).astype(np.float32)
+        # plus the weights just around every half-integer multiple of d32
+        halves = np.array([(k + 0.5) * float(d32) for k in range(127)], dtype=np.float32)
+        w = np.concatenate([w, halves, -halves, np.nextafter(halves, np.float32(0)),
+                            np.nextafter(halves, np.float32(np.inf)), np.float32([0.0, -0.0, amax, -amax])])
+        got = oracle.code_fl32(w, d32)
+        want = [_half_away_code(_fl32_of_fraction(Fraction(float(v)) / Fraction(float(d32)))) for v in w]
+        assert got.tolist() == want, amax
+
+
+def test_fl32_rule_on_page_values():
+    """With d32 = 1 the binary32 quotient is the weight itself, so the page's
+    rounding facts apply unchanged (0.49999997 -> 0, half away from zero)."""
+    import oracle
+    for kind, w, sbits, expected in _golden():
+        if kind == "code" and int(sbits, 16) == 0x3C00:
+            assert int(oracle.code_fl32(np.float32([float(w)]), 1.0)[0]) == int(expected), w
+
+
+def test_fl32_blocks_exact_halves_closed_form():
+    """Blocks whose maximum is 127 * 2^e: d32 = 2^e exactly, so a weight
+    (k + 1/2) 2^e has the exact quotient k + 1/2 and the code k + 1."""
+    import oracle
+    for e in [-10, -3, 0, 2]:
+        step = np.float32(2.0 ** e)
+        ks = np.arange(31, dtype=np.float32)
+        blk = np.concatenate([(ks + np.float32(0.5)) * step, [np.float32(127.0) * step]]).astype(np.float32)
+        w = np.stack([blk, -blk])
+        q, s, fl = oracle.quantize_rows_fl32(w)
+        assert fl == 0
+        want = np.concatenate([np.arange(1, 32), [127]])
+        assert q[0].tolist() == want.tolist() and q[1].tolist() == (-want).tolist()
+        assert int(s[0, 0]) == int(oracle.f32_to_f16(np.float32([step]))[0])
+
+
+def test_fl32_blocks_match_exact_arithmetic_and_flags():
+    """Whole blocks: scale as in the exact mode, codes by the exact
+    re-derivation, zero / non-finite blocks as in the exact mode."""
+    import oracle
+    from fractions import Fraction
+    w = synth.weights(6, 256, 0, "fl32.blocks")
+    w[2, 32:64] = 0.0
+    w[3, 0] = np.inf
+    w[4, 64:96] *= np.float32(1e-38)
+    q, s, fl = oracle.quantize_rows_fl32(w, with_flags=True)
+    q_e, s_e, fl_e = oracle.quantize_rows(w, with_flags=True)
+    assert np.array_equal(s, s_e) and np.array_equal(fl, fl_e)
+    for r in range(6):
+        for b in range(8):
+            blk = w[r, 32 * b:32 * b + 32]
+            if fl[r, b] or s[r, b] == 0:
+                assert not q[r, 32 * b:32 * b + 32].any()
+                continue
+            d32 = np.float32(np.max(np.abs(blk)) / np.float32(127.0))
+            want = [_half_away_code(_fl32_of_fraction(Fraction(float(v)) / Fraction(float(d32)))) for v in blk]
+            assert q[r, 32 * b:32 * b + 32].tolist() == want
