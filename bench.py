@@ -377,6 +377,15 @@ def extra_rows(torch, q8, peak):
                 t = timed(fns, reps=3)
                 rows[f"{name}_M{M}_{vn}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
                                              "us": round(t * 1e6, 2), "GMAC/s": round(M * N * K / t / 1e9, 1)}
+            # the copies as separate calls (default kernels), plain and chained:
+            # a decode step of one call per matrix, weights fixed
+            descs = [q8.make_descs([(q, s, x, y)])[0] for (q, s) in cps]
+            wsc = q8.workspace(q8.q8_linear_batch_workspace_size(descs[0], M), dev)
+            for ch, cn in ((False, "calls"), (True, "chained_calls")):
+                fns = [lambda d=d, M=M, ch=ch: q8.q8_linear_batch(descs=d, M=M, ws=wsc, chained=ch) for d in descs]
+                t = timed(fns, reps=3)
+                rows[f"{name}_M{M}_{cn}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
+                                             "us": round(t * 1e6, 2)}
             # steady state: the distinct copies as ONE batched launch (default kernels)
             nb_ = min(len(cps), q8.Q8_MAX_BATCH)
             ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(nb_)]

@@ -628,22 +628,9 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, u
     }
     p.pool_total = p.pool_off[grid];
     p.chained = chained ? 1 : 0;
-    if (chained) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = sizeof(Smem);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gemv_kernel, p) != cudaSuccess) return Q8_ERR_CUDA;
-        return Q8_OK;
-    }
-    gemv_kernel<<<grid, kThreads, sizeof(Smem), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+    if (launch_kernel(gemv_kernel, dim3(grid), dim3(kThreads), sizeof(Smem), stream, chained, p) != cudaSuccess)
+        return Q8_ERR_CUDA;
+    return Q8_OK;
 }
 
 }  // namespace q8

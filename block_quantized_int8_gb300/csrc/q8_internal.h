@@ -62,11 +62,13 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, u
 
 // 1 <= M <= 8 bulk-copy pipeline with warp MMA (q8_pipe.cu): K <= 4096.
 bool pipe_k_supported(int64_t K);
-q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
+q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
+                      bool chained = false);
 
 // 2 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256.
 bool tile_k_supported(int64_t K);
-q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream);
+q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
+                      bool chained = false);
 
 // GGUF Q8_0 block repack (q8_gguf.cu): nblocks blocks of 34 bytes (binary16
 // scale, 32 int8 codes) <-> planar codes (32 bytes per block) and scales.
@@ -81,6 +83,30 @@ bool encode_2d(CUtensorMap *map, int elem_bytes, const void *base, uint64_t inne
 // dims[i + 1], box[] the box extent per dimension.
 bool encode_tmap(CUtensorMap *map, int elem_bytes, const void *base, int rank, const uint64_t *dims,
                  const uint64_t *stride_bytes, const uint32_t *box, bool swizzle128);
+
+// kernel<<<grid, block, smem, stream>>>(p); chained: launched as a
+// programmatic dependent of the previous kernel in the stream (it may start
+// as that kernel's CTAs exit; it must wait with griddepcontrol.wait before
+// reading anything that kernel may write).
+template <typename P>
+inline cudaError_t launch_kernel(void (*kernel)(P), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 bool chained, const P &p) {
+    if (!chained) {
+        kernel<<<grid, block, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 
 q8_status launch_skinny(const q8_linear_desc *descs, int count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream,

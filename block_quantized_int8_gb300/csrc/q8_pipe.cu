@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         fence_mbar_init();
     }
     __syncthreads();
+    // a chained launch after this one may start as soon as SM slots free up
+    if (tid == 0) pdl_launch_dependents();
     if (end <= begin) return;
 
     // ---- refills ------------------------------------------------------------------
@@ -296,6 +298,9 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         const int d0 = find_pdesc(p, begin);
         for (int pi = 0; pi < min(S, nstages); ++pi) issue(pi, d0);
     }
+    // the first stages are weights only; x and y only after the kernels
+    // before this one (when launched as their dependent) have completed
+    pdl_wait_prior();
 
     // ---- consumers --------------------------------------------------------------
     int d = find_pdesc(p, begin);
@@ -541,7 +546,8 @@ bool pipe_k_supported(int64_t K) { return K <= kPipeMaxK && shape_of(static_cast
 
 namespace {
 
-q8_status launch_set(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
+q8_status launch_set(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
+                     bool chained) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (g_configured_dev != di->device) {
@@ -601,23 +607,22 @@ q8_status launch_set(const q8_linear_desc *descs, int count, int M, uint32_t *de
     }
     while (c < grid) p.cta_begin[++c] = stages;
     const size_t smem = static_cast<size_t>(p.ctl_off) + kCtlBytes;
-    if (wide_x)
-        pipe_kernel<16><<<grid, kThreads, smem, stream>>>(p);
-    else
-        pipe_kernel<12><<<grid, kThreads, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+    const cudaError_t e = wide_x ? launch_kernel(pipe_kernel<16>, dim3(grid), dim3(kThreads), smem, stream, chained, p)
+                                 : launch_kernel(pipe_kernel<12>, dim3(grid), dim3(kThreads), smem, stream, chained, p);
+    return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 
 }  // namespace
 
-q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
+q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
+                      bool chained) {
     if (M < 1 || M > 8) return Q8_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i)
         if (!pipe_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
     // every mix of K <= 4096 fits one ring (the largest half-tile stage
     // with a full tile's reduction entries still leaves two slots), so the
     // launch never depends on which matrices share it
-    return launch_set(descs, count, M, dev_status, stream);
+    return launch_set(descs, count, M, dev_status, stream, chained);
 }
 
 }  // namespace q8

@@ -302,6 +302,10 @@ skinny_kernel(const __grid_constant__ BatchParams p) {
         fence_mbar_init();
     }
     __syncthreads();
+    // chained launches: let the next kernel start early, and wait for the
+    // previous one before reading x or the workspace
+    if (tid == 0) pdl_launch_dependents();
+    pdl_wait_prior();
 
     int item = blockIdx.x;
     if (item >= p.total_items) return;
@@ -330,7 +334,7 @@ skinny_kernel(const __grid_constant__ BatchParams p) {
 }
 
 template <int MT, int VAR>
-q8_status run(const BatchParams &p, const DeviceInfo *di, cudaStream_t stream) {
+q8_status run(const BatchParams &p, const DeviceInfo *di, cudaStream_t stream, bool chained) {
     using C = Cfg<MT, VAR>;
     static int configured_dev = -1;
     static int occ = 0;
@@ -344,8 +348,10 @@ q8_status run(const BatchParams &p, const DeviceInfo *di, cudaStream_t stream) {
         configured_dev = di->device;
     }
     const int grid = std::min(p.total_items, di->sm_count * occ);
-    skinny_kernel<MT, VAR><<<grid, kSkinnyThreads, C::SMEM, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+    return launch_kernel(skinny_kernel<MT, VAR>, dim3(grid), dim3(kSkinnyThreads), C::SMEM, stream, chained, p) ==
+                   cudaSuccess
+               ? Q8_OK
+               : Q8_ERR_CUDA;
 }
 
 }  // namespace
@@ -444,11 +450,11 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
         if (st != Q8_OK) return st;
     }
     if (n[kRoutePipe] > 0) {
-        const q8_status st = launch_pipe(part[kRoutePipe], n[kRoutePipe], M, dev_status, stream);
+        const q8_status st = launch_pipe(part[kRoutePipe], n[kRoutePipe], M, dev_status, stream, chained);
         if (st != Q8_OK) return st;
     }
     if (n[kRouteTile] > 0) {
-        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, dev_status, stream);
+        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, dev_status, stream, chained);
         if (st != Q8_OK) return st;
     }
     if (count == 0) return Q8_OK;
@@ -488,16 +494,16 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     if (variant == Q8_VARIANT_AUTO) variant = (M == 1) ? Q8_VARIANT_SIMT : Q8_VARIANT_MMA;
 
     if (variant == Q8_VARIANT_MMA) {
-        if (M <= 8) return run<8, Q8_VARIANT_MMA>(p, di, stream);
-        if (M <= 16) return run<16, Q8_VARIANT_MMA>(p, di, stream);
-        return run<32, Q8_VARIANT_MMA>(p, di, stream);
+        if (M <= 8) return run<8, Q8_VARIANT_MMA>(p, di, stream, chained);
+        if (M <= 16) return run<16, Q8_VARIANT_MMA>(p, di, stream, chained);
+        return run<32, Q8_VARIANT_MMA>(p, di, stream, chained);
     }
-    if (M <= 1) return run<1, Q8_VARIANT_SIMT>(p, di, stream);
-    if (M <= 2) return run<2, Q8_VARIANT_SIMT>(p, di, stream);
-    if (M <= 4) return run<4, Q8_VARIANT_SIMT>(p, di, stream);
-    if (M <= 8) return run<8, Q8_VARIANT_SIMT>(p, di, stream);
-    if (M <= 16) return run<16, Q8_VARIANT_SIMT>(p, di, stream);
-    return run<32, Q8_VARIANT_SIMT>(p, di, stream);
+    if (M <= 1) return run<1, Q8_VARIANT_SIMT>(p, di, stream, chained);
+    if (M <= 2) return run<2, Q8_VARIANT_SIMT>(p, di, stream, chained);
+    if (M <= 4) return run<4, Q8_VARIANT_SIMT>(p, di, stream, chained);
+    if (M <= 8) return run<8, Q8_VARIANT_SIMT>(p, di, stream, chained);
+    if (M <= 16) return run<16, Q8_VARIANT_SIMT>(p, di, stream, chained);
+    return run<32, Q8_VARIANT_SIMT>(p, di, stream, chained);
 }
 
 }  // namespace q8

@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         fence_mbar_init();
     }
     __syncthreads();
+    // a chained launch after this one may start as soon as SM slots free up
+    if (tid == 0) pdl_launch_dependents();
     if (ie <= ib) return;
 
     // total stages of this CTA
@@ -212,7 +214,13 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         }
     }
 
-    auto issue = [&](int k, Pos pos) {
+    // stage k at position pos: all bytes announced on the slot's barrier,
+    // then the weight boxes and (unless deferred) the x box
+    auto issue_x = [&](int k, Pos pos) {
+        const int slot = k % kSlots;
+        tma_3d(base + slot * kStage + kCodeBytes, &p.m[pos.d].x, 0, 0, 4 * pos.chunk, &full[slot]);
+    };
+    auto issue = [&](int k, Pos pos, bool with_x) {
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
         const TMaps &T = p.m[pos.d];
@@ -220,14 +228,24 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const int row0 = (pos.item - D.item_begin) * D.R;
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + (MP * 512 << D.lgS) + kScaleBytes));
         tma_3d(st, &T.q, 0, row0, 2 * pos.chunk, &full[slot]);
-        tma_3d(st + kCodeBytes, &T.x, 0, 0, 4 * pos.chunk, &full[slot]);
         tma_2d(st + kCodeBytes + kXBytes, &T.s, 8 * pos.chunk, row0, &full[slot]);
+        if (with_x) issue_x(k, pos);
     };
     Pos pos{find_tdesc(p, ib), ib, 0};
+    // the first stages' weights go out at once; their x only after the
+    // kernels before this one (when launched as their dependent) completed
     if (tid == 0) {
         Pos q = pos;
         for (int k = 0; k < min(kSlots, nstages); ++k) {
-            issue(k, q);
+            issue(k, q, false);
+            q.next(p);
+        }
+    }
+    pdl_wait_prior();
+    if (tid == 0) {
+        Pos q = pos;
+        for (int k = 0; k < min(kSlots, nstages); ++k) {
+            issue_x(k, q);
             q.next(p);
         }
     }
@@ -355,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
                 if (k + kSlots < nstages) {
                     Pos q = pos;
                     for (int s2 = 0; s2 < kSlots; ++s2) q.next(p);
-                    issue(k + kSlots, q);
+                    issue(k + kSlots, q, true);
                 }
             }
         }
@@ -379,7 +397,7 @@ bool configure(int &occ) {
 }
 
 template <int MT>
-q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, cudaStream_t stream) {
+q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, cudaStream_t stream, bool chained) {
     const int grid = std::min(std::min(items, di->sm_count * g_occ), kMaxGrid);
     // cut the item list into `grid` ranges of (nearly) equal bytes
     int c = 0;
@@ -394,8 +412,10 @@ q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, c
         }
     }
     while (c < grid) p.cta_begin[++c] = items;
-    tile_kernel<MT><<<grid, kThreads, smem_bytes<MT>(), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
+    return launch_kernel(tile_kernel<MT>, dim3(grid), dim3(kThreads), smem_bytes<MT>(), stream, chained, p) ==
+                   cudaSuccess
+               ? Q8_OK
+               : Q8_ERR_CUDA;
 }
 
 // Chunks per stage of a matrix with KC chunks in a launch that asks for S:
@@ -413,7 +433,8 @@ int log2_of(int S) { return S >= 4 ? 2 : (S >= 2 ? 1 : 0); }
 
 bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
 
-q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream) {
+q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
+                      bool chained) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (M < 2 || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
@@ -478,8 +499,9 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
     p.count = count;
     p.M = M;
     if (items == 0) return Q8_OK;
-    if (MT == 1) return run<1>(p, di, items, total_bytes, stream);
-    return MT == 2 ? run<2>(p, di, items, total_bytes, stream) : run<4>(p, di, items, total_bytes, stream);
+    if (MT == 1) return run<1>(p, di, items, total_bytes, stream, chained);
+    return MT == 2 ? run<2>(p, di, items, total_bytes, stream, chained)
+                   : run<4>(p, di, items, total_bytes, stream, chained);
 }
 
 }  // namespace q8

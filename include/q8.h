@@ -201,8 +201,10 @@ q8_status q8_linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M,
  * stages of weights (q, s) before that kernel completes, and x, y and ws only
  * after it has completed and its writes are visible.  So the previous work
  * may produce x, but must not write any q or s of this call.  Same results,
- * bit for bit, as q8_linear_batch.  M = 1 matrices served by the GEMV start
- * early; other kernels run as in q8_linear_batch.
+ * bit for bit, as q8_linear_batch.  Every kernel family of the call is
+ * launched this way; the bulk-copy kernels (M <= 8 GEMV and pipeline) and the
+ * TMA tile kernel issue their first weight stages before the wait, the
+ * general kernel waits first.
  */
 q8_status q8_linear_batch_chained(const q8_linear_desc *descs, int32_t count, int32_t M,
                                   void *ws, size_t ws_bytes,

@@ -269,13 +269,14 @@ def test_gemv_pool_counter_returns_to_zero(oracle):
         check_tol(y.cpu().numpy(), y_ref, B, "pooled GEMV")
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 12, 24])
 def test_chained_calls_match_plain_calls(oracle, M):
     """q8_linear_batch_chained over a stream of passes (new x each pass, one
     workspace, weights fixed) gives the same bits as q8_linear_batch, also in
-    a CUDA graph, and leaves the M = 1 pool counter zero."""
+    a CUDA graph, and leaves the M = 1 pool counter zero.  The shapes reach
+    every kernel family (GEMV, pipeline, tiles, general)."""
     from block_quantized_int8_gb300 import q8
-    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096)]
+    shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (300, 2080)]
     w = []
     for i, (N, K) in enumerate(shapes):
         qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"ch{i}"))
