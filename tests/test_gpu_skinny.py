@@ -179,6 +179,38 @@ def test_layer_set_batch_sampled(oracle):
         check_tol(y.cpu().numpy()[:, rows], y_ref, B, "layer set")
 
 
+def test_layer_set_bench_step_sampled(oracle):
+    """The benchmark's own step: the layer set built by bench.py, 8 passes
+    launched with q8_linear_batch_chained as it times them, twice in a row on
+    one workspace; sampled outputs of every pass and matrix against the
+    oracle, and the second step bit-identical to the first."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from block_quantized_int8_gb300 import q8
+    ls = bench.LayerSet(torch, q8)
+    ls.y_all.fill_(float("nan"))
+    ls.step(chained=True)
+    torch.cuda.synchronize()
+    first = ls.y_all.clone()
+    ls.y_all.fill_(float("nan"))
+    ls.step(chained=True)
+    torch.cuda.synchronize()
+    assert torch.equal(ls.y_all, first)
+    assert int(ls.ws.view(-1)[-256:].count_nonzero()) == 0
+    for layer in range(synth.LAYERS):
+        for (name, K, N) in synth.LAYER_MATRICES:
+            w = synth.weights(N, K, 0, synth.layer_weight_tag(layer, name))
+            rows = np.unique(np.concatenate([synth.rng(layer, "step." + name).choice(N, 16, replace=False),
+                                             [0, N - 1]]))
+            qn, sn, _ = oracle.quantize_rows(w[rows])
+            for p in (0, synth.PASSES - 1, layer % synth.PASSES):
+                y_ref, B = oracle.matmul(qn, sn, ls.x_host[(p, K)])
+                y = ls.y[p][layer][name].cpu().numpy()[:, rows]
+                check_tol(y, y_ref, B, f"bench step pass {p} layer {layer} {name}")
+
+
 # ---------------------------------------------------------------------------
 # determinism, graph replay, batch == separate calls
 # ---------------------------------------------------------------------------
