@@ -630,6 +630,21 @@ def main():
     e2e, h2d, d2h = e2e_gbs(torch, ls, max(20, min(200, args.steps // 10)), bytes_step, chained)
 
     rows = {} if (args.no_rows or rank != 0) else extra_rows(torch, q8, peak)
+    if rows:
+        # the same step, plain and chained, captured once into a CUDA graph
+        for ch, cn in ((False, "plain"), (True, "chained")):
+            g = torch.cuda.CUDAGraph()
+            s_ = torch.cuda.Stream()
+            with torch.cuda.stream(s_):
+                ls.step(chained=ch)
+            s_.synchronize()
+            with torch.cuda.graph(g, stream=s_):
+                ls.step(chained=ch)
+            dtg = time_steps(torch, g.replay, 200, 5)
+            rows[f"layer_set_step_graph_{cn}"] = {"GB/s": round(bytes_step * 200 / dtg / 1e9, 1),
+                                                 "frac": round(bytes_step * 200 / dtg / 1e9 / peak, 3),
+                                                 "us_per_step": round(dtg / 200 * 1e6, 2)}
+            del g
 
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -90,6 +90,7 @@ struct GParams {
     int32_t grid;
     int32_t pool_total;     // stages in the pool
     int32_t chained;        // launched as a programmatic dependent: weights may be read early
+    int32_t early_signal;   // the grid fills every CTA slot: signal dependents at start
     int32_t cta_begin[kMaxGrid + 1];  // CTA c's balanced range [cta_begin[c], cta_begin[c+1])
     int32_t cta_split[kMaxGrid];      // it owns [cta_begin[c], cta_split[c]); the rest is pooled
     int32_t pool_off[kMaxGrid + 1];   // pool index of the first pooled stage of CTA c's range
@@ -389,6 +390,9 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
                     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];"
                                  :: "r"(smem_addr(&sm.named[slot])) : "memory");
                     prod_ok = false;
+                    // nothing left to issue: a chained launch after this one
+                    // may start once every CTA is this far
+                    if (!p.early_signal) pdl_launch_dependents();
                     return;
                 }
                 i = pool_stage(p, static_cast<int>(j));
@@ -544,8 +548,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
     for (int i = tid; i < 2 * kStages * kRedRows; i += kThreads) (&sm.cnt[0][0])[i] = 0u;
     __syncthreads();
-    // a chained launch after this one may start as soon as SM slots free up
-    if (tid == 0) pdl_launch_dependents();
+    // A grid that fills every CTA slot lets a chained launch after it start
+    // at once: its CTAs can only take the slots ours free as they exit.  A
+    // smaller grid signals late (else chained calls would start one after
+    // another and crowd the GPU with waiting CTAs).
+    if (p.early_signal && tid == 0) pdl_launch_dependents();
     cta_work<kJMax>(p, sm, begin, split, warp, lane);
 }
 
@@ -628,6 +635,7 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, u
     }
     p.pool_total = p.pool_off[grid];
     p.chained = chained ? 1 : 0;
+    p.early_signal = grid >= di->sm_count * g_occ ? 1 : 0;
     if (launch_kernel(gemv_kernel, dim3(grid), dim3(kThreads), sizeof(Smem), stream, chained, p) != cudaSuccess)
         return Q8_ERR_CUDA;
     return Q8_OK;

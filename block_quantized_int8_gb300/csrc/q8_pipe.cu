@@ -97,6 +97,7 @@ struct PParams {
     int32_t red_off;     // partial tiles: S entries of red_entry bytes
     int32_t red_entry;   // 8 warps x 32 lanes x (float4 full tiles, float2 half tiles)
     int32_t ctl_off;     // counters [kMaxSlots][8], release counts [kMaxSlots], then full[kMaxSlots]
+    int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
     int32_t cta_begin[kMaxGrid + 1];
 };
 
@@ -258,8 +259,9 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         fence_mbar_init();
     }
     __syncthreads();
-    // a chained launch after this one may start as soon as SM slots free up
-    if (tid == 0) pdl_launch_dependents();
+    // a grid that fills every CTA slot signals a chained launch after it at
+    // once (its CTAs can only take the slots ours free); a smaller one late
+    if (p.early_signal && tid == 0) pdl_launch_dependents();
     if (end <= begin) return;
 
     // ---- refills ------------------------------------------------------------------
@@ -309,6 +311,9 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
     int kb0 = 0, nblk = 0;
     uint32_t slow = 0u;    // blocks that take the exact bf16 path
     for (int i = begin, k = 0; i < end; ++i, ++k) {
+        // every stage of this CTA is issued: a chained launch after this one
+        // may start once all CTAs are this far
+        if (!p.early_signal && k == max(0, nstages - S) && tid == 0) pdl_launch_dependents();
         while (i >= p.d[d].stage_begin + p.d[d].stages) ++d;
         const PDesc &D = p.d[d];
         const int lp = D.lp;
@@ -607,6 +612,7 @@ q8_status launch_set(const q8_linear_desc *descs, int count, int M, uint32_t *de
     }
     while (c < grid) p.cta_begin[++c] = stages;
     const size_t smem = static_cast<size_t>(p.ctl_off) + kCtlBytes;
+    p.early_signal = grid >= di->sm_count * g_occ ? 1 : 0;
     const cudaError_t e = wide_x ? launch_kernel(pipe_kernel<16>, dim3(grid), dim3(kThreads), smem, stream, chained, p)
                                  : launch_kernel(pipe_kernel<12>, dim3(grid), dim3(kThreads), smem, stream, chained, p);
     return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;

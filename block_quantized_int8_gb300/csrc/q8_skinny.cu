@@ -302,9 +302,8 @@ skinny_kernel(const __grid_constant__ BatchParams p) {
         fence_mbar_init();
     }
     __syncthreads();
-    // chained launches: let the next kernel start early, and wait for the
-    // previous one before reading x or the workspace
-    if (tid == 0) pdl_launch_dependents();
+    // chained launches: wait for the previous kernel before reading x or the
+    // workspace (a chained launch after this one starts when this one ends)
     pdl_wait_prior();
 
     int item = blockIdx.x;

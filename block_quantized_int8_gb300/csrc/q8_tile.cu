@@ -79,6 +79,7 @@ struct TParams {
     uint32_t *status;
     int32_t count;
     int32_t M;
+    int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
     int32_t cta_begin[kMaxGrid + 1];
 };
 static_assert(sizeof(TParams) <= 32764, "kernel parameters exceed the 32764-byte limit");
@@ -200,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         fence_mbar_init();
     }
     __syncthreads();
-    // a chained launch after this one may start as soon as SM slots free up
-    if (tid == 0) pdl_launch_dependents();
+    // a grid that fills every CTA slot signals a chained launch after it at
+    // once (its CTAs can only take the slots ours free); a smaller one late
+    if (p.early_signal && tid == 0) pdl_launch_dependents();
     if (ie <= ib) return;
 
     // total stages of this CTA
@@ -265,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         for (int j = 0; j < MT; ++j) acc[c][j][0] = acc[c][j][1] = acc[c][j][2] = acc[c][j][3] = 0.f;
 
     for (int k = 0; k < nstages; ++k) {
+        // every stage of this CTA is issued: a chained launch after this one
+        // may start once all CTAs are this far
+        if (!p.early_signal && k == max(0, nstages - kSlots) && tid == 0) pdl_launch_dependents();
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
         const int lgS = C == 1 ? 0 : D.lgS;  // C == 1: never split
@@ -412,6 +417,7 @@ q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, c
         }
     }
     while (c < grid) p.cta_begin[++c] = items;
+    p.early_signal = grid >= di->sm_count * g_occ ? 1 : 0;
     return launch_kernel(tile_kernel<MT>, dim3(grid), dim3(kThreads), smem_bytes<MT>(), stream, chained, p) ==
                    cudaSuccess
                ? Q8_OK
