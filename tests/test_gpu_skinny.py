@@ -179,6 +179,27 @@ def test_layer_set_batch_sampled(oracle):
         check_tol(y.cpu().numpy()[:, rows], y_ref, B, "layer set")
 
 
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_chained_calls_keep_write_order(oracle, M):
+    """Chained calls that write the same outputs from different activations,
+    back to back: the last call's values must be what remains (a dependent
+    launch writes y only after the calls before it have completed)."""
+    from block_quantized_int8_gb300 import q8
+    N, K = 1536, 4096
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, "wo"))
+    q, s = weights_dev(qn, sn)
+    xs = [x_dev(synth.activations(M, K, 0, f"wox{i}")) for i in range(5)]
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = q8.workspace(q8.q8_linear_batch_workspace_size(q8.make_descs([(q, s, xs[0], y)])[0], M))
+    want = torch.empty_like(y)
+    q8.q8_linear_batch([(q, s, xs[-1], want)], ws=ws)
+    for rep in range(3):
+        for x in xs:
+            q8.q8_linear_batch([(q, s, x, y)], ws=ws, chained=True)
+        torch.cuda.synchronize()
+        assert torch.equal(y, want)
+
+
 def test_layer_set_bench_step_sampled(oracle):
     """The benchmark's own step: the layer set built by bench.py, 8 passes
     launched with q8_linear_batch_chained as it times them, twice in a row on
