@@ -257,38 +257,64 @@ def per_launch_ms(torch, ls, reps, variant=0):
 
 
 def e2e_gbs(torch, ls, steps, bytes_per_step, chained=False):
-    """Whole step through the public API with host buffers: one pinned H2D copy
-    of every pass's activations, the 8 batch launches, a D2H copy of each
-    pass's outputs (issued on a second stream as soon as that pass is done, so
-    it overlaps the next pass), and a host-side wait for the result, timed by
-    the host clock."""
+    """Whole step through the public API with host buffers, timed by the host
+    clock: every step copies all passes' activations from pinned host memory
+    (one H2D copy), runs the 8 batch launches, copies each pass's outputs to
+    pinned host memory (on a second stream, as soon as that pass is done, so
+    it overlaps the next pass) and the host reads the step's result.  Two
+    host output buffers alternate, so step i + 1 is queued before the host
+    waits for step i's result (the GPU does not idle while the host reads);
+    the loop ends only after the last step's result has been read.  The
+    device outputs alternate as well (a second set of descriptors), so a
+    step's kernels never overwrite outputs still being copied out."""
     xh = torch.from_numpy(np.concatenate([ls.x_host[k].reshape(-1) for k in ls.x_keys]).view(np.int16)).pin_memory()
-    yh = torch.empty(ls.y_all.shape, dtype=ls.y_all.dtype, pin_memory=True)
+    yh = [torch.empty(ls.y_all.shape, dtype=ls.y_all.dtype, pin_memory=True) for _ in range(2)]
+    y_dev = [ls.y_all, torch.empty_like(ls.y_all)]
+    delta = y_dev[1].data_ptr() - y_dev[0].data_ptr()
+
+    def shifted(d):
+        arr = (ls.q8.LinearDesc * len(d))()
+        for k in range(len(d)):
+            arr[k] = ls.q8.LinearDesc(d[k].q, d[k].s, d[k].x, d[k].y + delta, d[k].N, d[k].K, d[k].ldx, d[k].ldy)
+        return arr
+    descs = [ls.descs, [shifted(d) for d in ls.descs]]
     h2d = xh.numel() * 2
-    d2h = yh.numel() * 4
+    d2h = yh[0].numel() * 4
     per_pass = ls.y_all.numel() // synth.PASSES
     copy_stream = torch.cuda.Stream()
     done = [torch.cuda.Event() for _ in range(synth.PASSES)]
+    step_done = [torch.cuda.Event() for _ in range(2)]
+    checksum = [0.0]
 
-    def one():
+    def issue(i):
         cs = torch.cuda.current_stream()
+        out, ydev, dsc = yh[i % 2], y_dev[i % 2], descs[i % 2]
         ls.x_all.view(torch.int16).copy_(xh, non_blocking=True)
         for p in range(synth.PASSES):
-            ls.q8.q8_linear_batch(descs=ls.descs[p], M=1, ws=ls.ws, chained=chained)
+            ls.q8.q8_linear_batch(descs=dsc[p], M=1, ws=ls.ws, chained=chained)
             done[p].record(cs)
             copy_stream.wait_event(done[p])
             with torch.cuda.stream(copy_stream):
-                yh[p * per_pass:(p + 1) * per_pass].copy_(ls.y_all[p * per_pass:(p + 1) * per_pass],
-                                                          non_blocking=True)
-        copy_stream.synchronize()
-        cs.synchronize()
+                out[p * per_pass:(p + 1) * per_pass].copy_(ydev[p * per_pass:(p + 1) * per_pass], non_blocking=True)
+        step_done[i % 2].record(copy_stream)
 
-    for _ in range(3):
-        one()
+    def read(i):
+        step_done[i % 2].synchronize()
+        checksum[0] += float(yh[i % 2][0])  # the host touches the result
+
+    def run(n):
+        issue(0)
+        for i in range(1, n):
+            issue(i)
+            read(i - 1)
+        read(n - 1)
+
+    run(3)
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    run(steps)
     dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
     return bytes_per_step * steps / dt / 1e9, h2d, d2h
 
 
