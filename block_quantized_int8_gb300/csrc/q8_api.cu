@@ -127,6 +127,17 @@ q8_status q8_planar_to_gguf(const int8_t *q, const uint16_t *s, int64_t rows, in
     return launch_gguf_export(q, s, rows * (K / 32), blocks, reinterpret_cast<cudaStream_t>(stream));
 }
 
+q8_status q8_selftest_wait_timeout(uint64_t limit_ns, uint32_t *dev_status, uint64_t *dev_elapsed_ns,
+                                   q8_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return Q8_ERR_ARG;
+    if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
+    if (dev_elapsed_ns && !aligned(dev_elapsed_ns, 8)) return Q8_ERR_ALIGN;
+    const DeviceInfo *di;
+    q8_status st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_selftest_wait_timeout(limit_ns, dev_status, dev_elapsed_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {
     if (N <= 0 || K <= 0 || (K % 32) != 0 || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
     q8_linear_desc d{};

@@ -80,13 +80,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
-// Wait for phase `parity` of `bar` to complete; false if kWaitLimitNs passed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// After giving up on a wait: keep this thread -- so its CTA and the CTA's
+// shared memory -- alive for a bounded time, so that bulk copies already
+// issued into that shared memory land before it is released.
+constexpr uint64_t kDrainNs = 2ull * 1000ull * 1000ull;  // 2 ms
+__device__ __forceinline__ void drain_after_timeout() {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kDrainNs) __nanosleep(1000);
+}
+
+// Wait for phase `parity` of `bar` to complete; false if limit_ns passed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 // Programmatic dependent launch: let the next kernel in the stream start

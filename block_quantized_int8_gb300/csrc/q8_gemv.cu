@@ -481,6 +481,7 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
             load_x(p.d[d]);
             if (!mbar_wait_bounded(&sm.full[slot], (k / kStages) & 1)) {
                 if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+                drain_after_timeout();
                 return;
             }
         } else {
@@ -489,6 +490,7 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
             const int kp = k - nown;  // pool positions before this one
             if (!mbar_wait_bounded(&sm.named[slot], (kp / kStages) & 1)) {
                 if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+                drain_after_timeout();
                 return;
             }
             i = *reinterpret_cast<volatile const int32_t *>(&sm.sidx[slot]);
@@ -497,6 +499,7 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
             load_x(p.d[d]);
             if (!mbar_wait_bounded(&sm.full[slot], (k / kStages) & 1)) {
                 if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+                drain_after_timeout();
                 return;
             }
         }

@@ -75,6 +75,10 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
 q8_status launch_gguf_ingest(const void *blocks, int64_t nblocks, int8_t *q, uint16_t *s, cudaStream_t stream);
 q8_status launch_gguf_export(const int8_t *q, const uint16_t *s, int64_t nblocks, void *blocks, cudaStream_t stream);
 
+// Bounded wait on an mbarrier nothing arrives on (q8_selftest.cu).
+q8_status launch_selftest_wait_timeout(uint64_t limit_ns, uint32_t *status, uint64_t *elapsed_ns,
+                                       cudaStream_t stream);
+
 // 2-D TMA tensor map over a row-major [outer][inner] array of 1- or 2-byte
 // elements (q8_tmap.cu; cached by parameters).  false if encoding fails.
 bool encode_2d(CUtensorMap *map, int elem_bytes, const void *base, uint64_t inner, uint64_t outer,

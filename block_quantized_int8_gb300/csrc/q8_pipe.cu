@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) pipe_kernel(const __grid_constant
         const int slot = k % S;
         if (!mbar_wait_bounded(&full[slot], (k / S) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+            drain_after_timeout();
             return;
         }
         const uint8_t *codes = smem_raw + static_cast<size_t>(slot) * p.slot_bytes;

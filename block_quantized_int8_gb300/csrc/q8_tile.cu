@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const int cls = (pos.chunk + ks) & (C - 1);
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+            drain_after_timeout();
             return;
         }
         {

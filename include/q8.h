@@ -90,6 +90,17 @@ q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K,
                            int8_t *q, uint16_t *s,
                            uint32_t *dev_status, q8_stream_t stream);
 
+/*
+ * q8_selftest_wait_timeout -- exercise the kernels' failure path without a
+ * fault: one thread waits, with the same bounded mbarrier wait the kernels
+ * use, on a barrier that nothing ever arrives on, gives up after limit_ns
+ * (1 .. 1e9), ORs Q8_DEV_TIMEOUT into *dev_status and writes the time it
+ * waited (ns) to *dev_elapsed_ns (both device pointers, nullable).  The
+ * context stays usable.  Q8_ERR_ARG for a limit out of range.
+ */
+q8_status q8_selftest_wait_timeout(uint64_t limit_ns, uint32_t *dev_status, uint64_t *dev_elapsed_ns,
+                                   q8_stream_t stream);
+
 /* Code rules of q8_quantize_rows_ex. */
 #define Q8_QUANT_EXACT 0  /* as q8_quantize_rows: exact quotient by the stored binary16 scale */
 #define Q8_QUANT_FL32 1   /* compatibility: binary32 quotient w / d (d = amax/127 in binary32) */

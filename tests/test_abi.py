@@ -134,6 +134,14 @@ def test_quantize_ex_validation(L):
     assert L.q8_quantize_rows_ex(A, 0, 32, A, A, q8.Q8_QUANT_FL32, None, None) == q8.Q8_OK
 
 
+def test_selftest_validation(L):
+    from block_quantized_int8_gb300 import q8
+    assert L.q8_selftest_wait_timeout(0, None, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_selftest_wait_timeout(2_000_000_000, None, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_selftest_wait_timeout(1000, A + 2, None, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_selftest_wait_timeout(1000, None, A + 4, None) == q8.Q8_ERR_ALIGN
+
+
 def test_gguf_validation(L):
     """Argument checks of the GGUF repack happen on the host, before any CUDA call."""
     from block_quantized_int8_gb300 import q8
