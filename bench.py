@@ -222,6 +222,22 @@ class LayerSet:
         return True
 
 
+def max_over_ranks(torch, dist, seconds, device):
+    """The slowest rank's time (every rank gets it); seconds alone without a
+    process group."""
+    if dist is None:
+        return seconds
+    t = torch.tensor([seconds], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step, steps, t_max, world):
+    """Whole-job throughput: every rank moved bytes_per_step per step; the job
+    took the slowest rank's time."""
+    return world * bytes_per_step * steps / t_max / 1e9
+
+
 def time_steps(torch, fn, steps, warmup):
     for _ in range(warmup):
         fn()
@@ -641,12 +657,8 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks = clk.stop()
-    t_max = dt
-    if dist:
-        t = torch.tensor([dt], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    value = world * bytes_step * args.steps / t_max / 1e9
+    t_max = max_over_ranks(torch, dist, dt, "cuda")
+    value = whole_job_gbs(bytes_step, args.steps, t_max, world)
 
     # kernel duration, live, on the launching stream
     launch_ms = per_launch_ms(torch, ls, reps=20, variant=args.variant)
