@@ -18,6 +18,7 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -236,6 +237,35 @@ def whole_job_gbs(bytes_per_step, steps, t_max, world):
     """Whole-job throughput: every rank moved bytes_per_step per step; the job
     took the slowest rank's time."""
     return world * bytes_per_step * steps / t_max / 1e9
+
+
+def ceilings(torch, q8, nbytes=2 << 30, reps=5):
+    """The two references of the "Frigg" README's "The machine": a device-to-
+    device copy (cudaMemcpyAsync; read + write bytes) and a streaming read
+    (q8_stream_read), GB/s, measured in this run."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    words = q8.lib().q8_stream_read_out_words()
+    out = torch.zeros(max(int(words), 1), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def t_of(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    t_copy = t_of(lambda: dst.copy_(src))
+    t_read = t_of(lambda: q8.lib().q8_stream_read(src.data_ptr(), nbytes, out.data_ptr(),
+                                                  ctypes.c_void_p(stream.cuda_stream)))
+    del src, dst
+    return 2 * nbytes / t_copy / 1e9, nbytes / t_read / 1e9
 
 
 def time_steps(torch, fn, steps, warmup):
@@ -666,6 +696,7 @@ def main():
     traffic, _ = profile_traffic()
 
     e2e, h2d, d2h = e2e_gbs(torch, ls, max(20, min(200, args.steps // 10)), bytes_step, chained)
+    c_copy, c_read = ceilings(torch, q8)
 
     rows = {} if (args.no_rows or rank != 0) else extra_rows(torch, q8, peak)
     if rows:
@@ -708,6 +739,11 @@ def main():
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                          else "fallback 6.8 TB/s", "kernel": "gemv_kernel (q8_linear_batch, M=1, one pass of 64 matrices)",
                          "launch_us": round(launch_ms * 1e3, 2), "bytes_per_launch": bytes_pass},
+            "ceilings": {"d2d_copy_gbs": round(c_copy, 1), "stream_read_gbs": round(c_read, 1),
+                         "step_frac_of_copy": round(value / world / c_copy, 4),
+                         "step_frac_of_read": round(value / world / c_read, 4),
+                         "launch_frac_of_read": round(achieved / c_read, 4),
+                         "note": "measured in this run: cudaMemcpyAsync D2D (read+write bytes) and q8_stream_read"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": ls.launches_per_step * args.steps,

@@ -138,6 +138,21 @@ q8_status q8_selftest_wait_timeout(uint64_t limit_ns, uint32_t *dev_status, uint
     return launch_selftest_wait_timeout(limit_ns, dev_status, dev_elapsed_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t q8_stream_read_out_words(void) {
+    const DeviceInfo *di = device_info();
+    return di ? static_cast<size_t>(stream_read_grid(di)) : 0;
+}
+
+q8_status q8_stream_read(const void *src, size_t bytes, uint32_t *out, q8_stream_t stream) {
+    if (bytes == 0) return Q8_OK;
+    if (!src || !out) return Q8_ERR_ARG;
+    if (!aligned(src, 16) || (bytes % 16) != 0 || !aligned(out, 4)) return Q8_ERR_ALIGN;
+    const DeviceInfo *di;
+    q8_status st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_stream_read(src, bytes, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {
     if (N <= 0 || K <= 0 || (K % 32) != 0 || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
     q8_linear_desc d{};

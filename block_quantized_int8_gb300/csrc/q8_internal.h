@@ -75,6 +75,12 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
 q8_status launch_gguf_ingest(const void *blocks, int64_t nblocks, int8_t *q, uint16_t *s, cudaStream_t stream);
 q8_status launch_gguf_export(const int8_t *q, const uint16_t *s, int64_t nblocks, void *blocks, cudaStream_t stream);
 
+// Streaming-read ceiling (q8_probe.cu): reads bytes (a multiple of 16) from a
+// 16-byte aligned buffer; each CTA XORs what it read into out[blockIdx.x]
+// (out holds stream_read_grid() words).
+int stream_read_grid(const DeviceInfo *di);
+q8_status launch_stream_read(const void *src, size_t bytes, uint32_t *out, cudaStream_t stream);
+
 // Bounded wait on an mbarrier nothing arrives on (q8_selftest.cu).
 q8_status launch_selftest_wait_timeout(uint64_t limit_ns, uint32_t *status, uint64_t *elapsed_ns,
                                        cudaStream_t stream);

@@ -36,7 +36,8 @@ Q8_QUANT_EXACT, Q8_QUANT_FL32 = 0, 1
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
            "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
            "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex", "q8_gguf_to_planar",
-           "q8_planar_to_gguf", "q8_quantize_rows_ex", "q8_selftest_wait_timeout")
+           "q8_planar_to_gguf", "q8_quantize_rows_ex", "q8_selftest_wait_timeout",
+           "q8_stream_read", "q8_stream_read_out_words")
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -81,6 +82,9 @@ def lib():
         L.q8_planar_to_gguf.argtypes = [P, P, I64, I64, P, P]
         L.q8_selftest_wait_timeout.argtypes = [ctypes.c_uint64, U32P, P, P]
         L.q8_selftest_wait_timeout.restype = ctypes.c_int
+        L.q8_stream_read.argtypes = [P, SZ, P, P]
+        L.q8_stream_read.restype = ctypes.c_int
+        L.q8_stream_read_out_words.restype = SZ
         L.q8_status_str.argtypes = [ctypes.c_int]
         L.q8_status_str.restype = ctypes.c_char_p
         L.q8_abi_version.restype = I32

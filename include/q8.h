@@ -91,6 +91,17 @@ q8_status q8_quantize_rows(const float *w, int64_t rows, int64_t K,
                            uint32_t *dev_status, q8_stream_t stream);
 
 /*
+ * q8_stream_read -- the streaming-read ceiling the decode kernels are
+ * measured against ("Frigg" README, "The machine": copy, read and GEMV
+ * bandwidth side by side).  Reads `bytes` (a multiple of 16) from the
+ * 16-byte aligned device buffer `src` with 16-byte non-allocating loads and
+ * XORs what it read into out[0 .. q8_stream_read_out_words()) (device
+ * words, zeroed by the caller, one per CTA), so the loads are not elided.
+ */
+q8_status q8_stream_read(const void *src, size_t bytes, uint32_t *out, q8_stream_t stream);
+size_t q8_stream_read_out_words(void);
+
+/*
  * q8_selftest_wait_timeout -- exercise the kernels' failure path without a
  * fault: one thread waits, with the same bounded mbarrier wait the kernels
  * use, on a barrier that nothing ever arrives on, gives up after limit_ns
