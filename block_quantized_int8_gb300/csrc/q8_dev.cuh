@@ -174,6 +174,16 @@ __device__ __forceinline__ void codes4_to_f32(uint32_t w, float &f0, float &f1, 
 __device__ __forceinline__ float bf16lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// bf16 bits b that binary16 holds exactly: zero, or |b| in [2^-17, 65504]
+// (biased exponent >= 110 and magnitude bits <= 0x477F = 65280, the largest
+// bf16 not above 65504); NaN and infinity fail the second test.  Integer
+// compares only (measured: the same test on floats made the pipeline
+// kernel's x preparation several times slower).
+__device__ __forceinline__ bool bf16_fits_f16(uint32_t b) {
+    const uint32_t m = b & 0x7FFFu;
+    return m == 0u || m - 0x3700u <= 0x477Fu - 0x3700u;
+}
+
 // binary16 bits -> float (exact)
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
     float f;

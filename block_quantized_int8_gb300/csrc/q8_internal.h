@@ -47,8 +47,12 @@ size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *pla
 
 // Workspace of a skinny call: the general kernel's plan of every matrix, then
 // (when some matrix is served by the GEMV) a 256-byte block whose first word
-// is the GEMV's pool counter, at *sched_off (SIZE_MAX if none).
-size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off);
+// is the GEMV's pool counter, at *sched_off (SIZE_MAX if none), then (when
+// some matrix is served by the tile kernel) the tile kernel's x copies, one
+// tile_x_bytes region per such matrix in call order, at *tile_off (SIZE_MAX
+// if none).
+size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
+                        size_t *tile_off = nullptr);
 
 // M = 1 bulk-copy pipeline (q8_gemv.cu): matrices with K <= 12288.
 bool gemv_k_supported(int64_t K);
@@ -67,8 +71,11 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
 
 // 2 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256.
 bool tile_k_supported(int64_t K);
-q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
-                      bool chained = false);
+// workspace bytes of one matrix served by the tile kernel (its x copy and
+// per-chunk flags); the matrices of a call take consecutive regions from xws
+size_t tile_x_bytes(int64_t K, int M);
+q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
+                      cudaStream_t stream, bool chained = false);
 
 // GGUF Q8_0 block repack (q8_gguf.cu): nblocks blocks of 34 bytes (binary16
 // scale, 32 int8 codes) <-> planar codes (32 bytes per block) and scales.

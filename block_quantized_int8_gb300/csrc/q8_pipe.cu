@@ -192,16 +192,6 @@ __device__ __noinline__ float4 slow_blocks(const uint8_t *ca, const uint8_t *cb,
     return acc;
 }
 
-// bf16 bits b that binary16 holds exactly: zero, or |b| in [2^-17, 65504]
-// (biased exponent >= 110 and magnitude bits <= 0x477F = 65280, the largest
-// bf16 not above 65504); NaN and infinity fail the second test.  Integer
-// compares only (measured: the same test on floats made the x preparation
-// at the head of each CTA several times slower).
-__device__ __forceinline__ bool bf16_fits_f16(uint32_t b) {
-    const uint32_t m = b & 0x7FFFu;
-    return m == 0u || m - 0x3700u <= 0x477Fu - 0x3700u;
-}
-
 // x slice of activation row g (xg, null past M) as binary16 for the mma B
 // operand.  bf16 has 8 significant bits, so binary16 holds a bf16 value
 // exactly when it is zero or its magnitude lies in [2^-17, 65504] (below

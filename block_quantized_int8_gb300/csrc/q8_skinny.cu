@@ -408,14 +408,26 @@ Route route_of(int64_t K, int M, int variant) {
 
 }  // namespace
 
-size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off) {
+size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
+                        size_t *tile_off) {
     size_t need = count > 0 ? plan_skinny(descs, count, M, plans) : 0;
     *sched_off = SIZE_MAX;
     bool gemv = false;
-    for (int i = 0; i < count; ++i) gemv = gemv || route_of(descs[i].K, M, Q8_VARIANT_AUTO) == kRouteGemv;
+    size_t tile_bytes = 0;
+    for (int i = 0; i < count; ++i) {
+        const Route r = route_of(descs[i].K, M, Q8_VARIANT_AUTO);
+        gemv = gemv || r == kRouteGemv;
+        if (r == kRouteTile) tile_bytes += tile_x_bytes(descs[i].K, M);
+    }
     if (gemv) {
         *sched_off = (need + 255) / 256 * 256;
         need = *sched_off + 256;
+    }
+    if (tile_off) *tile_off = SIZE_MAX;
+    if (tile_bytes > 0) {
+        const size_t off = (need + 255) / 256 * 256;
+        if (tile_off) *tile_off = off;
+        need = off + tile_bytes;
     }
     return need;
 }
@@ -434,8 +446,8 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     // serves it, and the GEMV's pool counter) is checked before anything is
     // enqueued; the general kernel uses the front of it
     SplitPlan plans[Q8_MAX_BATCH];
-    size_t sched_off;
-    const size_t need = skinny_workspace(all, all_count, M, plans, &sched_off);
+    size_t sched_off, tile_off;
+    const size_t need = skinny_workspace(all, all_count, M, plans, &sched_off, &tile_off);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return Q8_ERR_ALIGN;
     const q8_linear_desc *descs = part[kRouteGeneral];
@@ -453,7 +465,8 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
         if (st != Q8_OK) return st;
     }
     if (n[kRouteTile] > 0) {
-        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, dev_status, stream, chained);
+        uint8_t *xws = tile_off == SIZE_MAX ? nullptr : static_cast<uint8_t *>(ws) + tile_off;
+        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, xws, dev_status, stream, chained);
         if (st != Q8_OK) return st;
     }
     if (count == 0) return Q8_OK;

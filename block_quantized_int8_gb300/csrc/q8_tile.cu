@@ -18,10 +18,18 @@
 //    first stages and the warp that releases a slot last issues the next one.
 //  * The 8 warps split a stage as 8 / S row tiles of 16 x S chunks.  S (1, 2
 //    or 4) is chosen per launch so that a small launch still fills the GPU.
-//  * Per 32-code block a warp converts its codes to bf16 exactly (a sign
-//    split, |q| <= 127), runs two mma.sync.m16n8k16 per 8 activation rows
-//    (weights as A, x^T as B) and adds the result times the binary16 block
-//    scale of each row to an fp32 accumulator.  Products are exact.
+//  * Per 32-code block a warp converts its codes exactly (|q| <= 127), runs
+//    two mma.sync.m16n8k16 per 8 activation rows (weights as A, x^T as B)
+//    and adds the result times the binary16 block scale of each row to an
+//    fp32 accumulator.  Products are exact.  For M <= 16 the operands are
+//    binary16 (codes in three operations per pair) wherever binary16 holds
+//    the chunk's x exactly, bf16 (codes by a sign split, four operations per
+//    pair) elsewhere: a small kernel launched first copies each distinct x
+//    into the workspace, chunk by chunk, as binary16 when every value of the
+//    chunk (all M rows) converts exactly, as the unchanged bf16 bits
+//    otherwise, with one flag word per chunk saying which, and the tile
+//    kernel reads x from that copy.  For M > 16 they are bf16, x read in
+//    place.
 //  * fp32 sums are kept in C = 4 / (row-tiles of 8 x rows) classes: chunk c
 //    goes to class c mod C, summed in chunk order; at the end of an item the
 //    classes are added in class order.  A class is never split between
@@ -55,6 +63,11 @@ constexpr int kRedBytes = 8192;         // class partials of one item: (8 / S) x
 template <int MT>
 constexpr int smem_bytes() { return 1024 + kSlots * kStage + (MT < 4 ? kRedBytes : 0) + 128; }
 static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
+// M <= 16 reads x from the workspace copy (binary16 where exact); M > 16 reads
+// the caller's bf16 x (measured: with four 8-row tiles per block the binary16
+// conversion of the codes gains nothing, and the second operand path costs
+// registers)
+constexpr bool tile_uses_x_copy(int MT) { return MT < 4; }
 
 struct TMaps {
     CUtensorMap q;      // int8 [N][K] as {128, N, K/128}, box {128, R, 2S}, 128-byte swizzle
@@ -64,6 +77,7 @@ struct TMaps {
 
 struct TDesc {
     float *y;
+    const uint32_t *xflag;  // per chunk: 0 = x copy is binary16, 1 = bf16
     int64_t ldy;
     int32_t N;
     int32_t KC;          // chunks per row, K / 256
@@ -123,7 +137,8 @@ struct Pos {
 //   cb: the chunk's first code box (128 K-bytes x R rows, swizzled), rb = R x 128
 //   xb: the chunk's first x box (64 K x MP rows, swizzled)
 //   sa, sb: the block scales of rows ra and ra + 8
-template <int MT>
+//   F16: x of the chunk is binary16 (else bf16)
+template <int MT, bool F16>
 __device__ __forceinline__ void chunk_mma(float (&a)[MT][4], const uint8_t *cb, int rb, const uint8_t *xb,
                                           const uint16_t *sa, const uint16_t *sb, int ra, const uint32_t (&offq)[4],
                                           const uint32_t (&offx)[2], int g) {
@@ -136,17 +151,29 @@ __device__ __forceinline__ void chunk_mma(float (&a)[MT][4], const uint8_t *cb, 
         const float s_a = f16_bits_to_f32(sa[bl]);
         const float s_b = f16_bits_to_f32(sb[bl]);
         uint32_t a01, a23, a45, a67, b01, b23, b45, b67;
-        codes4_to_bf16x2(wa.x, a01, a23);
-        codes4_to_bf16x2(wa.y, a45, a67);
-        codes4_to_bf16x2(wb.x, b01, b23);
-        codes4_to_bf16x2(wb.y, b45, b67);
+        if constexpr (F16) {
+            codes4_to_f16x2(wa.x, a01, a23);
+            codes4_to_f16x2(wa.y, a45, a67);
+            codes4_to_f16x2(wb.x, b01, b23);
+            codes4_to_f16x2(wb.y, b45, b67);
+        } else {
+            codes4_to_bf16x2(wa.x, a01, a23);
+            codes4_to_bf16x2(wa.y, a45, a67);
+            codes4_to_bf16x2(wb.x, b01, b23);
+            codes4_to_bf16x2(wb.y, b45, b67);
+        }
         const uint8_t *xbox = xb + (bl >> 1) * (MP * 128);
 #pragma unroll
         for (int j = 0; j < MT; ++j) {
             const uint4 xj = *reinterpret_cast<const uint4 *>(xbox + (8 * j + g) * 128 + offx[bl & 1]);
             float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-            mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xj.x, xj.y);
-            mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xj.z, xj.w);
+            if constexpr (F16) {
+                mma_f16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xj.x, xj.y);
+                mma_f16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xj.z, xj.w);
+            } else {
+                mma_bf16_16816(d0, d1, d2, d3, a01, b01, a23, b23, xj.x, xj.y);
+                mma_bf16_16816(d0, d1, d2, d3, a45, b45, a67, b67, xj.z, xj.w);
+            }
             a[j][0] = fmaf(s_a, d0, a[j][0]);
             a[j][1] = fmaf(s_a, d1, a[j][1]);
             a[j][2] = fmaf(s_b, d2, a[j][2]);
@@ -176,6 +203,7 @@ template <int MT>
 __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant__ TParams p) {
     constexpr int MP = MT * 8;
     constexpr int C = 4 / MT;  // accumulator classes
+    constexpr bool kCopy = tile_uses_x_copy(MT);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -260,6 +288,12 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
 #pragma unroll
     for (int h = 0; h < 2; ++h) offx[h] = (((4 * h + t) ^ g)) << 4;
 
+    // x flags (bit j: the chunk this warp computes in stage j of the item is
+    // bf16, else binary16) of up to 32 stages, loaded at the item's first
+    // stage and every 32 stages after; written by the x copy kernel, which
+    // completed before the wait above; read through L2
+    uint32_t xmask = 0u;
+
     float acc[C][MT][4];
 #pragma unroll
     for (int c = 0; c < C; ++c)
@@ -278,6 +312,12 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const int ks = warp >> (3 - lgS);             // chunk of the stage
         const int ra = 16 * rt + g;                   // item-local rows of this lane: ra, ra + 8
         const int cls = (pos.chunk + ks) & (C - 1);
+        const int js = pos.chunk >> lgS;  // stage of the item
+        if (kCopy && (js & 31) == 0) {
+            const int c = pos.chunk + ks + S * lane;
+            xmask = __ballot_sync(0xffffffffu, c < D.KC && __ldcg(D.xflag + c) != 0u);
+        }
+        const uint32_t xbf = kCopy ? (xmask >> (js & 31)) & 1u : 1u;
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
             drain_after_timeout();
@@ -290,21 +330,31 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             const uint8_t *xb = st + kCodeBytes + 4 * ks * (MP * 128);
             const uint16_t *sa = reinterpret_cast<const uint16_t *>(st + kCodeBytes + kXBytes) + (ra << (3 + lgS)) + 8 * ks;
             const uint16_t *sb = sa + (8 << (3 + lgS));
+            // the class index must be a constant for the accumulators to stay
+            // in registers: one call per class and operand type
+#define Q8_TILE_CHUNK(c)                                                          \
+    do {                                                                          \
+        if (kCopy && xbf == 0u)                                                   \
+            chunk_mma<MT, kCopy>(acc[(c) % C], cb, rb, xb, sa, sb, ra, offq, offx, g); \
+        else                                                                      \
+            chunk_mma<MT, false>(acc[(c) % C], cb, rb, xb, sa, sb, ra, offq, offx, g); \
+    } while (0)
             if constexpr (C == 4) {
                 switch (cls) {
-                    case 0: chunk_mma<MT>(acc[0], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
-                    case 1: chunk_mma<MT>(acc[1 % C], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
-                    case 2: chunk_mma<MT>(acc[2 % C], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
-                    default: chunk_mma<MT>(acc[3 % C], cb, rb, xb, sa, sb, ra, offq, offx, g); break;
+                    case 0: Q8_TILE_CHUNK(0); break;
+                    case 1: Q8_TILE_CHUNK(1); break;
+                    case 2: Q8_TILE_CHUNK(2); break;
+                    default: Q8_TILE_CHUNK(3); break;
                 }
             } else if constexpr (C == 2) {
                 if (cls == 0)
-                    chunk_mma<MT>(acc[0], cb, rb, xb, sa, sb, ra, offq, offx, g);
+                    Q8_TILE_CHUNK(0);
                 else
-                    chunk_mma<MT>(acc[1 % C], cb, rb, xb, sa, sb, ra, offq, offx, g);
+                    Q8_TILE_CHUNK(1);
             } else {
-                chunk_mma<MT>(acc[0], cb, rb, xb, sa, sb, ra, offq, offx, g);
+                Q8_TILE_CHUNK(0);
             }
+#undef Q8_TILE_CHUNK
         }
         // the item's last stage: add the classes in class order and store y
         if (pos.chunk + S == D.KC) {
@@ -388,6 +438,70 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     }
 }
 
+// ---- the x copy ------------------------------------------------------------------
+struct XJob {
+    const uint16_t *x;    // bf16 bits [M][ldx]
+    uint16_t *xo;         // copy [M][K], binary16 or bf16 bits per chunk
+    uint32_t *flag;       // [K / 256]: 0 = binary16, 1 = bf16
+    int64_t ldx;
+    int64_t K;
+    int32_t chunk_begin;  // first CTA of this x
+};
+
+struct XParams {
+    XJob j[Q8_MAX_BATCH];
+    int32_t count;
+    int32_t M;
+};
+
+// One CTA per chunk of 256 columns of one x, all M <= 32 rows: thread t
+// holds the 8 values at columns 8 (t % 32) .. 8 (t % 32) + 7 of rows t / 32,
+// t / 32 + 8, t / 32 + 16 and t / 32 + 24.  The chunk goes out as binary16 if
+// binary16 holds every one of its values exactly, else bit for bit as bf16.
+__global__ void __launch_bounds__(kThreads) x_copy_kernel(const __grid_constant__ XParams p) {
+    // the tile kernel may start launching at once: it reads weights only
+    // until this kernel has completed
+    pdl_launch_dependents();
+    int j = 0;
+    while (j + 1 < p.count && static_cast<int>(blockIdx.x) >= p.j[j + 1].chunk_begin) ++j;
+    const XJob &J = p.j[j];
+    const int c = static_cast<int>(blockIdx.x) - J.chunk_begin;
+    const int64_t col = static_cast<int64_t>(c) * kChunk + 8 * (threadIdx.x & 31);
+    const int r0 = static_cast<int>(threadIdx.x >> 5);
+    // x may be written by the kernels before this one
+    pdl_wait_prior();
+    uint4 v[4];
+    bool inexact = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + 8 * i;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.M) {
+            v[i] = __ldcg(reinterpret_cast<const uint4 *>(J.x + r * J.ldx + col));
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                inexact |= !bf16_fits_f16(w[e] & 0xFFFFu) || !bf16_fits_f16(w[e] >> 16);
+        }
+    }
+    const bool keep = __syncthreads_or(inexact) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + 8 * i;
+        if (r < p.M) {
+            uint4 o = v[i];
+            if (!keep) {
+                o.x = f32x2_to_f16x2(bf16lo_f32(v[i].x), bf16hi_f32(v[i].x));
+                o.y = f32x2_to_f16x2(bf16lo_f32(v[i].y), bf16hi_f32(v[i].y));
+                o.z = f32x2_to_f16x2(bf16lo_f32(v[i].z), bf16hi_f32(v[i].z));
+                o.w = f32x2_to_f16x2(bf16lo_f32(v[i].w), bf16hi_f32(v[i].w));
+            }
+            *reinterpret_cast<uint4 *>(J.xo + r * J.K + col) = o;
+        }
+    }
+    if (threadIdx.x == 0) J.flag[c] = keep ? 1u : 0u;
+}
+
 int g_configured_dev = -1;
 int g_occ = 0;
 
@@ -440,8 +554,19 @@ int log2_of(int S) { return S >= 4 ? 2 : (S >= 2 ? 1 : 0); }
 
 bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
 
-q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
-                      bool chained) {
+namespace {
+size_t up256(int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); }
+}  // namespace
+
+// workspace of one matrix: its x copy, then one flag word per chunk (none
+// where the kernel reads the caller's x)
+size_t tile_x_bytes(int64_t K, int M) {
+    if (!tile_uses_x_copy(M <= 8 ? 1 : (M <= 16 ? 2 : 4))) return 0;
+    return up256(static_cast<int64_t>(M) * K * 2) + up256(K / kChunk * 4);
+}
+
+q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
+                      cudaStream_t stream, bool chained) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (M < 2 || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
@@ -454,7 +579,10 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
         g_configured_dev = di->device;
     }
     static thread_local TParams p;
+    static thread_local XParams xp;
     const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
+    const bool copy = tile_uses_x_copy(MT);
+    if (copy && xws == nullptr) return Q8_ERR_WORKSPACE;
     const int MP = 8 * MT;
     const int C = 4 / MT;
     // the fewest chunks per stage that give every SM an item (measured: a
@@ -472,10 +600,40 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
     }
     int items = 0;
     double total_bytes = 0.0;
+    // x copies: matrix i owns the workspace region after those of 0 .. i-1;
+    // a matrix whose x (pointer, row stride, K) an earlier one already has
+    // reads that one's copy
+    int xcopy[Q8_MAX_BATCH];
+    size_t region[Q8_MAX_BATCH];
+    int chunks = 0;
+    xp.count = 0;
+    xp.M = M;
+    size_t off = 0;
+    for (int i = 0; i < count && copy; ++i) {
+        const q8_linear_desc &d = descs[i];
+        region[i] = off;
+        off += tile_x_bytes(d.K, M);
+        xcopy[i] = -1;
+        for (int j = 0; j < i && xcopy[i] < 0; ++j)
+            if (descs[j].x == d.x && descs[j].ldx == d.ldx && descs[j].K == d.K) xcopy[i] = xcopy[j];
+        if (xcopy[i] >= 0) continue;
+        XJob &J = xp.j[xp.count];
+        J.x = d.x;
+        J.xo = reinterpret_cast<uint16_t *>(xws + region[i]);
+        J.flag = reinterpret_cast<uint32_t *>(xws + region[i] + up256(static_cast<int64_t>(M) * d.K * 2));
+        J.ldx = d.ldx;
+        J.K = d.K;
+        J.chunk_begin = chunks;
+        chunks += static_cast<int>(d.K / kChunk);
+        xcopy[i] = xp.count++;
+    }
     for (int i = 0; i < count; ++i) {
         TDesc &D = p.d[i];
         TMaps &T = p.m[i];
         const q8_linear_desc &d = descs[i];
+        // x as the kernel reads it: the copy [M][K], or the caller's [M][ldx]
+        const void *xsrc = copy ? static_cast<const void *>(xp.j[xcopy[i]].xo) : static_cast<const void *>(d.x);
+        const int64_t xld = copy ? d.K : d.ldx;
         const int64_t KC = d.K / kChunk;
         const int Sd = split_for(KC, S);
         const uint32_t R = static_cast<uint32_t>(128 / Sd);
@@ -483,15 +641,16 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
         const uint64_t qstr[2] = {static_cast<uint64_t>(d.K), 128};
         const uint32_t qbox[3] = {128, R, static_cast<uint32_t>(2 * Sd)};
         const uint64_t xdims[3] = {64, static_cast<uint64_t>(M), static_cast<uint64_t>(d.K / 64)};
-        const uint64_t xstr[2] = {static_cast<uint64_t>(d.ldx) * 2, 128};
+        const uint64_t xstr[2] = {static_cast<uint64_t>(xld) * 2, 128};
         const uint32_t xbox[3] = {64, static_cast<uint32_t>(MP), static_cast<uint32_t>(4 * Sd)};
         const int64_t nb = d.K / 32;
         if (!encode_tmap(&T.q, 1, d.q, 3, qdims, qstr, qbox, true) ||
-            !encode_tmap(&T.x, 2, d.x, 3, xdims, xstr, xbox, true) ||
+            !encode_tmap(&T.x, 2, xsrc, 3, xdims, xstr, xbox, true) ||
             !encode_2d(&T.s, 2, d.s, static_cast<uint64_t>(nb), static_cast<uint64_t>(d.N),
                        static_cast<uint64_t>(nb) * 2, static_cast<uint32_t>(8 * Sd), R, false))
             return Q8_ERR_CUDA;
         D.y = d.y;
+        D.xflag = copy ? xp.j[xcopy[i]].flag : nullptr;
         D.ldy = d.ldy;
         D.N = static_cast<int32_t>(d.N);
         D.KC = static_cast<int32_t>(KC);
@@ -506,9 +665,13 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint32_t *d
     p.count = count;
     p.M = M;
     if (items == 0) return Q8_OK;
-    if (MT == 1) return run<1>(p, di, items, total_bytes, stream, chained);
-    return MT == 2 ? run<2>(p, di, items, total_bytes, stream, chained)
-                   : run<4>(p, di, items, total_bytes, stream, chained);
+    // the x copy (waits for the kernels before it when chained), then the
+    // tiles as its dependent: their first weight stages load while it runs
+    if (copy && launch_kernel(x_copy_kernel, dim3(chunks), dim3(kThreads), 0, stream, chained, xp) != cudaSuccess)
+        return Q8_ERR_CUDA;
+    const bool dep = copy || chained;
+    if (MT == 1) return run<1>(p, di, items, total_bytes, stream, dep);
+    return MT == 2 ? run<2>(p, di, items, total_bytes, stream, dep) : run<4>(p, di, items, total_bytes, stream, dep);
 }
 
 }  // namespace q8

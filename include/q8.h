@@ -239,8 +239,16 @@ q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t
                              int32_t variant, void *ws, size_t ws_bytes,
                              uint32_t *dev_status, q8_stream_t stream);
 
-/* Workspace bytes (split-K partial sums and tickets) for the calls above;
- * depends only on the shapes, not on the device.  0 means none is needed. */
+/* Workspace bytes for the calls above; depends only on the shapes, not on
+ * the device.  0 means none is needed.  It holds the split-K partial sums and
+ * tickets, at M = 1 the GEMV's counter block, and for every matrix that the
+ * tile kernel serves (2 <= M <= 32, K a multiple of 256, and M > 8 or
+ * K > 1536) a copy of its x, M * K * 2 bytes rounded up to 256, plus a
+ * 256-byte-rounded flag word per 256 columns of K: each 256-column chunk of
+ * x (all M rows) is copied as binary16 where binary16 holds all its values
+ * exactly, else as bf16, and the matmul takes the matching operand type.
+ * The copies need no zeroing; the words the kernels count with are left
+ * zero. */
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M);
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M);
 

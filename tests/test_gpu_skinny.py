@@ -469,3 +469,52 @@ def test_gemv_mixed_batch_tolerance(oracle):
     for m_np, y in zip(mats_np, ys):
         (y1,) = run_batch([m_np], 1, 0)
         assert np.array_equal(y1, y)
+
+
+@pytest.mark.parametrize("N,K,M", [(300, 1024, 12), (130, 2048, 3), (96, 1536, 16)])
+def test_tile_x_copy_chunks(oracle, N, K, M):
+    """The tile kernel (M <= 16) reads x from a copy in the workspace: each 256-column
+    chunk (all M rows) as binary16 when binary16 holds every value of the
+    chunk exactly (zero, or magnitude in [2^-17, 65504]), else as the bf16
+    bits, with one flag word per chunk (0 = binary16).  Checked against that
+    rule restated on the float values, then the result against the oracle."""
+    from block_quantized_int8_gb300 import q8
+    KC = K // 256
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"xc{N}.{K}"))
+    xn = synth.activations(M, K, 0, f"xcx{M}.{K}").copy()
+    # chunk 1 gets a value below binary16's exact range in its last row,
+    # chunk 3 (if any) one above it in its first row; the rest stay N(0, 1)
+    tiny = np.array([3e-7], dtype=np.float32).view(np.uint32)[0] >> 16
+    huge = np.array([1e5], dtype=np.float32).view(np.uint32)[0] >> 16
+    xn[M - 1, 256 + 17] = tiny
+    if KC > 3:
+        xn[0, 3 * 256 + 200] = huge
+    xf = (xn.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    a = np.abs(xf)
+    fits = (a == 0) | ((a >= 2.0 ** -17) & (a <= 65504.0))
+    want_flags = np.array([0 if fits[:, 256 * c:256 * (c + 1)].all() else 1 for c in range(KC)], np.uint32)
+    assert want_flags[1] == 1 and 0 in want_flags
+
+    q, s = weights_dev(qn, sn)
+    x = x_dev(xn)
+    need = q8.q8_workspace_size(N, K, M)
+    copy_bytes = (M * K * 2 + 255) // 256 * 256
+    tile_bytes = copy_bytes + (KC * 4 + 255) // 256 * 256
+    assert need >= tile_bytes
+    ws = q8.workspace(need)
+    y = q8.q8_gemm_skinny(q, s, x, ws=ws)
+    torch.cuda.synchronize()
+    w = ws.cpu().numpy()
+    off = need - tile_bytes
+    got_copy = w[off:off + M * K * 2].view(np.uint16).reshape(M, K)
+    got_flags = w[off + copy_bytes:off + copy_bytes + KC * 4].view(np.uint32)
+    assert np.array_equal(got_flags, want_flags)
+    for c in range(KC):
+        cols = slice(256 * c, 256 * (c + 1))
+        if want_flags[c]:
+            want = xn[:, cols]
+        else:
+            want = xf[:, cols].astype(np.float16).view(np.uint16)
+        assert np.array_equal(got_copy[:, cols], want), f"chunk {c}"
+    y_ref, B = oracle.matmul(qn, sn, xn, threads=8)
+    check_tol(y.cpu().numpy(), y_ref, B, f"x copy N={N} K={K} M={M}")
