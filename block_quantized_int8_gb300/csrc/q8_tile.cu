@@ -1,7 +1,7 @@
 // q8_tile.cu -- Q8_0 W8A16 matmul for 2 <= M <= 32 activation rows over one or
 // several matrices in one persistent launch (K a multiple of 256).  Serves
-// M = 9..32, and M = 2..8 when a matrix has K > 1536 (q8_pipe.cu is faster on
-// the shorter rows, the chunked tiles on the longer ones).
+// M = 9..32, and M = 2..8 unless K = 1536 (there q8_pipe.cu's whole-row
+// stages are as fast in batches and faster for a lone matrix).
 //
 // Y[m][n] = sum_k s[n][k/32] * q[n][k] * x[m][k]; "Frigg" README, Finding 8
 // (a batched W8A16 kernel reads each weight once for the whole batch of rows)

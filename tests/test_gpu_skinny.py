@@ -238,9 +238,9 @@ def test_layer_set_bench_step_sampled(oracle):
 @pytest.mark.parametrize("M", [1, 3, 8, 20])
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
-    # shapes that the automatic routing sends to different kernels: K <= 1536
-    # and K % 256 != 0 (pipeline for M <= 8), K > 1536 with K % 256 == 0
-    # (tiles for M >= 2), K > 4096 off the 256 grid and K > 12288 (general)
+    # shapes that the automatic routing sends to different kernels: K = 1536
+    # or K % 256 != 0 (pipeline for M <= 8), other K % 256 == 0 (tiles for
+    # M >= 2), K > 4096 off the 256 grid and K > 12288 (general)
     shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 256),
               (130, 2080), (300, 4128), (96, 12800)]
     mats_np = []
@@ -258,7 +258,7 @@ def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
 def test_tile_k_split_keeps_bits(oracle, M, K):
     """A lone small matrix gets its K split across warps (to fill the GPU);
     in a launch with many rows it is not.  Its result must not change."""
-    if M <= 8 and K <= 1536:
+    if M <= 8 and K == 1536:
         pytest.skip("served by the pipeline kernel, not the tiles")
     qn, sn, _ = oracle.quantize_rows(synth.weights(1536, K, 0, "ks"))
     mat = (qn, sn, synth.activations(M, K, 0, "ksx"))
