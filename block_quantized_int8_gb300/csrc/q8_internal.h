@@ -48,9 +48,8 @@ size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *pla
 // Workspace of a skinny call: the general kernel's plan of every matrix, then
 // (when some matrix is served by the GEMV) a 256-byte block whose first word
 // is the GEMV's pool counter, at *sched_off (SIZE_MAX if none), then (when
-// some matrix is served by the tile kernel) the tile kernel's x copies, one
-// tile_x_bytes region per such matrix in call order, at *tile_off (SIZE_MAX
-// if none).
+// some matrix is served by the tile kernel) the tile kernel's workspace
+// (tile_workspace of those matrices) at *tile_off (SIZE_MAX if none).
 size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
                         size_t *tile_off = nullptr);
 
@@ -71,9 +70,12 @@ q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *d
 
 // 2 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256.
 bool tile_k_supported(int64_t K);
-// workspace bytes of one matrix served by the tile kernel (its x copy and
-// per-chunk flags); the matrices of a call take consecutive regions from xws
-size_t tile_x_bytes(int64_t K, int M);
+// workspace bytes of the tile kernel for these matrices: each one's x copy
+// and per-chunk flags (M <= 16), in call order, then the tickets and
+// partials of the row blocks that CTAs share; the tickets (zero between
+// launches) are [*ticket_off, *ticket_off + *ticket_bytes)
+size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off = nullptr,
+                      size_t *ticket_bytes = nullptr);
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
                       cudaStream_t stream, bool chained = false);
 

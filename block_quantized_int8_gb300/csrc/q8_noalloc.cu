@@ -80,10 +80,18 @@ extern "C" q8_status q8_gemm_skinny_noalloc(const int8_t *q, const uint16_t *s, 
 
     if (need > 0) {
         // clear the words the kernels count with: the ticket words (first in
-        // the layout) and the GEMV's pool counter block (last)
+        // the layout), the GEMV's pool counter block and the tile kernel's
+        // tickets of shared row blocks
         SplitPlan pl;
-        size_t sched_off;
-        (void)skinny_workspace(&d, 1, M, &pl, &sched_off);
+        size_t sched_off, tile_off;
+        (void)skinny_workspace(&d, 1, M, &pl, &sched_off, &tile_off);
+        if (tile_off != SIZE_MAX) {
+            size_t toff = 0, tbytes = 0;
+            (void)tile_workspace(&d, 1, M, &toff, &tbytes);
+            if (tbytes > 0 && cudaMemsetAsync(static_cast<unsigned char *>(ws) + tile_off + toff, 0, tbytes,
+                                              reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                return Q8_ERR_CUDA;
+        }
         const size_t ticket_bytes = pl.part_off - pl.ticket_off;
         if (ticket_bytes > 0 &&
             cudaMemsetAsync(static_cast<unsigned char *>(ws) + pl.ticket_off, 0, ticket_bytes,

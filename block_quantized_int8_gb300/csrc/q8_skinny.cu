@@ -417,12 +417,14 @@ size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan
     size_t need = count > 0 ? plan_skinny(descs, count, M, plans) : 0;
     *sched_off = SIZE_MAX;
     bool gemv = false;
-    size_t tile_bytes = 0;
+    q8_linear_desc tiles[Q8_MAX_BATCH];
+    int ntiles = 0;
     for (int i = 0; i < count; ++i) {
         const Route r = route_of(descs[i].K, M, Q8_VARIANT_AUTO);
         gemv = gemv || r == kRouteGemv;
-        if (r == kRouteTile) tile_bytes += tile_x_bytes(descs[i].K, M);
+        if (r == kRouteTile && ntiles < Q8_MAX_BATCH) tiles[ntiles++] = descs[i];
     }
+    const size_t tile_bytes = ntiles > 0 ? tile_workspace(tiles, ntiles, M) : 0;
     if (gemv) {
         *sched_off = (need + 255) / 256 * 256;
         need = *sched_off + 256;

@@ -8,16 +8,13 @@
 // and Finding 3 (one launch for the many small matrices of a decode step).
 //
 // Design (TMA fed, tensor cores through warp mma):
-//  * K is cut into chunks of 256.  A stage is S consecutive chunks of
-//    R = 128 / S weight rows (32 KB of codes), with the x chunks and block
-//    scales that go with them, each loaded by one cp.async.bulk.tensor (codes
-//    and x in the 128-byte swizzled layout, so the lanes' fragment reads fall
-//    on distinct banks).  An item is R rows of one matrix over all of K; CTAs
-//    own contiguous, byte-balanced ranges of items and stream them through a
-//    2-slot ring (two CTAs per SM).  No producer warp: thread 0 issues the
-//    first stages and the warp that releases a slot last issues the next one.
-//  * The 8 warps split a stage as 8 / S row tiles of 16 x S chunks.  S (1, 2
-//    or 4) is chosen per launch so that a small launch still fills the GPU.
+//  * K is cut into chunks of 256.  A stage is one chunk of 128 weight rows
+//    (32 KB of codes), with the x chunk and the block scales that go with
+//    it, each loaded by one cp.async.bulk.tensor (codes and x in the
+//    128-byte swizzled layout, so the lanes' fragment reads fall on distinct
+//    banks).  The 8 warps own 16 rows each.  No producer warp: thread 0
+//    issues the first stages and the warp that releases a slot last issues
+//    the next one, through a 2-slot ring (two CTAs per SM).
 //  * Per 32-code block a warp converts its codes exactly (|q| <= 127), runs
 //    two mma.sync.m16n8k16 per 8 activation rows (weights as A, x^T as B)
 //    and adds the result times the binary16 block scale of each row to an
@@ -30,16 +27,22 @@
 //    otherwise, with one flag word per chunk saying which, and the tile
 //    kernel reads x from that copy.  For M > 16 they are bf16, x read in
 //    place.
-//  * fp32 sums are kept in C = 4 / (row-tiles of 8 x rows) classes: chunk c
-//    goes to class c mod C, summed in chunk order; at the end of an item the
-//    classes are added in class order.  A class is never split between
-//    warps (S divides C), so the bits do not depend on S: a matrix gives the
-//    same result alone or in any batch.  With S > 1 the warps publish their
-//    classes in shared memory and the last warp of the row tile adds them.
+//  * Work units: the chunks of a matrix fall into C classes of consecutive
+//    chunks (up to 4 of at least 2 chunks each for M <= 16, 1 above); an item is one class
+//    of one block of 128 rows.  A class's blocks are summed in chunk order,
+//    and a row block's classes are added in class order, so the result
+//    depends on the matrix and M only: the same bits alone or in any batch,
+//    for any grid.  CTAs own contiguous, byte-balanced ranges of items (four
+//    per row block instead of one keeps the ranges even); a CTA that holds
+//    a row block from its first class adds the classes as it goes; where a
+//    row block is shared between CTAs, each writes its partial (the running
+//    sum through its last class, or single classes) to the workspace and the
+//    last to arrive on the row block's ticket adds them in class order.
 // Every wait is bounded (Q8_DEV_TIMEOUT on expiry).
 #include <cuda.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "q8_dev.cuh"
 #include "q8_internal.h"
@@ -51,28 +54,37 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunk = 256;             // K per chunk
+constexpr int kRows = 128;              // weight rows per stage and per item
 constexpr int kSlots = 2;
 constexpr int kMaxGrid = 320;           // >= SMs x 2 on GB300 (the parameter block is near its limit)
-constexpr int kCodeBytes = 32768;       // codes of a stage: (128 / S) rows x 256 S
-constexpr int kXBytes = 16384;          // x of a stage: MP rows x 256 S bf16, MP S <= 32
-constexpr int kScaleBytes = 2048;       // block scales of a stage: (128 / S) rows x 8 S
+constexpr int kMaxClasses = 4;
+constexpr int kCodeBytes = kRows * kChunk;  // codes of a stage
+constexpr int kXBytes = 16384;              // x of a stage: MP rows x 256 bf16, MP <= 32
+constexpr int kScaleBytes = kRows * 16;     // block scales of a stage: 128 rows x 8
 constexpr int kStage = kCodeBytes + kXBytes + kScaleBytes;  // a multiple of 1024
-constexpr int kRedBytes = 8192;         // class partials of one item: (8 / S) x C x 32 lanes x 4 MT floats
-// shared memory of tile_kernel<MT>: alignment slack, ring, class partials
-// (only where K can be split: MT < 4), barriers and counters
-template <int MT>
-constexpr int smem_bytes() { return 1024 + kSlots * kStage + (MT < 4 ? kRedBytes : 0) + 128; }
+// shared memory of tile_kernel: alignment slack, ring, barriers and counters
+constexpr int smem_bytes() { return 1024 + kSlots * kStage + 128; }
 static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
 // M <= 16 reads x from the workspace copy (binary16 where exact); M > 16 reads
 // the caller's bf16 x (measured: with four 8-row tiles per block the binary16
 // conversion of the codes gains nothing, and the second operand path costs
 // registers)
 constexpr bool tile_uses_x_copy(int MT) { return MT < 4; }
+// classes of a matrix with KC chunks: the most, up to 4, that divide KC
+// into classes of at least two chunks (measured: single-chunk classes cost
+// more at their ends than they balance); one for M > 16 (the accumulators
+// of a running class sum fit the registers for M <= 16 only)
+int classes_for(int64_t KC, int MT) {
+    if (MT >= 4) return 1;
+    for (int c = kMaxClasses; c > 1; --c)
+        if (KC % c == 0 && KC / c >= 2) return c;
+    return 1;
+}
 
 struct TMaps {
-    CUtensorMap q;      // int8 [N][K] as {128, N, K/128}, box {128, R, 2S}, 128-byte swizzle
-    CUtensorMap x;      // bf16 [M][ldx] as {64, M, K/64}, box {64, MP, 4S}, 128-byte swizzle
-    CUtensorMap s;      // binary16 [N][K/32], box {8S, R}
+    CUtensorMap q;      // int8 [N][K] as {128, N, K/128}, box {128, 128, 2}, 128-byte swizzle
+    CUtensorMap x;      // 16-bit [M][ld] as {64, M, K/64}, box {64, MP, 4}, 128-byte swizzle
+    CUtensorMap s;      // binary16 [N][K/32], box {8, 128}
 };
 
 struct TDesc {
@@ -82,21 +94,32 @@ struct TDesc {
     int32_t N;
     int32_t KC;          // chunks per row, K / 256
     int32_t item_begin;  // first global item of this matrix
-    int32_t items;       // ceil(N / R)
-    int32_t lgS;         // log2 of S, the chunks per stage (0, 1 or 2)
-    int32_t R;           // rows per item, 128 / S
+    int32_t items;       // row blocks x C
+    int32_t C;           // classes: class c holds chunks [c KC / C, (c + 1) KC / C)
+    int16_t cls[kMaxClasses + 1];  // the class bounds c KC / C
 };
 
+// A row block whose items are shared between CTAs: its partials and ticket
+// live in the workspace under a split id; `sharers` CTAs contribute, and the
+// one holding class 0 writes its running sum through class `pe`.
 struct TParams {
     TMaps m[Q8_MAX_BATCH];
     TDesc d[Q8_MAX_BATCH];
     uint32_t *status;
+    uint32_t *tickets;   // [split id][8 warps], zero between launches
+    float4 *parts;       // [split id][class][8 warps][32 lanes][MT]
     int32_t count;
     int32_t M;
     int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
     int32_t cta_begin[kMaxGrid + 1];
+    int16_t first_sid[kMaxGrid];  // split id of a CTA's first row block, -1 if whole
+    int16_t last_sid[kMaxGrid];   // split id of a CTA's last row block, -1 if whole
+    uint8_t sharers[kMaxGrid];
+    int8_t pe[kMaxGrid];
 };
 static_assert(sizeof(TParams) <= 32764, "kernel parameters exceed the 32764-byte limit");
+
+__host__ __device__ __forceinline__ int class_lo(int KC, int C, int c) { return (c * KC) / C; }
 
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *tm, int c0, int c1, uint64_t *bar) {
     asm volatile(
@@ -120,21 +143,38 @@ __device__ __forceinline__ int find_tdesc(const TParams &p, int item) {
     return d;
 }
 
-// Position (descriptor, item, first chunk) in a CTA's sequence of stages.
+// Position in a CTA's sequence of stages: descriptor, item, the chunk of
+// this stage and the end of the item's class.
 struct Pos {
-    int d, item, chunk;
+    int d, item, c, row0, chunk, cend;  // descriptor, item, its class and first row, chunk, class end
+    __device__ __forceinline__ void init(const TParams &p, int it) {
+        d = find_tdesc(p, it);
+        item = it;
+        const TDesc &D = p.d[d];
+        c = (it - D.item_begin) % D.C;
+        row0 = (it - D.item_begin) / D.C * kRows;
+        chunk = D.cls[c];
+        cend = D.cls[c + 1];
+    }
     __device__ __forceinline__ void next(const TParams &p) {
-        chunk += 1 << p.d[d].lgS;
-        if (chunk == p.d[d].KC) {
-            chunk = 0;
+        if (++chunk == cend) {
             ++item;
-            while (d + 1 < p.count && item >= p.d[d + 1].item_begin) ++d;
+            if (d + 1 < p.count && item >= p.d[d + 1].item_begin) {
+                while (d + 1 < p.count && item >= p.d[d + 1].item_begin) ++d;
+                c = 0;
+                row0 = 0;
+            } else if (++c == p.d[d].C) {
+                c = 0;
+                row0 += kRows;
+            }
+            chunk = p.d[d].cls[c];
+            cend = p.d[d].cls[c + 1];
         }
     }
 };
 
 // One chunk (8 blocks of 32) of a warp's 16-row tile into the accumulators a.
-//   cb: the chunk's first code box (128 K-bytes x R rows, swizzled), rb = R x 128
+//   cb: the chunk's first code box (128 K-bytes x 128 rows, swizzled), rb = 128 x 128
 //   xb: the chunk's first x box (64 K x MP rows, swizzled)
 //   sa, sb: the block scales of rows ra and ra + 8
 //   F16: x of the chunk is binary16 (else bf16)
@@ -199,18 +239,71 @@ __device__ __forceinline__ void store_tile(const TDesc &D, int row0, int ra, int
     }
 }
 
+
+// The partial of warp `warp` for class c of split row block `sid`:
+// [split id][class][warp][lane][MT] float4.
+template <int MT>
+__device__ __forceinline__ float4 *part_slot(const TParams &p, int sid, int c, int warp) {
+    return p.parts + ((static_cast<size_t>(sid) * kMaxClasses + c) * kWarps + warp) * 32 * MT;
+}
+
+template <int MT>
+__device__ __forceinline__ void put_part(float4 *slot, int lane, const float (&v)[MT][4]) {
+#pragma unroll
+    for (int j = 0; j < MT; ++j) slot[lane * MT + j] = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+}
+
+// Last of the sharers of split row block sid for this warp's rows: add the
+// partials in class order (the running sum through class pe, then the single
+// classes after it) and store the rows.  The tickets go back to zero.
+template <int MT>
+__device__ __forceinline__ void finish_split(const TParams &p, const TDesc &D, int sid, int warp, int lane,
+                                             int row0, int ra, int t) {
+    __threadfence();
+    __syncwarp();
+    uint32_t prev = 0;
+    if (lane == 0) prev = atomicAdd(&p.tickets[sid * kWarps + warp], 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev + 1 != p.sharers[sid]) return;
+    __threadfence();
+    const int pe = p.pe[sid];
+    float v[MT][4];
+    {
+        const float4 *s0 = part_slot<MT>(p, sid, pe, warp);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            const float4 u = __ldcg(s0 + lane * MT + j);
+            v[j][0] = u.x;
+            v[j][1] = u.y;
+            v[j][2] = u.z;
+            v[j][3] = u.w;
+        }
+    }
+    for (int c = pe + 1; c < D.C; ++c) {
+        const float4 *sc = part_slot<MT>(p, sid, c, warp);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            const float4 u = __ldcg(sc + lane * MT + j);
+            v[j][0] += u.x;
+            v[j][1] += u.y;
+            v[j][2] += u.z;
+            v[j][3] += u.w;
+        }
+    }
+    store_tile<MT>(D, row0, ra, t, p.M, v);
+    __syncwarp();
+    if (lane == 0) p.tickets[sid * kWarps + warp] = 0u;
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant__ TParams p) {
     constexpr int MP = MT * 8;
-    constexpr int C = 4 / MT;  // accumulator classes
     constexpr bool kCopy = tile_uses_x_copy(MT);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float4 *red = reinterpret_cast<float4 *>(base + kSlots * kStage);
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + kSlots * kStage + (MT < 4 ? kRedBytes : 0));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + kSlots * kStage);
     uint32_t *rel = reinterpret_cast<uint32_t *>(full + kSlots);  // per slot: warps done with it
-    uint32_t *cnt = rel + kSlots;                                 // per row tile: warps that published
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -225,7 +318,6 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             mbar_init(&full[i], 1);
             rel[i] = 0u;
         }
-        for (int i = 0; i < kWarps; ++i) cnt[i] = 0u;
         fence_mbar_init();
     }
     __syncthreads();
@@ -234,34 +326,37 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     if (p.early_signal && tid == 0) pdl_launch_dependents();
     if (ie <= ib) return;
 
-    // total stages of this CTA
+    // total stages of this CTA: the chunks of each item's class
     int nstages = 0;
     {
         int d = find_tdesc(p, ib);
         for (int it = ib; it < ie; ++it) {
             while (d + 1 < p.count && it >= p.d[d + 1].item_begin) ++d;
-            nstages += p.d[d].KC >> p.d[d].lgS;
+            const TDesc &D = p.d[d];
+            const int c = (it - D.item_begin) % D.C;
+            nstages += D.cls[c + 1] - D.cls[c];
         }
     }
 
     // stage k at position pos: all bytes announced on the slot's barrier,
     // then the weight boxes and (unless deferred) the x box
-    auto issue_x = [&](int k, Pos pos) {
+    auto issue_x = [&](int k, const Pos &pos) {
         const int slot = k % kSlots;
         tma_3d(base + slot * kStage + kCodeBytes, &p.m[pos.d].x, 0, 0, 4 * pos.chunk, &full[slot]);
     };
-    auto issue = [&](int k, Pos pos, bool with_x) {
+    auto issue = [&](int k, const Pos &pos, bool with_x) {
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
         const TMaps &T = p.m[pos.d];
         uint8_t *st = base + slot * kStage;
-        const int row0 = (pos.item - D.item_begin) * D.R;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + (MP * 512 << D.lgS) + kScaleBytes));
+        const int row0 = pos.row0;
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + MP * 512 + kScaleBytes));
         tma_3d(st, &T.q, 0, row0, 2 * pos.chunk, &full[slot]);
         tma_2d(st + kCodeBytes + kXBytes, &T.s, 8 * pos.chunk, row0, &full[slot]);
         if (with_x) issue_x(k, pos);
     };
-    Pos pos{find_tdesc(p, ib), ib, 0};
+    Pos pos;
+    pos.init(p, ib);
     // the first stages' weights go out at once; their x only after the
     // kernels before this one (when launched as their dependent) completed
     if (tid == 0) {
@@ -288,17 +383,18 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
 #pragma unroll
     for (int h = 0; h < 2; ++h) offx[h] = (((4 * h + t) ^ g)) << 4;
 
-    // x flags (bit j: the chunk this warp computes in stage j of the item is
-    // bf16, else binary16) of up to 32 stages, loaded at the item's first
-    // stage and every 32 stages after; written by the x copy kernel, which
-    // completed before the wait above; read through L2
+    const int ra = 16 * warp + g;  // item-local rows of this lane: ra, ra + 8
+    float acc[MT][4], fold[MT][4];
+#pragma unroll
+    for (int j = 0; j < MT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = fold[j][e] = 0.f;
+    // x flags of a matrix (bit j: chunk xbase + j reads bf16 x, else
+    // binary16), loaded when the matrix or the 32-chunk window changes;
+    // written by the x copy kernel, which completed before the wait above;
+    // read through L2
     uint32_t xmask = 0u;
-
-    float acc[C][MT][4];
-#pragma unroll
-    for (int c = 0; c < C; ++c)
-#pragma unroll
-        for (int j = 0; j < MT; ++j) acc[c][j][0] = acc[c][j][1] = acc[c][j][2] = acc[c][j][3] = 0.f;
+    int xd = -1, xbase = 0;
 
     for (int k = 0; k < nstages; ++k) {
         // every stage of this CTA is issued: a chained launch after this one
@@ -306,18 +402,14 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         if (!p.early_signal && k == max(0, nstages - kSlots) && tid == 0) pdl_launch_dependents();
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
-        const int lgS = C == 1 ? 0 : D.lgS;  // C == 1: never split
-        const int S = 1 << lgS;
-        const int rt = warp & ((kWarps >> lgS) - 1);  // row tile
-        const int ks = warp >> (3 - lgS);             // chunk of the stage
-        const int ra = 16 * rt + g;                   // item-local rows of this lane: ra, ra + 8
-        const int cls = (pos.chunk + ks) & (C - 1);
-        const int js = pos.chunk >> lgS;  // stage of the item
-        if (kCopy && (js & 31) == 0) {
-            const int c = pos.chunk + ks + S * lane;
-            xmask = __ballot_sync(0xffffffffu, c < D.KC && __ldcg(D.xflag + c) != 0u);
+        const int c = pos.c;
+        if (kCopy && (pos.d != xd || (pos.chunk & ~31) != xbase)) {
+            xd = pos.d;
+            xbase = pos.chunk & ~31;
+            const int ch = xbase + lane;
+            xmask = __ballot_sync(0xffffffffu, ch < D.KC && __ldcg(D.xflag + ch) != 0u);
         }
-        const uint32_t xbf = kCopy ? (xmask >> (js & 31)) & 1u : 1u;
+        const uint32_t xbf = kCopy ? (xmask >> (pos.chunk & 31)) & 1u : 1u;
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
             drain_after_timeout();
@@ -325,99 +417,46 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         }
         {
             const uint8_t *st = base + slot * kStage;
-            const int rb = D.R * 128;
-            const uint8_t *cb = st + 2 * ks * rb;
-            const uint8_t *xb = st + kCodeBytes + 4 * ks * (MP * 128);
-            const uint16_t *sa = reinterpret_cast<const uint16_t *>(st + kCodeBytes + kXBytes) + (ra << (3 + lgS)) + 8 * ks;
-            const uint16_t *sb = sa + (8 << (3 + lgS));
-            // the class index must be a constant for the accumulators to stay
-            // in registers: one call per class and operand type
-#define Q8_TILE_CHUNK(c)                                                          \
-    do {                                                                          \
-        if (kCopy && xbf == 0u)                                                   \
-            chunk_mma<MT, kCopy>(acc[(c) % C], cb, rb, xb, sa, sb, ra, offq, offx, g); \
-        else                                                                      \
-            chunk_mma<MT, false>(acc[(c) % C], cb, rb, xb, sa, sb, ra, offq, offx, g); \
-    } while (0)
-            if constexpr (C == 4) {
-                switch (cls) {
-                    case 0: Q8_TILE_CHUNK(0); break;
-                    case 1: Q8_TILE_CHUNK(1); break;
-                    case 2: Q8_TILE_CHUNK(2); break;
-                    default: Q8_TILE_CHUNK(3); break;
-                }
-            } else if constexpr (C == 2) {
-                if (cls == 0)
-                    Q8_TILE_CHUNK(0);
-                else
-                    Q8_TILE_CHUNK(1);
-            } else {
-                Q8_TILE_CHUNK(0);
-            }
-#undef Q8_TILE_CHUNK
+            const uint8_t *xb = st + kCodeBytes;
+            const uint16_t *sa = reinterpret_cast<const uint16_t *>(st + kCodeBytes + kXBytes) + ra * 8;
+            const uint16_t *sb = sa + 64;
+            if (kCopy && xbf == 0u)
+                chunk_mma<MT, kCopy>(acc, st, kRows * 128, xb, sa, sb, ra, offq, offx, g);
+            else
+                chunk_mma<MT, false>(acc, st, kRows * 128, xb, sa, sb, ra, offq, offx, g);
         }
-        // the item's last stage: add the classes in class order and store y
-        if (pos.chunk + S == D.KC) {
-            const int row0 = (pos.item - D.item_begin) * D.R;
-            float v[MT][4];
-            if (C == 1 || S == 1) {
+        if (pos.chunk + 1 == pos.cend) {
+            // the item's last stage.  A CTA that ran class 0 of the row block
+            // adds the classes as they come; otherwise, or where the row
+            // block goes on in another CTA, the partial goes to the
+            // workspace and the row block's last sharer adds them up
+            const int row0 = pos.row0;
+            const bool prefix = pos.item - c >= ib;
+            const bool last_here = c == D.C - 1 || pos.item == ie - 1;
+            if constexpr (MT == 4) {
+                store_tile<MT>(D, row0, ra, t, M, acc);  // one class: the item is the row block
+            } else if (prefix) {
 #pragma unroll
                 for (int j = 0; j < MT; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float x = acc[0][j][e];
-#pragma unroll
-                        for (int c = 1; c < C; ++c) x += acc[c][j][e];
-                        v[j][e] = x;
-                    }
-                store_tile<MT>(D, row0, ra, t, M, v);
-            } else {
-                // publish the classes this warp owns (c mod S == ks); the last
-                // of the row tile's S warps adds all of them
-#pragma unroll
-                for (int c = 0; c < C; ++c)
-                    if ((c & (S - 1)) == ks)
-#pragma unroll
-                        for (int j = 0; j < MT; ++j)
-                            red[((rt * C + c) * 32 + lane) * MT + j] =
-                                make_float4(acc[c][j][0], acc[c][j][1], acc[c][j][2], acc[c][j][3]);
-                __threadfence_block();
-                __syncwarp();
-                uint32_t prev = 0;
-                if (lane == 0) prev = atomicAdd(&cnt[rt], 1u);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                if (prev == static_cast<uint32_t>(S - 1)) {
-                    __threadfence_block();
-#pragma unroll
-                    for (int j = 0; j < MT; ++j) {
-                        float4 u = red[(rt * C * 32 + lane) * MT + j];
-#pragma unroll
-                        for (int c = 1; c < C; ++c) {
-                            const float4 w = red[((rt * C + c) * 32 + lane) * MT + j];
-                            u.x += w.x;
-                            u.y += w.y;
-                            u.z += w.z;
-                            u.w += w.w;
-                        }
-                        v[j][0] = u.x;
-                        v[j][1] = u.y;
-                        v[j][2] = u.z;
-                        v[j][3] = u.w;
-                    }
-                    store_tile<MT>(D, row0, ra, t, M, v);
-                    __syncwarp();
-                    if (lane == 0) cnt[rt] = 0u;
+                    for (int e = 0; e < 4; ++e) fold[j][e] = c == 0 ? acc[j][e] : fold[j][e] + acc[j][e];
+                if (c == D.C - 1) {
+                    store_tile<MT>(D, row0, ra, t, M, fold);
+                } else if (last_here && p.last_sid[blockIdx.x] >= 0) {
+                    const int sid = p.last_sid[blockIdx.x];
+                    put_part<MT>(part_slot<MT>(p, sid, c, warp), lane, fold);
+                    finish_split<MT>(p, D, sid, warp, lane, row0, ra, t);
                 }
+            } else if (p.first_sid[blockIdx.x] >= 0) {
+                const int sid = p.first_sid[blockIdx.x];
+                put_part<MT>(part_slot<MT>(p, sid, c, warp), lane, acc);
+                if (last_here) finish_split<MT>(p, D, sid, warp, lane, row0, ra, t);
             }
 #pragma unroll
-            for (int c = 0; c < C; ++c)
-#pragma unroll
-                for (int j = 0; j < MT; ++j) acc[c][j][0] = acc[c][j][1] = acc[c][j][2] = acc[c][j][3] = 0.f;
+            for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
         }
-        // release the slot (after the item's partials are read, so that the
-        // next item's cannot overwrite them: items have one stage if S == 1,
-        // at least two otherwise): reads ordered (fence, counter, fence)
-        // before the refill that the last of the 8 warps issues
+        // release the slot: reads ordered (fence, counter, fence) before the
+        // refill that the last of the 8 warps issues
         __syncwarp();
         if (lane == 0) {
             __threadfence_block();
@@ -507,62 +546,121 @@ int g_occ = 0;
 
 template <int MT>
 bool configure(int &occ) {
-    if (cudaFuncSetAttribute(tile_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<MT>()) != cudaSuccess)
+    if (cudaFuncSetAttribute(tile_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes()) != cudaSuccess)
         return false;
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT>, kThreads, smem_bytes<MT>()) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT>, kThreads, smem_bytes()) != cudaSuccess)
         return false;
     occ = std::min(occ, std::max(o, 1));
     return true;
 }
 
+
+// Cuts the item list into `grid` ranges of (nearly) equal bytes and marks
+// the row blocks that two or more ranges share: a split id each, the number
+// of CTAs that share it and the last class of the one that holds class 0.
 template <int MT>
-q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, cudaStream_t stream, bool chained) {
+q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, int max_sids, cudaStream_t stream,
+              bool chained) {
     const int grid = std::min(std::min(items, di->sm_count * g_occ), kMaxGrid);
-    // cut the item list into `grid` ranges of (nearly) equal bytes
     int c = 0;
     double acc = 0.0;
     p.cta_begin[0] = 0;
     for (int i = 0; i < p.count && c < grid - 1; ++i) {
         const TDesc &D = p.d[i];
-        const double per_row = static_cast<double>(D.KC) * kChunk * 1.0625;
         for (int it = 0; it < D.items && c < grid - 1; ++it) {
-            acc += per_row * std::min(D.R, D.N - it * D.R);
+            const int rb = it / D.C, cl = it % D.C;
+            const int rows = std::min(kRows, D.N - rb * kRows);
+            const int chunks = class_lo(D.KC, D.C, cl + 1) - class_lo(D.KC, D.C, cl);
+            acc += static_cast<double>(rows) * chunks * kChunk * 1.0625;
             while (c < grid - 1 && acc >= total_bytes * (c + 1) / grid) p.cta_begin[++c] = D.item_begin + it + 1;
         }
     }
     while (c < grid) p.cta_begin[++c] = items;
+
+    // row block of a global item: its first item, and the matrix's classes
+    int d = 0;
+    const auto block_of = [&](int item, int &first, int &C) {
+        d = 0;
+        while (d + 1 < p.count && item >= p.d[d + 1].item_begin) ++d;
+        C = p.d[d].C;
+        first = item - (item - p.d[d].item_begin) % C;
+    };
+    int nsid = 0, cur_key = -1;
+    const auto sid_of = [&](int key) {
+        if (key != cur_key) {
+            cur_key = key;
+            p.sharers[nsid] = 0;
+            p.pe[nsid] = -1;
+            ++nsid;
+        }
+        return nsid - 1;
+    };
+    for (int i = 0; i < grid; ++i) {
+        p.first_sid[i] = p.last_sid[i] = -1;
+        const int b = p.cta_begin[i], e = p.cta_begin[i + 1];
+        if (e <= b) continue;
+        int kf, cf, kl, cl;
+        block_of(b, kf, cf);
+        block_of(e - 1, kl, cl);
+        if (kf == kl) {
+            if (b == kf && e == kf + cf) continue;  // the whole row block
+            if (nsid >= max_sids && kf != cur_key) return Q8_ERR_WORKSPACE;
+            const int s = sid_of(kf);
+            p.first_sid[i] = p.last_sid[i] = static_cast<int16_t>(s);
+            ++p.sharers[s];
+            if (b == kf) p.pe[s] = static_cast<int8_t>(e - 1 - kf);
+            continue;
+        }
+        if (b > kf) {  // enters its first row block after class 0
+            if (nsid >= max_sids && kf != cur_key) return Q8_ERR_WORKSPACE;
+            const int s = sid_of(kf);
+            p.first_sid[i] = static_cast<int16_t>(s);
+            ++p.sharers[s];
+        }
+        if (e < kl + cl) {  // leaves its last row block before its last class
+            if (nsid >= max_sids && kl != cur_key) return Q8_ERR_WORKSPACE;
+            const int s = sid_of(kl);
+            p.last_sid[i] = static_cast<int16_t>(s);
+            ++p.sharers[s];
+            p.pe[s] = static_cast<int8_t>(e - 1 - kl);
+        }
+    }
     p.early_signal = grid >= di->sm_count * g_occ ? 1 : 0;
-    return launch_kernel(tile_kernel<MT>, dim3(grid), dim3(kThreads), smem_bytes<MT>(), stream, chained, p) ==
+    return launch_kernel(tile_kernel<MT>, dim3(grid), dim3(kThreads), smem_bytes(), stream, chained, p) ==
                    cudaSuccess
                ? Q8_OK
                : Q8_ERR_CUDA;
 }
 
-// Chunks per stage of a matrix with KC chunks in a launch that asks for S:
-// the largest power of two <= S that divides KC and leaves an item at least
-// two stages (the class partials of an item are read before the slot of its
-// last stage is released; two stages keep the next item's from landing first).
-int split_for(int64_t KC, int S) {
-    while (S > 1 && (KC % S != 0 || KC < 2 * S)) S >>= 1;
-    return S;
-}
+size_t up256(int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); }
 
-int log2_of(int S) { return S >= 4 ? 2 : (S >= 2 ? 1 : 0); }
+int mt_for(int M) { return M <= 8 ? 1 : (M <= 16 ? 2 : 4); }
+
+// Split row blocks a call may have: at most one per CTA boundary and one per
+// row block.
+int64_t max_splits(const q8_linear_desc *descs, int count, int M) {
+    if (mt_for(M) == 4) return 0;
+    int64_t rbs = 0;
+    for (int i = 0; i < count; ++i) rbs += (descs[i].N + kRows - 1) / kRows;
+    return std::min<int64_t>(kMaxGrid, rbs);
+}
 
 }  // namespace
 
 bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
 
-namespace {
-size_t up256(int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); }
-}  // namespace
-
-// workspace of one matrix: its x copy, then one flag word per chunk (none
-// where the kernel reads the caller's x)
-size_t tile_x_bytes(int64_t K, int M) {
-    if (!tile_uses_x_copy(M <= 8 ? 1 : (M <= 16 ? 2 : 4))) return 0;
-    return up256(static_cast<int64_t>(M) * K * 2) + up256(K / kChunk * 4);
+size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off, size_t *ticket_bytes) {
+    const int MT = mt_for(M);
+    size_t bytes = 0;
+    if (tile_uses_x_copy(MT))
+        for (int i = 0; i < count; ++i)
+            bytes += up256(static_cast<int64_t>(M) * descs[i].K * 2) + up256(descs[i].K / kChunk * 4);
+    const int64_t ms = max_splits(descs, count, M);
+    if (ticket_off) *ticket_off = bytes;
+    if (ticket_bytes) *ticket_bytes = up256(ms * kWarps * 4);
+    if (ms > 0) bytes += up256(ms * kWarps * 4) + static_cast<size_t>(ms) * kMaxClasses * kWarps * 32 * MT * 16;
+    return bytes;
 }
 
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
@@ -580,53 +678,44 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     }
     static thread_local TParams p;
     static thread_local XParams xp;
-    const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
-    const bool copy = tile_uses_x_copy(MT);
-    if (copy && xws == nullptr) return Q8_ERR_WORKSPACE;
+    const int MT = mt_for(M);
     const int MP = 8 * MT;
-    const int C = 4 / MT;
-    // the fewest chunks per stage that give every SM an item (measured: a
-    // split costs more than the second CTA per SM gains); the results do not
-    // depend on it
-    int S = 1;
-    for (;;) {
-        int64_t n_items = 0;
-        for (int i = 0; i < count; ++i) {
-            const int R = 128 / split_for(descs[i].K / kChunk, S);
-            n_items += (descs[i].N + R - 1) / R;
-        }
-        if (S >= C || n_items >= di->sm_count) break;
-        S *= 2;
-    }
-    int items = 0;
-    double total_bytes = 0.0;
+    const bool copy = tile_uses_x_copy(MT);
+    size_t ticket_off = 0, ticket_bytes = 0;
+    const size_t need = tile_workspace(descs, count, M, &ticket_off, &ticket_bytes);
+    if (need > 0 && xws == nullptr) return Q8_ERR_WORKSPACE;
+    const int64_t ms = max_splits(descs, count, M);
+    p.tickets = ms > 0 ? reinterpret_cast<uint32_t *>(xws + ticket_off) : nullptr;
+    p.parts = ms > 0 ? reinterpret_cast<float4 *>(xws + ticket_off + ticket_bytes) : nullptr;
+
     // x copies: matrix i owns the workspace region after those of 0 .. i-1;
     // a matrix whose x (pointer, row stride, K) an earlier one already has
     // reads that one's copy
     int xcopy[Q8_MAX_BATCH];
-    size_t region[Q8_MAX_BATCH];
     int chunks = 0;
     xp.count = 0;
     xp.M = M;
     size_t off = 0;
     for (int i = 0; i < count && copy; ++i) {
         const q8_linear_desc &d = descs[i];
-        region[i] = off;
-        off += tile_x_bytes(d.K, M);
+        const size_t region = off;
+        off += up256(static_cast<int64_t>(M) * d.K * 2) + up256(d.K / kChunk * 4);
         xcopy[i] = -1;
         for (int j = 0; j < i && xcopy[i] < 0; ++j)
             if (descs[j].x == d.x && descs[j].ldx == d.ldx && descs[j].K == d.K) xcopy[i] = xcopy[j];
         if (xcopy[i] >= 0) continue;
         XJob &J = xp.j[xp.count];
         J.x = d.x;
-        J.xo = reinterpret_cast<uint16_t *>(xws + region[i]);
-        J.flag = reinterpret_cast<uint32_t *>(xws + region[i] + up256(static_cast<int64_t>(M) * d.K * 2));
+        J.xo = reinterpret_cast<uint16_t *>(xws + region);
+        J.flag = reinterpret_cast<uint32_t *>(xws + region + up256(static_cast<int64_t>(M) * d.K * 2));
         J.ldx = d.ldx;
         J.K = d.K;
         J.chunk_begin = chunks;
         chunks += static_cast<int>(d.K / kChunk);
         xcopy[i] = xp.count++;
     }
+    int items = 0;
+    double total_bytes = 0.0;
     for (int i = 0; i < count; ++i) {
         TDesc &D = p.d[i];
         TMaps &T = p.m[i];
@@ -635,29 +724,28 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         const void *xsrc = copy ? static_cast<const void *>(xp.j[xcopy[i]].xo) : static_cast<const void *>(d.x);
         const int64_t xld = copy ? d.K : d.ldx;
         const int64_t KC = d.K / kChunk;
-        const int Sd = split_for(KC, S);
-        const uint32_t R = static_cast<uint32_t>(128 / Sd);
         const uint64_t qdims[3] = {128, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K / 128)};
         const uint64_t qstr[2] = {static_cast<uint64_t>(d.K), 128};
-        const uint32_t qbox[3] = {128, R, static_cast<uint32_t>(2 * Sd)};
+        const uint32_t qbox[3] = {128, kRows, 2};
         const uint64_t xdims[3] = {64, static_cast<uint64_t>(M), static_cast<uint64_t>(d.K / 64)};
         const uint64_t xstr[2] = {static_cast<uint64_t>(xld) * 2, 128};
-        const uint32_t xbox[3] = {64, static_cast<uint32_t>(MP), static_cast<uint32_t>(4 * Sd)};
+        const uint32_t xbox[3] = {64, static_cast<uint32_t>(MP), 4};
         const int64_t nb = d.K / 32;
         if (!encode_tmap(&T.q, 1, d.q, 3, qdims, qstr, qbox, true) ||
             !encode_tmap(&T.x, 2, xsrc, 3, xdims, xstr, xbox, true) ||
             !encode_2d(&T.s, 2, d.s, static_cast<uint64_t>(nb), static_cast<uint64_t>(d.N),
-                       static_cast<uint64_t>(nb) * 2, static_cast<uint32_t>(8 * Sd), R, false))
+                       static_cast<uint64_t>(nb) * 2, 8, kRows, false))
             return Q8_ERR_CUDA;
         D.y = d.y;
         D.xflag = copy ? xp.j[xcopy[i]].flag : nullptr;
         D.ldy = d.ldy;
         D.N = static_cast<int32_t>(d.N);
         D.KC = static_cast<int32_t>(KC);
-        D.lgS = log2_of(Sd);
-        D.R = static_cast<int32_t>(R);
+        D.C = classes_for(KC, MT);
+        for (int c = 0; c <= kMaxClasses; ++c)
+            D.cls[c] = static_cast<int16_t>(c <= D.C ? class_lo(static_cast<int>(KC), D.C, c) : KC);
         D.item_begin = items;
-        D.items = static_cast<int32_t>((d.N + R - 1) / R);
+        D.items = static_cast<int32_t>((d.N + kRows - 1) / kRows) * D.C;
         items += D.items;
         total_bytes += static_cast<double>(d.N) * d.K * 1.0625;
     }
@@ -670,8 +758,10 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     if (copy && launch_kernel(x_copy_kernel, dim3(chunks), dim3(kThreads), 0, stream, chained, xp) != cudaSuccess)
         return Q8_ERR_CUDA;
     const bool dep = copy || chained;
-    if (MT == 1) return run<1>(p, di, items, total_bytes, stream, dep);
-    return MT == 2 ? run<2>(p, di, items, total_bytes, stream, dep) : run<4>(p, di, items, total_bytes, stream, dep);
+    const int msi = static_cast<int>(ms);
+    if (MT == 1) return run<1>(p, di, items, total_bytes, msi, stream, dep);
+    return MT == 2 ? run<2>(p, di, items, total_bytes, msi, stream, dep)
+                   : run<4>(p, di, items, total_bytes, msi, stream, dep);
 }
 
 }  // namespace q8

@@ -247,8 +247,11 @@ q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t
  * 256-byte-rounded flag word per 256 columns of K: each 256-column chunk of
  * x (all M rows) is copied as binary16 where binary16 holds all its values
  * exactly, else as bf16, and the matmul takes the matching operand type.
- * The copies need no zeroing; the words the kernels count with are left
- * zero. */
+ * After the copies come, for M <= 16, the tickets (one 32-byte group each,
+ * 256-byte rounded) and fp32 partials (16 KB x ceil(M / 8) each) of up to
+ * min(320, total 128-row blocks of those matrices) row blocks whose work is
+ * shared between CTAs.  The copies and partials need no zeroing; the words
+ * the kernels count with are left zero. */
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M);
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M);
 

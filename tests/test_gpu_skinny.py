@@ -498,8 +498,14 @@ def test_tile_x_copy_chunks(oracle, N, K, M):
     q, s = weights_dev(qn, sn)
     x = x_dev(xn)
     need = q8.q8_workspace_size(N, K, M)
-    copy_bytes = (M * K * 2 + 255) // 256 * 256
-    tile_bytes = copy_bytes + (KC * 4 + 255) // 256 * 256
+    up = lambda b: (b + 255) // 256 * 256
+    copy_bytes = up(M * K * 2)
+    # after the copy and its flags: the tickets and partials of row blocks
+    # that CTAs share, for at most min(320, row blocks) of them
+    MT = 1 if M <= 8 else 2
+    ms = min(320, (N + 127) // 128)
+    split_bytes = up(ms * 8 * 4) + ms * 4 * 8 * 32 * MT * 16
+    tile_bytes = copy_bytes + up(KC * 4) + split_bytes
     assert need >= tile_bytes
     ws = q8.workspace(need)
     y = q8.q8_gemm_skinny(q, s, x, ws=ws)
