@@ -235,14 +235,17 @@ def test_layer_set_bench_step_sampled(oracle):
 # ---------------------------------------------------------------------------
 # determinism, graph replay, batch == separate calls
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("M", [1, 3, 8, 20])
+@pytest.mark.parametrize("M", [1, 3, 8, 12, 20])
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
     # shapes that the automatic routing sends to different kernels: K = 1536
     # or K % 256 != 0 (pipeline for M <= 8), other K % 256 == 0 (tiles for
     # M >= 2), K > 4096 off the 256 grid and K > 12288 (general)
+    # (the tiles' K classes: 4 at K = 4096, 3 at K = 1536, 2 of 5 chunks at
+    # K = 2560, 1 at K = 256; a lone matrix shares its row blocks between
+    # CTAs, a batch mostly does not)
     shapes = [(4608, 1536), (1536, 1536), (8192, 1536), (1536, 4096), (77, 256),
-              (130, 2080), (300, 4128), (96, 12800)]
+              (130, 2080), (300, 4128), (96, 12800), (300, 2560)]
     mats_np = []
     for i, (N, K) in enumerate(shapes):
         qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"bs{i}"))
@@ -256,8 +259,10 @@ def test_batch_equals_separate_calls_bitwise(oracle, variant, M):
 @pytest.mark.parametrize("M", [4, 12, 24])
 @pytest.mark.parametrize("K", [1536, 4096])
 def test_tile_k_split_keeps_bits(oracle, M, K):
-    """A lone small matrix gets its K split across warps (to fill the GPU);
-    in a launch with many rows it is not.  Its result must not change."""
+    """A lone small matrix has its row blocks' K classes spread over several
+    CTAs (to fill the GPU), so its row blocks are added through the
+    workspace; in a launch with many rows most are not.  Its result must not
+    change."""
     if M <= 8 and K == 1536:
         pytest.skip("served by the pipeline kernel, not the tiles")
     qn, sn, _ = oracle.quantize_rows(synth.weights(1536, K, 0, "ks"))
