@@ -467,6 +467,13 @@ def extra_rows(torch, q8, peak):
             bb = by * nb_
             rows[f"{name}_M{M}_batch{nb_}"] = {"GB/s": round(bb / t / 1e9, 1), "frac": round(bb / t / 1e9 / peak, 3),
                                                "us": round(t * 1e6, 2), "GMAC/s": round(nb_ * M * N * K / t / 1e9, 1)}
+            # the same batch with the batch-invariant arithmetic (rows independent of M)
+            if K % 256 == 0:
+                t = timed([lambda bd=bd, M=M: q8.q8_linear_batch(descs=bd, M=M,
+                                                                 variant=q8.Q8_VARIANT_BATCH_INVARIANT)], reps=5)
+                rows[f"{name}_M{M}_batch{nb_}_invariant"] = {"GB/s": round(bb / t / 1e9, 1),
+                                                             "frac": round(bb / t / 1e9 / peak, 3),
+                                                             "us": round(t * 1e6, 2)}
             del ys, wsb
         del cps
     # prefill-shaped GEMM on tcgen05 (compute-bound: report TFLOP/s)

@@ -182,7 +182,7 @@ namespace {
 q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant, void *ws,
                        size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream, bool chained) {
     if (!descs || count < 0 || count > Q8_MAX_BATCH) return Q8_ERR_ARG;
-    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_MMA) return Q8_ERR_ARG;
+    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_BATCH_INVARIANT) return Q8_ERR_ARG;
     if (M < 0 || M > Q8_SKINNY_MAX_M) return Q8_ERR_SHAPE;
     if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
     // drop empty matrices; check the rest
@@ -191,6 +191,7 @@ q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, in
     for (int i = 0; i < count; ++i) {
         q8_status st = check_desc(descs[i], M);
         if (st != Q8_OK) return st;
+        if (variant == Q8_VARIANT_BATCH_INVARIANT && descs[i].K % 256 != 0) return Q8_ERR_SHAPE;
         if (descs[i].N > 0) live[n++] = descs[i];
     }
     if (M == 0 || n == 0) return Q8_OK;

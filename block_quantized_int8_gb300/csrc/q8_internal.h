@@ -76,8 +76,10 @@ bool tile_k_supported(int64_t K);
 // launches) are [*ticket_off, *ticket_off + *ticket_bytes)
 size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off = nullptr,
                       size_t *ticket_bytes = nullptr);
+// invariant: the batch-invariant arithmetic (bf16 operands, one class, no
+// x copy, any 1 <= M <= 32), which needs no workspace
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
-                      cudaStream_t stream, bool chained = false);
+                      cudaStream_t stream, bool chained = false, bool invariant = false);
 
 // GGUF Q8_0 block repack (q8_gguf.cu): nblocks blocks of 34 bytes (binary16
 // scale, 32 int8 codes) <-> planar codes (32 bytes per block) and scales.

@@ -111,6 +111,7 @@ struct TParams {
     int32_t count;
     int32_t M;
     int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
+    int32_t invariant;     // batch-invariant arithmetic: bf16 operands from the caller's x, one class
     int32_t cta_begin[kMaxGrid + 1];
     int16_t first_sid[kMaxGrid];  // split id of a CTA's first row block, -1 if whole
     int16_t last_sid[kMaxGrid];   // split id of a CTA's last row block, -1 if whole
@@ -403,13 +404,13 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
         const int c = pos.c;
-        if (kCopy && (pos.d != xd || (pos.chunk & ~31) != xbase)) {
+        if (kCopy && !p.invariant && (pos.d != xd || (pos.chunk & ~31) != xbase)) {
             xd = pos.d;
             xbase = pos.chunk & ~31;
             const int ch = xbase + lane;
             xmask = __ballot_sync(0xffffffffu, ch < D.KC && __ldcg(D.xflag + ch) != 0u);
         }
-        const uint32_t xbf = kCopy ? (xmask >> (pos.chunk & 31)) & 1u : 1u;
+        const uint32_t xbf = kCopy && !p.invariant ? (xmask >> (pos.chunk & 31)) & 1u : 1u;
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
             drain_after_timeout();
@@ -664,10 +665,10 @@ size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *tic
 }
 
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
-                      cudaStream_t stream, bool chained) {
+                      cudaStream_t stream, bool chained, bool invariant) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
-    if (M < 2 || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
+    if (M < (invariant ? 1 : 2) || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i)
         if (!tile_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
     if (g_configured_dev != di->device) {
@@ -680,11 +681,13 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     static thread_local XParams xp;
     const int MT = mt_for(M);
     const int MP = 8 * MT;
-    const bool copy = tile_uses_x_copy(MT);
+    // the batch-invariant arithmetic reads the caller's x and keeps one
+    // class per row block (no shared row blocks): no workspace
+    const bool copy = !invariant && tile_uses_x_copy(MT);
     size_t ticket_off = 0, ticket_bytes = 0;
-    const size_t need = tile_workspace(descs, count, M, &ticket_off, &ticket_bytes);
+    const size_t need = invariant ? 0 : tile_workspace(descs, count, M, &ticket_off, &ticket_bytes);
     if (need > 0 && xws == nullptr) return Q8_ERR_WORKSPACE;
-    const int64_t ms = max_splits(descs, count, M);
+    const int64_t ms = invariant ? 0 : max_splits(descs, count, M);
     p.tickets = ms > 0 ? reinterpret_cast<uint32_t *>(xws + ticket_off) : nullptr;
     p.parts = ms > 0 ? reinterpret_cast<float4 *>(xws + ticket_off + ticket_bytes) : nullptr;
 
@@ -741,7 +744,7 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         D.ldy = d.ldy;
         D.N = static_cast<int32_t>(d.N);
         D.KC = static_cast<int32_t>(KC);
-        D.C = classes_for(KC, MT);
+        D.C = invariant ? 1 : classes_for(KC, MT);
         for (int c = 0; c <= kMaxClasses; ++c)
             D.cls[c] = static_cast<int16_t>(c <= D.C ? class_lo(static_cast<int>(KC), D.C, c) : KC);
         D.item_begin = items;
@@ -752,6 +755,7 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     p.status = dev_status;
     p.count = count;
     p.M = M;
+    p.invariant = invariant ? 1 : 0;
     if (items == 0) return Q8_OK;
     // the x copy (waits for the kernels before it when chained), then the
     // tiles as its dependent: their first weight stages load while it runs

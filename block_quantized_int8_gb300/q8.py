@@ -29,7 +29,7 @@ Q8_DEV_SCALE_OVF = 0x2
 Q8_DEV_TIMEOUT = 0x4
 Q8_SKINNY_MAX_M = 32
 Q8_MAX_BATCH = 64
-Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA = 0, 1, 2
+Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA, Q8_VARIANT_BATCH_INVARIANT = 0, 1, 2, 3
 Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_128x64 = 0, 1, 2, 3
 Q8_QUANT_EXACT, Q8_QUANT_FL32 = 0, 1
 
@@ -269,7 +269,7 @@ def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None
     the weights; the variant is then automatic)."""
     if descs is None:
         descs, M = make_descs(mats)
-    need = q8_linear_batch_workspace_size(descs, M)
+    need = 0 if variant == Q8_VARIANT_BATCH_INVARIANT else q8_linear_batch_workspace_size(descs, M)
     if ws is None and need:
         ws = workspace(need)
     nbytes = 0 if ws is None else ws.numel()

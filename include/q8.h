@@ -70,6 +70,18 @@ typedef enum q8_status {
 #define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: TMA-fed warp-MMA tiles (K % 256 == 0, K != 1536) or the warp-MMA pipeline; M > 8: the tiles */
 #define Q8_VARIANT_SIMT 1    /* CUDA-core FFMA: codes dequantised in registers, one FMA per weight per row */
 #define Q8_VARIANT_MMA  2    /* warp mma.sync bf16 on exact bf16 codes, block scale applied in fp32 */
+/* Batch-invariant: row m of Y is the same, bit for bit, for every M in
+ * 1..32 that includes that row (a decode row equals the same row computed
+ * in a batch).  Source: "Frigg" README, Finding 4 (a matmul over one row
+ * is not bit-identical to the same matmul over a batch holding it, so a
+ * decode row could not be compared with a batch row).  Every row takes the
+ * same arithmetic whatever M is: the TMA-fed tile kernel with bf16
+ * operands, exact products, per-block fp32 results times the block scale
+ * added in block order, one sum per row over all of K (a warp MMA computes
+ * each output from its own row only).  K must be a multiple of 256 (else
+ * Q8_ERR_SHAPE); it needs no workspace.  Slower than AUTO where AUTO splits
+ * K or uses binary16 operands. */
+#define Q8_VARIANT_BATCH_INVARIANT 3
 
 /*
  * q8_quantize_rows -- Q8_0-quantize binary32 weights w[rows][K] along K.

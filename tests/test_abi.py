@@ -90,6 +90,10 @@ def test_batch_validation(L):
     assert L.q8_linear_batch(d, 65, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch(None, 1, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch_ex(d, 2, 1, 7, None, 0, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_batch_ex(d, 2, 1, 4, None, 0, None, None) == q8.Q8_ERR_ARG
+    # the batch-invariant variant takes K multiples of 256 only (checked
+    # before anything touches the device)
+    assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_BATCH_INVARIANT, None, 0, None, None) == q8.Q8_ERR_SHAPE
     d[1].K = 48
     assert L.q8_linear_batch(d, 2, 1, None, 0, None, None) == q8.Q8_ERR_SHAPE
     d[1].K = 64

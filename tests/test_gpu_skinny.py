@@ -529,3 +529,42 @@ def test_tile_x_copy_chunks(oracle, N, K, M):
         assert np.array_equal(got_copy[:, cols], want), f"chunk {c}"
     y_ref, B = oracle.matmul(qn, sn, xn, threads=8)
     check_tol(y.cpu().numpy(), y_ref, B, f"x copy N={N} K={K} M={M}")
+
+
+def test_batch_invariant_rows(oracle):
+    """Q8_VARIANT_BATCH_INVARIANT: row m of Y is the same, bit for bit, for
+    every M that includes it, alone or in a batch of matrices, and within
+    the tolerance of the oracle."""
+    from block_quantized_int8_gb300 import q8
+    shapes = [(300, 4096), (1536, 1536), (130, 256), (4100, 2048)]
+    mats = []
+    for i, (N, K) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"inv{i}"))
+        mats.append((qn, sn, synth.activations(32, K, 0, f"invx{i}")))
+    dev_w = [weights_dev(qn, sn) for (qn, sn, _) in mats]
+
+    def run(M, which):
+        outs, ms = [], []
+        for i in which:
+            q, s = dev_w[i]
+            x = x_dev(np.ascontiguousarray(mats[i][2][:M]))
+            y = torch.full((M, q.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+            ms.append((q, s, x, y))
+            outs.append(y)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q8.q8_linear_batch(ms, variant=q8.Q8_VARIANT_BATCH_INVARIANT, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        return [y.cpu().numpy() for y in outs]
+
+    everything = list(range(len(mats)))
+    full = run(32, everything)
+    for i, (qn, sn, xn) in enumerate(mats):
+        y_ref, B = oracle.matmul(qn, sn, xn, threads=8)
+        check_tol(full[i], y_ref, B, f"invariant N={qn.shape[0]} K={qn.shape[1]}")
+    for M in (1, 2, 3, 5, 8, 9, 12, 16, 17, 24, 31):
+        part = run(M, everything)
+        for i in everything:
+            assert np.array_equal(part[i], full[i][:M]), f"matrix {i} at M={M}"
+        (alone,) = run(M, [1])
+        assert np.array_equal(alone, full[1][:M])
