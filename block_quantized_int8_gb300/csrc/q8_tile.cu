@@ -38,6 +38,9 @@
 //    row block is shared between CTAs, each writes its partial (the running
 //    sum through its last class, or single classes) to the workspace and the
 //    last to arrive on the row block's ticket adds them in class order.
+//  * Batch-invariant mode (any 1 <= M <= 32): bf16 operands from the
+//    caller's x and one class, so every row's arithmetic is the same for
+//    every M (a warp MMA computes each output from its own row only).
 // Every wait is bounded (Q8_DEV_TIMEOUT on expiry).
 #include <cuda.h>
 
