@@ -216,3 +216,28 @@ def matmul(q: np.ndarray, s: np.ndarray, x_bf16: np.ndarray, rows=None, threads:
     qs = np.ascontiguousarray(q[rows])
     ss = np.ascontiguousarray(s[rows])
     return matmul(qs, ss, x, None, threads)
+
+
+def matmul_w8a8(q: np.ndarray, s: np.ndarray, x_bf16: np.ndarray):
+    """W8A8 reference: each activation row is Q8_0-quantized by the same rule
+    as the weights (``quantize_rows`` of its binary32 value), then
+    y[m][n] = sum_b s_w[n][b] s_x[m][b] sum_{k in b} q_w[n][k] q_x[m][k].
+    That is the plain dot product of the dequantised weights and the
+    dequantised activations, taken here in binary64 by a library matmul
+    (every product s q is exact in binary64).  Source: "MODEL-BASELINE-
+    RESULTS" (fak), ACT 3 item 1 (weights and activations both in 32-element
+    Q8_0 blocks) and item 3 (the int8 block dot product).  Returns (y, B)
+    with B = sum |w'| |x'| for the tolerance."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    N, K = q.shape
+    if s.shape != (N, K // 32) or x.shape[1] != K:
+        raise ValueError("shape mismatch")
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    qx, sx, _ = quantize_rows(xf)
+    wd = q.astype(np.float64) * np.repeat(f16_to_f64(s), 32, axis=1)
+    xd = qx.astype(np.float64) * np.repeat(f16_to_f64(sx), 32, axis=1)
+    return xd @ wd.T, np.abs(xd) @ np.abs(wd).T

@@ -534,3 +534,44 @@ def test_fl32_blocks_match_exact_arithmetic_and_flags():
             d32 = np.float32(np.max(np.abs(blk)) / np.float32(127.0))
             want = [_half_away_code(_fl32_of_fraction(Fraction(float(v)) / Fraction(float(d32)))) for v in blk]
             assert q[r, 32 * b:32 * b + 32].tolist() == want
+
+
+# ---------------------------------------------------------------------------
+# W8A8 reference
+# ---------------------------------------------------------------------------
+def _bf16_bits(v):
+    return (np.asarray(v, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_w8a8_integer_activations_reduce_to_w8a16(oracle):
+    """Activations that are integers in [-127, 127] with 127 in every block
+    quantize to themselves (scale 1, codes = values), so W8A8 equals the
+    W8A16 reference on them."""
+    rng = np.random.default_rng(7)
+    N, K, M = 37, 128, 3
+    q, s, _ = oracle.quantize_rows(synth.weights(N, K, 0, "w8a8i"))
+    xv = rng.integers(-126, 127, size=(M, K)).astype(np.float32)
+    xv[:, ::32] = 127.0
+    y8, B8 = oracle.matmul_w8a8(q, s, _bf16_bits(xv))
+    y16, B16 = oracle.matmul(q, s, _bf16_bits(xv))
+    assert np.allclose(y8, y16, rtol=1e-13, atol=0)
+    assert np.allclose(B8, B16, rtol=1e-13, atol=0)
+
+
+def test_w8a8_brute_force_exact(oracle):
+    """Tiny random case against exact rational arithmetic written out block
+    by block (each activation block's scale and codes from the Q8_0 rule of
+    its binary32 values): a transposed scale or a wrong block index fails."""
+    N, K, M = 3, 64, 2
+    q, s, _ = oracle.quantize_rows(synth.weights(N, K, 0, "w8a8b"))
+    x = synth.activations(M, K, 0, "w8a8bx")
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    qx, sx, _ = oracle.quantize_rows(xf)
+    y, _ = oracle.matmul_w8a8(q, s, x)
+    f16 = lambda bits: Fraction(float(np.uint16(bits).view(np.float16)))
+    for m in range(M):
+        for n in range(N):
+            exact = sum(f16(s[n, b]) * f16(sx[m, b]) *
+                        sum(int(q[n, k]) * int(qx[m, k]) for k in range(32 * b, 32 * b + 32))
+                        for b in range(K // 32))
+            assert abs(y[m, n] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
