@@ -474,6 +474,15 @@ def extra_rows(torch, q8, peak):
                 rows[f"{name}_M{M}_batch{nb_}_invariant"] = {"GB/s": round(bb / t / 1e9, 1),
                                                              "frac": round(bb / t / 1e9 / peak, 3),
                                                              "us": round(t * 1e6, 2)}
+                # and W8A8 (x quantized to Q8_0 per row, int8 block dots; same bytes counted)
+                ws8 = q8.workspace(int(q8.lib().q8_linear_batch_workspace_size_ex(bd, len(bd), M,
+                                                                                   q8.Q8_VARIANT_W8A8)), dev)
+                t = timed([lambda bd=bd, M=M, ws8=ws8: q8.q8_linear_batch(descs=bd, M=M, ws=ws8,
+                                                                          variant=q8.Q8_VARIANT_W8A8)], reps=5)
+                rows[f"{name}_M{M}_batch{nb_}_w8a8"] = {"GB/s": round(bb / t / 1e9, 1),
+                                                        "frac": round(bb / t / 1e9 / peak, 3),
+                                                        "us": round(t * 1e6, 2)}
+                del ws8
             del ys, wsb
         del cps
     # prefill-shaped GEMM on tcgen05 (compute-bound: report TFLOP/s)

@@ -163,6 +163,19 @@ size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {
     return skinny_workspace(&d, 1, M, &pl, &sched_off);
 }
 
+size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant) {
+    if (variant == Q8_VARIANT_BATCH_INVARIANT) return 0;
+    if (variant != Q8_VARIANT_W8A8) return q8_linear_batch_workspace_size(descs, count, M);
+    if (!descs || count < 1 || count > Q8_MAX_BATCH || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
+    q8_linear_desc tmp[Q8_MAX_BATCH];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+        if (descs[i].N <= 0 || descs[i].K <= 0 || descs[i].K % 256) continue;
+        tmp[n++] = descs[i];
+    }
+    return n > 0 ? tile_workspace(tmp, n, M, nullptr, nullptr, true) : 0;
+}
+
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M) {
     if (!descs || count < 1 || count > Q8_MAX_BATCH || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
     q8_linear_desc tmp[Q8_MAX_BATCH];
@@ -182,7 +195,7 @@ namespace {
 q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant, void *ws,
                        size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream, bool chained) {
     if (!descs || count < 0 || count > Q8_MAX_BATCH) return Q8_ERR_ARG;
-    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_BATCH_INVARIANT) return Q8_ERR_ARG;
+    if (variant < Q8_VARIANT_AUTO || variant > Q8_VARIANT_W8A8) return Q8_ERR_ARG;
     if (M < 0 || M > Q8_SKINNY_MAX_M) return Q8_ERR_SHAPE;
     if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
     // drop empty matrices; check the rest
@@ -191,7 +204,8 @@ q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, in
     for (int i = 0; i < count; ++i) {
         q8_status st = check_desc(descs[i], M);
         if (st != Q8_OK) return st;
-        if (variant == Q8_VARIANT_BATCH_INVARIANT && descs[i].K % 256 != 0) return Q8_ERR_SHAPE;
+        if ((variant == Q8_VARIANT_BATCH_INVARIANT || variant == Q8_VARIANT_W8A8) && descs[i].K % 256 != 0)
+            return Q8_ERR_SHAPE;
         if (descs[i].N > 0) live[n++] = descs[i];
     }
     if (M == 0 || n == 0) return Q8_OK;

@@ -75,11 +75,12 @@ bool tile_k_supported(int64_t K);
 // partials of the row blocks that CTAs share; the tickets (zero between
 // launches) are [*ticket_off, *ticket_off + *ticket_bytes)
 size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off = nullptr,
-                      size_t *ticket_bytes = nullptr);
-// invariant: the batch-invariant arithmetic (bf16 operands, one class, no
-// x copy, any 1 <= M <= 32), which needs no workspace
+                      size_t *ticket_bytes = nullptr, bool w8a8 = false);
+// mode 0: the default arithmetic; 1: batch-invariant (bf16 operands, one
+// class, no x copy, any 1 <= M <= 32, no workspace); 2: W8A8 (x quantized
+// to Q8_0 in the workspace, int8 block dots, any 1 <= M <= 32)
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
-                      cudaStream_t stream, bool chained = false, bool invariant = false);
+                      cudaStream_t stream, bool chained = false, int mode = 0);
 
 // GGUF Q8_0 block repack (q8_gguf.cu): nblocks blocks of 34 bytes (binary16
 // scale, 32 int8 codes) <-> planar codes (32 bytes per block) and scales.

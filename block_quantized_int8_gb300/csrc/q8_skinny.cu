@@ -403,7 +403,8 @@ enum Route { kRouteGemv, kRoutePipe, kRouteTile, kRouteGeneral, kRoutes };
 // best stage shape, the two are within 4 % and a lone matrix takes 8.7 us
 // on the pipeline against 10.7 us on the tiles.)
 Route route_of(int64_t K, int M, int variant) {
-    if (variant == Q8_VARIANT_BATCH_INVARIANT) return kRouteTile;  // every M, K % 256 == 0 (checked)
+    if (variant == Q8_VARIANT_BATCH_INVARIANT || variant == Q8_VARIANT_W8A8)
+        return kRouteTile;  // every M, K % 256 == 0 (checked)
     if (M == 1 && variant != Q8_VARIANT_MMA && gemv_k_supported(K)) return kRouteGemv;
     if (variant == Q8_VARIANT_SIMT) return kRouteGeneral;
     if (M >= 2 && tile_k_supported(K) && (M > 8 || K != 1536)) return kRouteTile;
@@ -454,10 +455,15 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     // enqueued; the general kernel uses the front of it
     SplitPlan plans[Q8_MAX_BATCH];
     size_t sched_off = SIZE_MAX, tile_off = SIZE_MAX;
-    // the batch-invariant arithmetic (tiles only) needs none
-    const size_t need = variant == Q8_VARIANT_BATCH_INVARIANT
-                            ? 0
-                            : skinny_workspace(all, all_count, M, plans, &sched_off, &tile_off);
+    // the batch-invariant arithmetic (tiles only) needs none; W8A8 (tiles
+    // only) needs the tile kernel's, from the start of the workspace
+    size_t need = 0;
+    if (variant == Q8_VARIANT_W8A8) {
+        need = tile_workspace(all, all_count, M, nullptr, nullptr, true);
+        tile_off = 0;
+    } else if (variant != Q8_VARIANT_BATCH_INVARIANT) {
+        need = skinny_workspace(all, all_count, M, plans, &sched_off, &tile_off);
+    }
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return Q8_ERR_ALIGN;
     const q8_linear_desc *descs = part[kRouteGeneral];
@@ -476,8 +482,8 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     }
     if (n[kRouteTile] > 0) {
         uint8_t *xws = tile_off == SIZE_MAX ? nullptr : static_cast<uint8_t *>(ws) + tile_off;
-        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, xws, dev_status, stream, chained,
-                                         variant == Q8_VARIANT_BATCH_INVARIANT);
+        const int mode = variant == Q8_VARIANT_BATCH_INVARIANT ? 1 : (variant == Q8_VARIANT_W8A8 ? 2 : 0);
+        const q8_status st = launch_tile(part[kRouteTile], n[kRouteTile], M, xws, dev_status, stream, chained, mode);
         if (st != Q8_OK) return st;
     }
     if (count == 0) return Q8_OK;

@@ -65,6 +65,15 @@ constexpr int kCodeBytes = kRows * kChunk;  // codes of a stage
 constexpr int kXBytes = 16384;              // x of a stage: MP rows x 256 bf16, MP <= 32
 constexpr int kScaleBytes = kRows * 16;     // block scales of a stage: 128 rows x 8
 constexpr int kStage = kCodeBytes + kXBytes + kScaleBytes;  // a multiple of 1024
+// W8A8: per chunk of 256, x row m's codes are 9 blocks of 32 (the 9th zero,
+// which spreads the rows over the shared-memory banks) and its scales 9
+// binary16; a chunk's MP rows are contiguous, so a stage's x is two bulk
+// copies (codes at the start of the x region, scales at kW8ScaleOff)
+constexpr int kW8Blocks = 9;
+constexpr int kW8Row = kW8Blocks * 32;
+constexpr int kW8ScaleOff = 32 * kW8Row;
+static_assert(kW8ScaleOff + 32 * kW8Blocks * 2 <= kXBytes, "W8A8 x of a stage exceeds its region");
+enum TileMode { kModeDefault = 0, kModeInvariant = 1, kModeW8A8 = 2 };
 // shared memory of tile_kernel: alignment slack, ring, barriers and counters
 constexpr int smem_bytes() { return 1024 + kSlots * kStage + 128; }
 static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
@@ -92,7 +101,7 @@ struct TMaps {
 
 struct TDesc {
     float *y;
-    const uint32_t *xflag;  // per chunk: 0 = x copy is binary16, 1 = bf16
+    const uint32_t *xflag;  // per chunk: 0 = x copy is binary16, 1 = bf16; W8A8: the x codes
     int64_t ldy;
     int32_t N;
     int32_t KC;          // chunks per row, K / 256
@@ -114,7 +123,8 @@ struct TParams {
     int32_t count;
     int32_t M;
     int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
-    int32_t invariant;     // batch-invariant arithmetic: bf16 operands from the caller's x, one class
+    int32_t mode;          // TileMode: batch-invariant (bf16 operands from the caller's x, one
+                           // class) or W8A8 (x quantized to Q8_0, integer block dots)
     int32_t cta_begin[kMaxGrid + 1];
     int16_t first_sid[kMaxGrid];  // split id of a CTA's first row block, -1 if whole
     int16_t last_sid[kMaxGrid];   // split id of a CTA's last row block, -1 if whole
@@ -145,6 +155,19 @@ __device__ __forceinline__ int find_tdesc(const TParams &p, int item) {
     int d = 0;
     while (d + 1 < p.count && item >= p.d[d + 1].item_begin) ++d;
     return d;
+}
+
+// D = A B on int8: A 16 x 32 (row), B 32 x 8 (column), int32 out.
+// Fragments: a0 / a1 rows g / g + 8 at k = 4t..4t+3, a2 / a3 the same rows at
+// k = 16 + 4t..; b0 / b1 column g at k = 4t.. and 16 + 4t..; d0 d1 row g,
+// columns 2t, 2t + 1, d2 d3 row g + 8.
+__device__ __forceinline__ void mma_s8_16832(int &d0, int &d1, int &d2, int &d3, uint32_t a0, uint32_t a1,
+                                             uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
 }
 
 // Position in a CTA's sequence of stages: descriptor, item, the chunk of
@@ -222,6 +245,37 @@ __device__ __forceinline__ void chunk_mma(float (&a)[MT][4], const uint8_t *cb, 
             a[j][1] = fmaf(s_a, d1, a[j][1]);
             a[j][2] = fmaf(s_b, d2, a[j][2]);
             a[j][3] = fmaf(s_b, d3, a[j][3]);
+        }
+    }
+}
+
+// W8A8: one chunk of a warp's 16-row tile against Q8_0 x.  Lane (g, t)
+// holds bytes 8t..8t+7 of each 32-code block of its weight rows and of x row
+// 8j + g; both operands use them as k = 4t..4t+3 and 16+4t..16+4t+3, so one
+// int8 MMA gives the exact block dot, scaled by s_w s_x (exact in fp32).
+//   xq: the chunk's x codes [MP][9 x 32]; xs: its scales [MP][9]
+template <int MT>
+__device__ __forceinline__ void chunk_mma_w8a8(float (&a)[MT][4], const uint8_t *cb, int rb, const uint8_t *xq,
+                                               const uint16_t *xs, const uint16_t *sa, const uint16_t *sb, int ra,
+                                               const uint32_t (&offq)[4], int g, int t) {
+#pragma unroll
+    for (int bl = 0; bl < kChunk / 32; ++bl) {
+        const uint8_t *cbox = cb + (bl >> 2) * rb;
+        const uint2 wa = *reinterpret_cast<const uint2 *>(cbox + ra * 128 + offq[bl & 3]);
+        const uint2 wb = *reinterpret_cast<const uint2 *>(cbox + (ra + 8) * 128 + offq[bl & 3]);
+        const float s_a = f16_bits_to_f32(sa[bl]);
+        const float s_b = f16_bits_to_f32(sb[bl]);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+            const uint2 xa = *reinterpret_cast<const uint2 *>(xq + (8 * j + g) * kW8Row + bl * 32 + 8 * t);
+            int d0, d1, d2, d3;
+            mma_s8_16832(d0, d1, d2, d3, wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
+            const float x0 = f16_bits_to_f32(xs[(8 * j + 2 * t) * kW8Blocks + bl]);
+            const float x1 = f16_bits_to_f32(xs[(8 * j + 2 * t + 1) * kW8Blocks + bl]);
+            a[j][0] = fmaf(s_a * x0, static_cast<float>(d0), a[j][0]);
+            a[j][1] = fmaf(s_a * x1, static_cast<float>(d1), a[j][1]);
+            a[j][2] = fmaf(s_b * x0, static_cast<float>(d2), a[j][2]);
+            a[j][3] = fmaf(s_b * x1, static_cast<float>(d3), a[j][3]);
         }
     }
 }
@@ -344,9 +398,21 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
 
     // stage k at position pos: all bytes announced on the slot's barrier,
     // then the weight boxes and (unless deferred) the x box
+    // x bytes of a stage: the TMA box, or for W8A8 the chunk's codes and scales
+    const uint32_t xbytes = p.mode == kModeW8A8 ? MP * (kW8Row + 2 * kW8Blocks) : MP * 512;
     auto issue_x = [&](int k, const Pos &pos) {
         const int slot = k % kSlots;
-        tma_3d(base + slot * kStage + kCodeBytes, &p.m[pos.d].x, 0, 0, 4 * pos.chunk, &full[slot]);
+        uint8_t *dst = base + slot * kStage + kCodeBytes;
+        if (p.mode == kModeW8A8) {
+            const TDesc &D = p.d[pos.d];
+            const uint8_t *xq = reinterpret_cast<const uint8_t *>(D.xflag);
+            const uint8_t *xs = xq + static_cast<size_t>(D.KC) * MP * kW8Row;
+            bulk_g2s(dst, xq + static_cast<size_t>(pos.chunk) * MP * kW8Row, MP * kW8Row, &full[slot]);
+            bulk_g2s(dst + kW8ScaleOff, xs + static_cast<size_t>(pos.chunk) * MP * kW8Blocks * 2, MP * kW8Blocks * 2,
+                     &full[slot]);
+        } else {
+            tma_3d(dst, &p.m[pos.d].x, 0, 0, 4 * pos.chunk, &full[slot]);
+        }
     };
     auto issue = [&](int k, const Pos &pos, bool with_x) {
         const int slot = k % kSlots;
@@ -354,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const TMaps &T = p.m[pos.d];
         uint8_t *st = base + slot * kStage;
         const int row0 = pos.row0;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + MP * 512 + kScaleBytes));
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + kScaleBytes) + xbytes);
         tma_3d(st, &T.q, 0, row0, 2 * pos.chunk, &full[slot]);
         tma_2d(st + kCodeBytes + kXBytes, &T.s, 8 * pos.chunk, row0, &full[slot]);
         if (with_x) issue_x(k, pos);
@@ -407,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const int slot = k % kSlots;
         const TDesc &D = p.d[pos.d];
         const int c = pos.c;
-        if (kCopy && !p.invariant && (pos.d != xd || (pos.chunk & ~31) != xbase)) {
+        if (kCopy && p.mode == kModeDefault && (pos.d != xd || (pos.chunk & ~31) != xbase)) {
             xd = pos.d;
             xbase = pos.chunk & ~31;
             const int ch = xbase + lane;
             xmask = __ballot_sync(0xffffffffu, ch < D.KC && __ldcg(D.xflag + ch) != 0u);
         }
-        const uint32_t xbf = kCopy && !p.invariant ? (xmask >> (pos.chunk & 31)) & 1u : 1u;
+        const uint32_t xbf = kCopy && p.mode == kModeDefault ? (xmask >> (pos.chunk & 31)) & 1u : 1u;
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
             drain_after_timeout();
@@ -424,7 +490,10 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             const uint8_t *xb = st + kCodeBytes;
             const uint16_t *sa = reinterpret_cast<const uint16_t *>(st + kCodeBytes + kXBytes) + ra * 8;
             const uint16_t *sb = sa + 64;
-            if (kCopy && xbf == 0u)
+            if (p.mode == kModeW8A8)
+                chunk_mma_w8a8<MT>(acc, st, kRows * 128, xb,
+                                   reinterpret_cast<const uint16_t *>(xb + kW8ScaleOff), sa, sb, ra, offq, g, t);
+            else if (kCopy && xbf == 0u)
                 chunk_mma<MT, kCopy>(acc, st, kRows * 128, xb, sa, sb, ra, offq, offx, g);
             else
                 chunk_mma<MT, false>(acc, st, kRows * 128, xb, sa, sb, ra, offq, offx, g);
@@ -486,6 +555,8 @@ struct XJob {
     const uint16_t *x;    // bf16 bits [M][ldx]
     uint16_t *xo;         // copy [M][K], binary16 or bf16 bits per chunk
     uint32_t *flag;       // [K / 256]: 0 = binary16, 1 = bf16
+    float *xf;            // W8A8: x as binary32 in the chunk-major block order of xq
+    int8_t *xq;           // W8A8: codes [K / 256][MP][9 x 32], then scales [K / 256][MP][9]
     int64_t ldx;
     int64_t K;
     int32_t chunk_begin;  // first CTA of this x
@@ -543,6 +614,24 @@ __global__ void __launch_bounds__(kThreads) x_copy_kernel(const __grid_constant_
         }
     }
     if (threadIdx.x == 0) J.flag[c] = keep ? 1u : 0u;
+}
+
+// W8A8: x as binary32 blocks in the order the quantizer turns into the
+// stage layout -- for chunk c, row m < MP, block b < 9: x[m][256 c + 32 b ..]
+// (zero past M and in the ninth block).  One CTA per chunk of one x.
+__global__ void __launch_bounds__(kThreads) w8a8_widen_kernel(const __grid_constant__ XParams p, int MP) {
+    int j = 0;
+    while (j + 1 < p.count && static_cast<int>(blockIdx.x) >= p.j[j + 1].chunk_begin) ++j;
+    const XJob &J = p.j[j];
+    const int c = static_cast<int>(blockIdx.x) - J.chunk_begin;
+    pdl_wait_prior();
+    float *out = J.xf + static_cast<size_t>(c) * MP * kW8Row;
+    for (int i = threadIdx.x; i < MP * kW8Row; i += kThreads) {
+        const int m = i / kW8Row, e = i - m * kW8Row;
+        float v = 0.f;
+        if (m < p.M && e < kChunk) v = __uint_as_float(static_cast<uint32_t>(J.x[m * J.ldx + c * kChunk + e]) << 16);
+        out[i] = v;
+    }
 }
 
 int g_configured_dev = -1;
@@ -650,16 +739,24 @@ int64_t max_splits(const q8_linear_desc *descs, int count, int M) {
     return std::min<int64_t>(kMaxGrid, rbs);
 }
 
+// workspace of one matrix's x: the binary16 copy and its flags (M <= 16),
+// or for W8A8 the binary32 blocks, then the codes and scales of x
+size_t tile_x_region(int64_t K, int M, bool w8a8) {
+    const int64_t KC = K / kChunk, MP = 8 * mt_for(M);
+    if (w8a8) return up256(KC * MP * kW8Row * 4) + up256(KC * MP * (kW8Row + 2 * kW8Blocks));
+    if (!tile_uses_x_copy(mt_for(M))) return 0;
+    return up256(static_cast<int64_t>(M) * K * 2) + up256(KC * 4);
+}
+
 }  // namespace
 
 bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
 
-size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off, size_t *ticket_bytes) {
+size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off, size_t *ticket_bytes,
+                      bool w8a8) {
     const int MT = mt_for(M);
     size_t bytes = 0;
-    if (tile_uses_x_copy(MT))
-        for (int i = 0; i < count; ++i)
-            bytes += up256(static_cast<int64_t>(M) * descs[i].K * 2) + up256(descs[i].K / kChunk * 4);
+    for (int i = 0; i < count; ++i) bytes += tile_x_region(descs[i].K, M, w8a8);
     const int64_t ms = max_splits(descs, count, M);
     if (ticket_off) *ticket_off = bytes;
     if (ticket_bytes) *ticket_bytes = up256(ms * kWarps * 4);
@@ -668,10 +765,11 @@ size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *tic
 }
 
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
-                      cudaStream_t stream, bool chained, bool invariant) {
+                      cudaStream_t stream, bool chained, int mode) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
-    if (M < (invariant ? 1 : 2) || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
+    const bool invariant = mode == kModeInvariant, w8 = mode == kModeW8A8;
+    if (M < (mode != kModeDefault ? 1 : 2) || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i)
         if (!tile_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
     if (g_configured_dev != di->device) {
@@ -686,9 +784,9 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     const int MP = 8 * MT;
     // the batch-invariant arithmetic reads the caller's x and keeps one
     // class per row block (no shared row blocks): no workspace
-    const bool copy = !invariant && tile_uses_x_copy(MT);
+    const bool copy = mode == kModeDefault && tile_uses_x_copy(MT);
     size_t ticket_off = 0, ticket_bytes = 0;
-    const size_t need = invariant ? 0 : tile_workspace(descs, count, M, &ticket_off, &ticket_bytes);
+    const size_t need = invariant ? 0 : tile_workspace(descs, count, M, &ticket_off, &ticket_bytes, w8);
     if (need > 0 && xws == nullptr) return Q8_ERR_WORKSPACE;
     const int64_t ms = invariant ? 0 : max_splits(descs, count, M);
     p.tickets = ms > 0 ? reinterpret_cast<uint32_t *>(xws + ticket_off) : nullptr;
@@ -702,10 +800,10 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     xp.count = 0;
     xp.M = M;
     size_t off = 0;
-    for (int i = 0; i < count && copy; ++i) {
+    for (int i = 0; i < count && (copy || w8); ++i) {
         const q8_linear_desc &d = descs[i];
         const size_t region = off;
-        off += up256(static_cast<int64_t>(M) * d.K * 2) + up256(d.K / kChunk * 4);
+        off += tile_x_region(d.K, M, w8);
         xcopy[i] = -1;
         for (int j = 0; j < i && xcopy[i] < 0; ++j)
             if (descs[j].x == d.x && descs[j].ldx == d.ldx && descs[j].K == d.K) xcopy[i] = xcopy[j];
@@ -714,6 +812,8 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         J.x = d.x;
         J.xo = reinterpret_cast<uint16_t *>(xws + region);
         J.flag = reinterpret_cast<uint32_t *>(xws + region + up256(static_cast<int64_t>(M) * d.K * 2));
+        J.xf = reinterpret_cast<float *>(xws + region);
+        J.xq = reinterpret_cast<int8_t *>(xws + region + up256(d.K / kChunk * MP * kW8Row * 4));
         J.ldx = d.ldx;
         J.K = d.K;
         J.chunk_begin = chunks;
@@ -743,7 +843,9 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
                        static_cast<uint64_t>(nb) * 2, 8, kRows, false))
             return Q8_ERR_CUDA;
         D.y = d.y;
-        D.xflag = copy ? xp.j[xcopy[i]].flag : nullptr;
+        D.xflag = copy ? xp.j[xcopy[i]].flag
+                  : w8 ? reinterpret_cast<const uint32_t *>(xp.j[xcopy[i]].xq)
+                       : nullptr;
         D.ldy = d.ldy;
         D.N = static_cast<int32_t>(d.N);
         D.KC = static_cast<int32_t>(KC);
@@ -758,12 +860,25 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     p.status = dev_status;
     p.count = count;
     p.M = M;
-    p.invariant = invariant ? 1 : 0;
+    p.mode = mode;
     if (items == 0) return Q8_OK;
     // the x copy (waits for the kernels before it when chained), then the
     // tiles as its dependent: their first weight stages load while it runs
     if (copy && launch_kernel(x_copy_kernel, dim3(chunks), dim3(kThreads), 0, stream, chained, xp) != cudaSuccess)
         return Q8_ERR_CUDA;
+    if (w8) {
+        // x to binary32 blocks, then the Q8_0 quantizer over them (codes and
+        // scales land in the stage layout); the tile kernel follows in order
+        w8a8_widen_kernel<<<chunks, kThreads, 0, stream>>>(xp, MP);
+        if (cudaGetLastError() != cudaSuccess) return Q8_ERR_CUDA;
+        for (int j = 0; j < xp.count; ++j) {
+            const XJob &J = xp.j[j];
+            const int64_t rows = J.K / kChunk * MP;
+            const q8_status st = launch_quantize(J.xf, rows, kW8Row, J.xq, reinterpret_cast<uint16_t *>(J.xq + rows * kW8Row),
+                                                 dev_status, stream);
+            if (st != Q8_OK) return st;
+        }
+    }
     const bool dep = copy || chained;
     const int msi = static_cast<int>(ms);
     if (MT == 1) return run<1>(p, di, items, total_bytes, msi, stream, dep);

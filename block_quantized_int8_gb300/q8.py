@@ -29,12 +29,12 @@ Q8_DEV_SCALE_OVF = 0x2
 Q8_DEV_TIMEOUT = 0x4
 Q8_SKINNY_MAX_M = 32
 Q8_MAX_BATCH = 64
-Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA, Q8_VARIANT_BATCH_INVARIANT = 0, 1, 2, 3
+Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA, Q8_VARIANT_BATCH_INVARIANT, Q8_VARIANT_W8A8 = 0, 1, 2, 3, 4
 Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_128x64 = 0, 1, 2, 3
 Q8_QUANT_EXACT, Q8_QUANT_FL32 = 0, 1
 
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
-           "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_gemm", "q8_status_str",
+           "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_linear_batch_workspace_size_ex", "q8_gemm", "q8_status_str",
            "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex", "q8_gguf_to_planar",
            "q8_planar_to_gguf", "q8_quantize_rows_ex", "q8_selftest_wait_timeout",
            "q8_stream_read", "q8_stream_read_out_words")
@@ -75,6 +75,8 @@ def lib():
         L.q8_workspace_size.restype = SZ
         L.q8_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32, I32]
         L.q8_linear_batch_workspace_size.restype = SZ
+        L.q8_linear_batch_workspace_size_ex.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, I32]
+        L.q8_linear_batch_workspace_size_ex.restype = SZ
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, U32P, P]
         L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
@@ -269,7 +271,7 @@ def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None
     the weights; the variant is then automatic)."""
     if descs is None:
         descs, M = make_descs(mats)
-    need = 0 if variant == Q8_VARIANT_BATCH_INVARIANT else q8_linear_batch_workspace_size(descs, M)
+    need = int(lib().q8_linear_batch_workspace_size_ex(descs, len(descs), M, variant))
     if ws is None and need:
         ws = workspace(need)
     nbytes = 0 if ws is None else ws.numel()

@@ -82,6 +82,18 @@ typedef enum q8_status {
  * Q8_ERR_SHAPE); it needs no workspace.  Slower than AUTO where AUTO splits
  * K or uses binary16 operands. */
 #define Q8_VARIANT_BATCH_INVARIANT 3
+/* W8A8: each activation row is quantized to Q8_0 by the weights' rule (the
+ * A1 quantizer of its binary32 values), then y = sum over blocks of
+ * s_w * s_x * (exact int8 block dot), one warp int8 MMA per block and 8
+ * rows.  Source: "MODEL-BASELINE-RESULTS" (fak), ACT 3 items 1 and 3
+ * (weights and activations in Q8_0 blocks, integer block dots).  Accuracy
+ * against the W8A8 definition as for the other variants (2e-3 * sum |w' x'|
+ * + 1e-6, x' the dequantised activations); against the bf16 activations it
+ * adds the activations' quantization error.  K must be a multiple of 256
+ * (else Q8_ERR_SHAPE); workspace: q8_linear_batch_workspace_size_ex(...,
+ * Q8_VARIANT_W8A8) bytes (the binary32 blocks, codes and scales of each
+ * distinct x, and the tile kernel's shared-row-block area). */
+#define Q8_VARIANT_W8A8 4
 
 /*
  * q8_quantize_rows -- Q8_0-quantize binary32 weights w[rows][K] along K.
@@ -266,6 +278,9 @@ q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t
  * the kernels count with are left zero. */
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M);
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M);
+/* The workspace of q8_linear_batch_ex with `variant` (the W8A8 variant needs
+ * its own; the batch-invariant one none; the others as above). */
+size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant);
 
 /*
  * q8_gemm -- prefill-shaped Y[M][N] = X[M][K] * W^T for M > 32 on the 5th

@@ -90,10 +90,19 @@ def test_batch_validation(L):
     assert L.q8_linear_batch(d, 65, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch(None, 1, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch_ex(d, 2, 1, 7, None, 0, None, None) == q8.Q8_ERR_ARG
-    assert L.q8_linear_batch_ex(d, 2, 1, 4, None, 0, None, None) == q8.Q8_ERR_ARG
     # the batch-invariant variant takes K multiples of 256 only (checked
     # before anything touches the device)
     assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_BATCH_INVARIANT, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_W8A8, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_linear_batch_ex(d, 2, 3, 5, None, 0, None, None) == q8.Q8_ERR_ARG
+    # workspace by variant: none for batch-invariant; W8A8 holds x as binary32
+    # blocks, codes and scales (per 256-wide chunk and 8-row group: 9 blocks)
+    w = (q8.LinearDesc * 1)()
+    w[0] = q8.LinearDesc(A, A, A, A, 1536, 4096, 4096, 1536)
+    assert L.q8_linear_batch_workspace_size_ex(w, 1, 4, q8.Q8_VARIANT_BATCH_INVARIANT) == 0
+    assert L.q8_linear_batch_workspace_size_ex(w, 1, 4, 0) == L.q8_linear_batch_workspace_size(w, 1, 4)
+    w8 = L.q8_linear_batch_workspace_size_ex(w, 1, 4, q8.Q8_VARIANT_W8A8)
+    assert w8 >= 16 * 8 * 288 * 4 + 16 * 8 * (288 + 18) and w8 % 256 == 0
     d[1].K = 48
     assert L.q8_linear_batch(d, 2, 1, None, 0, None, None) == q8.Q8_ERR_SHAPE
     d[1].K = 64

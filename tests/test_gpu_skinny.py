@@ -568,3 +568,50 @@ def test_batch_invariant_rows(oracle):
             assert np.array_equal(part[i], full[i][:M]), f"matrix {i} at M={M}"
         (alone,) = run(M, [1])
         assert np.array_equal(alone, full[1][:M])
+
+
+def _w8a8_run(mats_np, M):
+    from block_quantized_int8_gb300 import q8
+    mats, outs = [], []
+    for (qn, sn, xn) in mats_np:
+        q, s = weights_dev(qn, sn)
+        y = torch.full((M, qn.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+        mats.append((q, s, x_dev(np.ascontiguousarray(xn)), y))
+        outs.append(y)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8.q8_linear_batch(mats, variant=q8.Q8_VARIANT_W8A8, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return [y.cpu().numpy() for y in outs]
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 12, 16, 32])
+def test_w8a8_tolerance_and_batch(oracle, M):
+    """W8A8 (activations quantized to Q8_0 per row, int8 block dots) against
+    the oracle's W8A8 definition; a batch gives the same bits as separate calls."""
+    shapes = [(300, 4096), (1536, 1536), (130, 256), (4100, 2048)]
+    mats = []
+    for i, (N, K) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"w8{i}"))
+        mats.append((qn, sn, synth.activations(M, K, 0, f"w8x{i}.{M}")))
+    together = _w8a8_run(mats, M)
+    for m_np, y in zip(mats, together):
+        y_ref, B = oracle.matmul_w8a8(*m_np)
+        check_tol(y, y_ref, B, f"W8A8 N={m_np[0].shape[0]} K={m_np[0].shape[1]} M={M}")
+        (alone,) = _w8a8_run([m_np], M)
+        assert np.array_equal(alone, y)
+
+
+def test_w8a8_exact_case(oracle):
+    """Integer activations with 127 in every block quantize to themselves;
+    with small codes and power-of-two weight scales every sum is exact in
+    fp32, so the kernel matches the W8A8 definition bit for bit."""
+    N, K, M = 300, 1536, 9
+    q, s, _ = synth.exact_case(N, K, M, 0, "w8ex")
+    rng = np.random.default_rng(11)
+    xv = rng.integers(-126, 127, size=(M, K)).astype(np.float32)
+    xv[:, ::32] = 127.0
+    xb = (xv.view(np.uint32) >> 16).astype(np.uint16)
+    (y,) = _w8a8_run([(q, s, xb)], M)
+    y_ref, _ = oracle.matmul_w8a8(q, s, xb)
+    assert np.array_equal(y.astype(np.float64), y_ref)
