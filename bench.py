@@ -38,8 +38,7 @@ import synth  # noqa: E402
 METRIC = "Q8_0 W8A16 decode GEMV achieved HBM GB/s and % of GB300 peak, M=1..32"
 WORKLOAD = ("decode layer set: 16 layers x 8 passes, M=1, Q8_0 weights "
             "K1536->N4608 (QKV), 1536->1536 (o_proj), 1536->8192 (gate+up), 4096->1536 (down)")
-KERNEL_SOURCES = ["block_quantized_int8_gb300/csrc/q8_gemv.cu", "block_quantized_int8_gb300/csrc/q8_dev.cuh"]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_kernel_layer_set.md")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def log(*a):
@@ -66,27 +65,61 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def profile_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+def profile_traffic(kernel="gemv_kernel"):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu record
+    (profiles/traffic.json), if it was taken on the current kernel sources;
+    else None.  Returns (bytes or None, the sources' sha256)."""
     try:
-        txt = open(PROFILE_SUMMARY).read()
-    except OSError:
+        rec = json.load(open(PROFILE_JSON))[kernel]
+    except (OSError, ValueError, KeyError):
         return None, None
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, p), "rb").read())
-    vals = {}
-    for line in txt.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
-            k, v = line.strip().split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256") != h.hexdigest():
+    for p in rec.get("sources", []):
+        try:
+            h.update(open(os.path.join(ROOT, p), "rb").read())
+        except OSError:
+            return None, None
+    if rec.get("source_sha256") != h.hexdigest():
         return None, h.hexdigest()
     try:
-        return int(vals["traffic_bytes_per_launch"]), h.hexdigest()
-    except (KeyError, ValueError):
+        return int(rec["traffic_bytes_per_launch"]), h.hexdigest()
+    except (KeyError, ValueError, TypeError):
         return None, h.hexdigest()
+
+
+def gpu_temperature(index):
+    """GPU temperature (deg C) read with an nvidia-smi query, or None."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=temperature.gpu",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+        return float(out.stdout.strip().splitlines()[0])
+    except Exception:
+        return None
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or the machine type."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def spread(vals):
+    """Median, 10th and 90th percentile of a list (linear interpolation)."""
+    a = np.asarray(vals, dtype=np.float64)
+    return float(np.median(a)), float(np.percentile(a, 10)), float(np.percentile(a, 90))
 
 
 # ---------------------------------------------------------------------------
@@ -269,6 +302,8 @@ def ceilings(torch, q8, nbytes=2 << 30, reps=5):
 
 
 def time_steps(torch, fn, steps, warmup):
+    """Seconds for `steps` calls of fn, one CUDA event pair on the launching
+    stream around all of them (after `warmup` untimed calls)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -282,6 +317,26 @@ def time_steps(torch, fn, steps, warmup):
     e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / 1e3
+
+
+def time_blocks(torch, fn, steps, nblocks=20):
+    """Times `steps` calls of fn as min(nblocks, steps) consecutive blocks of
+    (nearly) equal size, with a CUDA event on the launching stream between
+    blocks.  Returns (seconds from the first event to the last, list of
+    seconds per step of each block)."""
+    nb = max(1, min(nblocks, steps))
+    sizes = [steps // nb + (1 if i < steps % nb else 0) for i in range(nb)]
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i, n in enumerate(sizes):
+        for _ in range(n):
+            fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = [evs[i].elapsed_time(evs[i + 1]) / 1e3 / sizes[i] for i in range(nb)]
+    return evs[0].elapsed_time(evs[-1]) / 1e3, per_step
 
 
 def per_launch_ms(torch, ls, reps, variant=0):
@@ -371,9 +426,12 @@ def extra_rows(torch, q8, peak):
     rows = {}
     L2 = 129 * 2**20
 
-    def timed(fn_list, reps=3):
-        """Mean seconds per call: the calls are captured once into a CUDA graph
-        (so host launch overhead is not measured) and the graph is replayed."""
+    def timed(fn_list, reps=20):
+        """Seconds per call: the calls are captured once into a CUDA graph (so
+        host launch overhead is not measured) and the graph is replayed
+        `reps` times, each replay between its own pair of CUDA events.
+        Returns the median replay's time per call; the 10th and 90th
+        percentiles go to spread_of[0]."""
         for f in fn_list:
             f()
         torch.cuda.synchronize()
@@ -383,14 +441,27 @@ def extra_rows(torch, q8, peak):
                 f()
         g.replay()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in evs:
+            e0.record()
             g.replay()
-        e1.record()
+            e1.record()
         torch.cuda.synchronize()
         del g
-        return e0.elapsed_time(e1) / 1e3 / (reps * len(fn_list))
+        med, p10, p90 = spread([a.elapsed_time(b) / 1e3 / len(fn_list) for a, b in evs])
+        spread_of[0] = (p10, p90)
+        return med
+
+    spread_of = [(0.0, 0.0)]
+
+    def row(nbytes, t, **extra):
+        """A context row: GB/s of `nbytes` per call at the median time t,
+        and the replays' 10th / 90th percentile times."""
+        p10, p90 = spread_of[0]
+        r = {"GB/s": round(nbytes / t / 1e9, 1), "frac": round(nbytes / t / 1e9 / peak, 3),
+             "us": round(t * 1e6, 2), "us_p10": round(p10 * 1e6, 2), "us_p90": round(p90 * 1e6, 2)}
+        r.update(extra)
+        return r
 
     def copies_for(nbytes):
         return max(1, int(np.ceil(4 * L2 / nbytes)))
@@ -402,29 +473,25 @@ def extra_rows(torch, q8, peak):
     yv = torch.empty((1, N), dtype=torch.float32, device=dev)
     by = matmul_bytes(N, K, 1)
     for v, name in ((1, "simt"), (2, "mma")):
-        t = timed([lambda v=v: q8.q8_linear_batch([(wq, ws_, xv, yv)], variant=v)], reps=20)
-        rows[f"vocab_gemv_M1_{name}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
-                                         "us": round(t * 1e6, 2)}
+        t = timed([lambda v=v: q8.q8_linear_batch([(wq, ws_, xv, yv)], variant=v)])
+        rows[f"vocab_gemv_M1_{name}"] = row(by, t)
     # the quantizer creating that matrix (bandwidth figure: 4 B in, 1.0625 B out per weight)
     wf = torch.from_numpy(synth.weights(N, K, 0, "vocab")).to(dev)
     qb, sb = torch.empty_like(wq), torch.empty_like(ws_)
-    t = timed([lambda: q8.q8_quantize_rows(wf, qb, sb)], reps=5)
-    qbytes = N * K * 4 + N * K + N * K // 16
-    rows["quantize_262144x1536"] = {"GB/s": round(qbytes / t / 1e9, 1), "frac": round(qbytes / t / 1e9 / peak, 3),
-                                    "us": round(t * 1e6, 2)}
+    t = timed([lambda: q8.q8_quantize_rows(wf, qb, sb)])
+    rows["quantize_262144x1536"] = row(N * K * 4 + N * K + N * K // 16, t)
     # GGUF Q8_0 ingest of that matrix (34 B in, 34 B out per block) and export
     raw = q8.q8_planar_to_gguf(wq, ws_)
-    t = timed([lambda: q8.q8_gguf_to_planar(raw, N, K, qb, sb)], reps=5)
     gbytes = 2 * raw.numel()
-    rows["gguf_ingest_262144x1536"] = {"GB/s": round(gbytes / t / 1e9, 1), "frac": round(gbytes / t / 1e9 / peak, 3),
-                                       "us": round(t * 1e6, 2)}
-    t = timed([lambda: q8.q8_planar_to_gguf(wq, ws_, raw)], reps=5)
-    rows["gguf_export_262144x1536"] = {"GB/s": round(gbytes / t / 1e9, 1), "frac": round(gbytes / t / 1e9 / peak, 3),
-                                       "us": round(t * 1e6, 2)}
+    t = timed([lambda: q8.q8_gguf_to_planar(raw, N, K, qb, sb)])
+    rows["gguf_ingest_262144x1536"] = row(gbytes, t)
+    t = timed([lambda: q8.q8_planar_to_gguf(wq, ws_, raw)])
+    rows["gguf_export_262144x1536"] = row(gbytes, t)
     del raw
     wsmall = torch.from_numpy(synth.quant_stress_rows()).to(dev)
     t = timed([lambda: q8.q8_quantize_rows(wsmall)], reps=50)
-    rows["quantize_32x4096"] = {"us": round(t * 1e6, 2)}
+    rows["quantize_32x4096"] = {"us": round(t * 1e6, 2), "us_p10": round(spread_of[0][0] * 1e6, 2),
+                                "us_p90": round(spread_of[0][1] * 1e6, 2)}
     del wf, qb, sb, wq, ws_
 
     # tiny GEMV and the M sweep, rotating over distinct weight copies
@@ -446,42 +513,35 @@ def extra_rows(torch, q8, peak):
                 ws = q8.workspace(q8.q8_linear_batch_workspace_size(descs[0], M), dev)
                 fns = [lambda d=d, v=v, M=M, ws=ws: q8.q8_linear_batch(descs=d, M=M, ws=ws, variant=v)
                        for d in descs]
-                t = timed(fns, reps=3)
-                rows[f"{name}_M{M}_{vn}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
-                                             "us": round(t * 1e6, 2), "GMAC/s": round(M * N * K / t / 1e9, 1)}
+                t = timed(fns)
+                rows[f"{name}_M{M}_{vn}"] = row(by, t, **{"GMAC/s": round(M * N * K / t / 1e9, 1)})
             # the copies as separate calls (default kernels), plain and chained:
             # a decode step of one call per matrix, weights fixed
             descs = [q8.make_descs([(q, s, x, y)])[0] for (q, s) in cps]
             wsc = q8.workspace(q8.q8_linear_batch_workspace_size(descs[0], M), dev)
             for ch, cn in ((False, "calls"), (True, "chained_calls")):
                 fns = [lambda d=d, M=M, ch=ch: q8.q8_linear_batch(descs=d, M=M, ws=wsc, chained=ch) for d in descs]
-                t = timed(fns, reps=3)
-                rows[f"{name}_M{M}_{cn}"] = {"GB/s": round(by / t / 1e9, 1), "frac": round(by / t / 1e9 / peak, 3),
-                                             "us": round(t * 1e6, 2)}
+                t = timed(fns)
+                rows[f"{name}_M{M}_{cn}"] = row(by, t)
             # steady state: the distinct copies as ONE batched launch (default kernels)
             nb_ = min(len(cps), q8.Q8_MAX_BATCH)
             ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(nb_)]
             bd, _ = q8.make_descs([(cps[i][0], cps[i][1], x, ys[i]) for i in range(nb_)])
             wsb = q8.workspace(q8.q8_linear_batch_workspace_size(bd, M), dev)
-            t = timed([lambda bd=bd, M=M, wsb=wsb: q8.q8_linear_batch(descs=bd, M=M, ws=wsb)], reps=5)
+            t = timed([lambda bd=bd, M=M, wsb=wsb: q8.q8_linear_batch(descs=bd, M=M, ws=wsb)])
             bb = by * nb_
-            rows[f"{name}_M{M}_batch{nb_}"] = {"GB/s": round(bb / t / 1e9, 1), "frac": round(bb / t / 1e9 / peak, 3),
-                                               "us": round(t * 1e6, 2), "GMAC/s": round(nb_ * M * N * K / t / 1e9, 1)}
+            rows[f"{name}_M{M}_batch{nb_}"] = row(bb, t, **{"GMAC/s": round(nb_ * M * N * K / t / 1e9, 1)})
             # the same batch with the batch-invariant arithmetic (rows independent of M)
             if K % 256 == 0:
                 t = timed([lambda bd=bd, M=M: q8.q8_linear_batch(descs=bd, M=M,
-                                                                 variant=q8.Q8_VARIANT_BATCH_INVARIANT)], reps=5)
-                rows[f"{name}_M{M}_batch{nb_}_invariant"] = {"GB/s": round(bb / t / 1e9, 1),
-                                                             "frac": round(bb / t / 1e9 / peak, 3),
-                                                             "us": round(t * 1e6, 2)}
+                                                                 variant=q8.Q8_VARIANT_BATCH_INVARIANT)])
+                rows[f"{name}_M{M}_batch{nb_}_invariant"] = row(bb, t)
                 # and W8A8 (x quantized to Q8_0 per row, int8 block dots; same bytes counted)
                 ws8 = q8.workspace(int(q8.lib().q8_linear_batch_workspace_size_ex(bd, len(bd), M,
                                                                                    q8.Q8_VARIANT_W8A8)), dev)
                 t = timed([lambda bd=bd, M=M, ws8=ws8: q8.q8_linear_batch(descs=bd, M=M, ws=ws8,
-                                                                          variant=q8.Q8_VARIANT_W8A8)], reps=5)
-                rows[f"{name}_M{M}_batch{nb_}_w8a8"] = {"GB/s": round(bb / t / 1e9, 1),
-                                                        "frac": round(bb / t / 1e9 / peak, 3),
-                                                        "us": round(t * 1e6, 2)}
+                                                                          variant=q8.Q8_VARIANT_W8A8)])
+                rows[f"{name}_M{M}_batch{nb_}_w8a8"] = row(bb, t)
                 del ws8
             del ys, wsb
         del cps
@@ -495,9 +555,10 @@ def extra_rows(torch, q8, peak):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         t = timed([lambda q0=q0, s0=s0, x=x, y=y: q8.q8_gemm(q0, s0, x, y)], reps=50)
         tf = 2.0 * M * N * K / t / 1e12
-        rows[f"prefill_gemm_M{M}_K{K}_N{N}"] = {"TFLOP/s": round(tf, 1), "frac": round(tf / tpk, 4),
-                                                "us": round(t * 1e6, 2),
-                                                "GB/s": round(matmul_bytes(N, K, M, 2) / t / 1e9, 1)}
+        rows[f"prefill_gemm_M{M}_K{K}_N{N}"] = {
+            "TFLOP/s": round(tf, 1), "frac": round(tf / tpk, 4), "us": round(t * 1e6, 2),
+            "us_p10": round(spread_of[0][0] * 1e6, 2), "us_p90": round(spread_of[0][1] * 1e6, 2),
+            "GB/s": round(matmul_bytes(N, K, M, 2) / t / 1e9, 1)}
     torch.cuda.empty_cache()
     return rows
 
@@ -505,14 +566,15 @@ def extra_rows(torch, q8, peak):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reported baseline, and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample(budget_s=12.0):
+def oracle_sample(budget_s=12.0, threads=None):
     """Time the oracle on the decode layer set (weights already quantized, as on
     the GPU side), matrix by matrix and pass by pass, until about `budget_s`
-    seconds of CPU work are spent.  Returns (GB/s of algorithmic bytes, cores,
-    sample text)."""
+    seconds of CPU work are spent, on `threads` host threads (all cores if
+    None; the oracle splits output rows over threads with identical bits).
+    Returns (GB/s of algorithmic bytes, threads, sample text)."""
     import oracle
     oracle.build()
-    cores = os.cpu_count() or 1
+    cores = threads or (os.cpu_count() or 1)
     done_bytes = 0
     spent = 0.0
     n_mats = 0
@@ -540,7 +602,7 @@ def oracle_sample(budget_s=12.0):
     return (done_bytes / spent / 1e9, cores,
             f"oracle (binary64 dequantise-then-dot) on the first {n_mats} of the layer set's "
             f"{synth.LAYERS * synth.PASSES * len(synth.LAYER_MATRICES)} matmuls (weights pre-quantized), "
-            f"{spent:.1f} s on {cores} threads")
+            f"{spent:.1f} s on {cores} thread{'s' if cores > 1 else ''}")
 
 
 def reference_arm(args, rank, world):
@@ -698,7 +760,9 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    dt = time_steps(torch, fn, args.steps, 0)
+    temp_start = gpu_temperature(local_rank)
+    dt, block_step_s = time_blocks(torch, fn, args.steps)
+    temp_end = gpu_temperature(local_rank)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -734,7 +798,12 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu:
         v, cores, sample = oracle_sample()
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        v1, _, sample1 = oracle_sample(budget_s=8.0, threads=1)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "cpu_model": cpu_model(),
+               "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1, "sample": sample1}}
+    blk_gbs = [bytes_step / t / 1e9 for t in block_step_s]
+    med, p10, p90 = spread(blk_gbs)
 
     if rank == 0:
         line = {
@@ -764,6 +833,11 @@ def main():
             "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": ls.launches_per_step * args.steps,
             "clocks": clocks,
+            "timing": {"blocks": len(block_step_s), "steps_per_block": round(args.steps / len(block_step_s), 3),
+                       "unit": "GB/s (rank 0, per block)", "median": round(med, 2), "p10": round(p10, 2),
+                       "p90": round(p90, 2), "gpu_temp_c_start": temp_start, "gpu_temp_c_end": temp_end,
+                       "note": "the timed steps in consecutive blocks, a CUDA event between blocks on the "
+                               "launching stream; value = all bytes / first-to-last event time"},
             "frac_of_peak": round(value / world / peak, 4),
             "rows": rows,
         }

@@ -28,7 +28,7 @@ const DeviceInfo *device_info() {
     return g_ok[dev] ? &g_info[dev] : nullptr;
 }
 
-static q8_status check_arch(const DeviceInfo **out) {
+q8_status check_arch(const DeviceInfo **out) {
     const DeviceInfo *di = device_info();
     if (!di) return Q8_ERR_CUDA;
     if (di->cc_major != 10 || di->cc_minor != 3) return Q8_ERR_ARCH;

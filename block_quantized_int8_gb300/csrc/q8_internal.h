@@ -19,6 +19,9 @@ struct DeviceInfo {
 
 // Cached properties of the current device; nullptr if a CUDA call failed.
 const DeviceInfo *device_info();
+// The current device's properties, if it is compute capability 10.3:
+// Q8_ERR_CUDA if they cannot be read, Q8_ERR_ARCH for another device.
+q8_status check_arch(const DeviceInfo **out);
 
 // ---- quantizer --------------------------------------------------------------
 // mode: Q8_QUANT_EXACT (codes from the stored scale) or Q8_QUANT_FL32.

@@ -30,19 +30,20 @@ constexpr size_t kNoAllocScratchBytes = Q8_NOALLOC_SCRATCH_BYTES;  // 4 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
+std::mutex g_mu;
 void *g_addr[kMaxDevices];
-cudaError_t g_err[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) by the first call made on it.  Make that
-// first call outside any CUDA stream capture.
+// Device address of the scratch on device `dev`, which must be current.  The
+// first successful lookup on a device is kept for later calls; a failed one
+// (for example one made during a stream capture) is not kept, so the next
+// call tries again.  The lookup may load the library's device code, which is
+// why the first call on a device belongs outside any stream capture.
 void *scratch_address(int dev) {
-    std::call_once(g_once[dev], [dev]() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_addr[dev] == nullptr) {
         void *p = nullptr;
-        g_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_addr[dev] = (g_err[dev] == cudaSuccess) ? p : nullptr;
-    });
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) g_addr[dev] = p;
+    }
     return g_addr[dev];
 }
 
@@ -56,7 +57,7 @@ extern "C" q8_status q8_gemm_skinny_noalloc(const int8_t *q, const uint16_t *s, 
                                             const uint16_t *x, int64_t ldx, int32_t M, float *y, int64_t ldy,
                                             uint32_t *dev_status, q8_stream_t stream) {
     // same argument rules as q8_gemm_skinny, plus the scratch limit, all
-    // checked before any CUDA call
+    // checked on the host before any CUDA call
     q8_linear_desc d{};
     d.q = q;
     d.s = s;
@@ -73,9 +74,13 @@ extern "C" q8_status q8_gemm_skinny_noalloc(const int8_t *q, const uint16_t *s, 
     const size_t need = q8_workspace_size(N, K, M);
     if (need > kNoAllocScratchBytes) return Q8_ERR_WORKSPACE;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return Q8_ERR_CUDA;
-    void *ws = scratch_address(dev);
+    // the device check comes before anything is queued: a call that fails
+    // it enqueues nothing
+    const DeviceInfo *di = nullptr;
+    st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    if (di->device < 0 || di->device >= kMaxDevices) return Q8_ERR_CUDA;
+    void *ws = scratch_address(di->device);
     if (ws == nullptr) return Q8_ERR_CUDA;
 
     if (need > 0) {

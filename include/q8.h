@@ -330,8 +330,12 @@ q8_status q8_gemm_ex(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
  *   the library until the process exits.  A shape whose scratch need
  *   (q8_workspace_size(N, K, M)) exceeds it returns Q8_ERR_WORKSPACE before
  *   any CUDA call.  Nothing is allocated or freed.
- *   The first call on a device looks the array's device address up (once per
- *   device, with that device current): make it outside any stream capture.
+ *   The first call on a device looks the array's device address up (with
+ *   that device current) and keeps it for later calls: make that first call
+ *   outside any stream capture (a lookup that fails is not kept, and the
+ *   next call tries again).  cudaDeviceReset() makes the kept address stale:
+ *   after resetting a device, do not call this entry point on it again in
+ *   the same process.
  *   All calls on a device share the array: calls whose kernels may overlap on
  *   the GPU (unordered streams) race on it; calls ordered on one stream do
  *   not.  Each call clears the ticket words it needs before its kernel runs.

@@ -615,3 +615,68 @@ def test_w8a8_exact_case(oracle):
     (y,) = _w8a8_run([(q, s, xb)], M)
     y_ref, _ = oracle.matmul_w8a8(q, s, xb)
     assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def _small_scale_activations(M, K, tag):
+    """bf16 bits [M][K]: N(0, 1) draws times one magnitude per 32-block,
+    cycling over 2^-8 .. 2^-24, 0 and 1, so that blocks get normal,
+    binary16-subnormal and zero activation scales (amax / 127 below 2^-14
+    is subnormal in binary16, below 2^-25 it rounds to zero)."""
+    g = synth.normal_f32((M, K), 0, tag).astype(np.float64)
+    mags = np.array([2.0 ** -8, 2.0 ** -12, 2.0 ** -16, 2.0 ** -20, 2.0 ** -24, 0.0, 1.0])
+    blk = np.arange(K) // 32
+    pick = (blk[None, :] + np.arange(M)[:, None]) % len(mags)
+    return synth.f32_to_bf16_bits((g * mags[pick]).astype(np.float32))
+
+
+@pytest.mark.parametrize("N,K,M,kind", [(300, 1536, 3, "normal"), (130, 4096, 12, "wide"),
+                                        (96, 2048, 32, "wide"), (200, 1024, 8, "small"),
+                                        (77, 2560, 17, "small")])
+def test_w8a8_activation_codes_bit_exact(oracle, N, K, M, kind):
+    """The W8A8 variant quantizes each activation row to Q8_0 in the
+    workspace with the weights' quantizer.  Read back, the codes and binary16
+    scales equal the oracle's quantize_rows of the binary32 activations bit
+    for bit, rows past M and each chunk's ninth (padding) block are zero, and
+    the device status equals the oracle's flags (wide-range rows hold blocks
+    whose scale overflows binary16).  Layout of the region: binary32 blocks
+    [K/256][MP][9 x 32], then codes [K/256][MP][9 x 32] and scales
+    [K/256][MP][9], MP = M rounded up to 8, 16 or 32.  The result then
+    satisfies the tolerance against the oracle's W8A8 reference."""
+    from block_quantized_int8_gb300 import q8
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"w8q{N}.{K}"))
+    if kind == "normal":
+        xn = synth.activations(M, K, 0, f"w8qx{M}.{K}")
+    elif kind == "wide":
+        xn = synth.wide_range_activations(M, K, 0, f"w8qw{M}.{K}")
+    else:
+        xn = _small_scale_activations(M, K, f"w8qs{M}.{K}")
+    xf = synth.bf16_bits_to_f32(xn)
+    qx, sx, flags = oracle.quantize_rows(xf)
+    if kind == "small":
+        sxf = oracle.f16_to_f64(sx)
+        assert (sxf == 0).any() and ((sxf > 0) & (sxf < 2.0 ** -14)).any() and (sxf >= 2.0 ** -14).any()
+    q, s = weights_dev(qn, sn)
+    x = x_dev(xn)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    descs, _ = q8.make_descs([(q, s, x, y)])
+    need = int(q8.lib().q8_linear_batch_workspace_size_ex(descs, 1, M, q8.Q8_VARIANT_W8A8))
+    ws = q8.workspace(need)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8.q8_linear_batch(descs=descs, M=M, ws=ws, variant=q8.Q8_VARIANT_W8A8, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == flags
+    KC = K // 256
+    MP = 8 if M <= 8 else (16 if M <= 16 else 32)
+    up = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    w = ws.cpu().numpy()
+    off = up(KC * MP * 288 * 4)
+    got_q = w[off:off + KC * MP * 288].view(np.int8).reshape(KC, MP, 9, 32)
+    got_s = w[off + KC * MP * 288:off + KC * MP * 288 + KC * MP * 9 * 2].view(np.uint16).reshape(KC, MP, 9)
+    want_q = np.zeros((KC, MP, 9, 32), np.int8)
+    want_q[:, :M, :8, :] = qx.reshape(M, KC, 8, 32).transpose(1, 0, 2, 3)
+    want_s = np.zeros((KC, MP, 9), np.uint16)
+    want_s[:, :M, :8] = sx.reshape(M, KC, 8).transpose(1, 0, 2)
+    assert np.array_equal(got_s, want_s)
+    assert np.array_equal(got_q, want_q)
+    y_ref, B = oracle.matmul_w8a8(qn, sn, xn)
+    check_tol(y.cpu().numpy(), y_ref, B, f"W8A8 {kind} N={N} K={K} M={M}")
