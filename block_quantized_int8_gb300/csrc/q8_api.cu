@@ -256,13 +256,14 @@ q8_status q8_gemv(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, cons
 
 q8_status q8_gemm(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
                   int32_t M, uint16_t *y, int64_t ldy, uint32_t *dev_status, q8_stream_t stream) {
-    return q8_gemm_ex(q, s, N, K, x, ldx, M, y, ldy, Q8_GEMM_TILE_AUTO, dev_status, stream);
+    return q8_gemm_ex(q, s, N, K, x, ldx, M, y, ldy, Q8_GEMM_TILE_AUTO, 0, dev_status, stream);
 }
 
 q8_status q8_gemm_ex(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
-                     int32_t M, uint16_t *y, int64_t ldy, int32_t tile, uint32_t *dev_status,
+                     int32_t M, uint16_t *y, int64_t ldy, int32_t tile, int32_t splits, uint32_t *dev_status,
                      q8_stream_t stream) {
-    if (tile < Q8_GEMM_TILE_AUTO || tile > Q8_GEMM_TILE_128x64) return Q8_ERR_ARG;
+    if (tile < Q8_GEMM_TILE_AUTO || tile > Q8_GEMM_TILE_64x128) return Q8_ERR_ARG;
+    if (splits < 0 || splits > Q8_GEMM_MAX_SPLITS) return Q8_ERR_ARG;
     q8_status st = check_weights(q, s, N, K);
     if (st != Q8_OK) return st;
     if (M < 0) return Q8_ERR_SHAPE;
@@ -274,7 +275,8 @@ q8_status q8_gemm_ex(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, c
     const DeviceInfo *di;
     st = check_arch(&di);
     if (st != Q8_OK) return st;
-    return launch_gemm_tc(q, s, N, K, x, ldx, M, y, ldy, tile, dev_status, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_tc(q, s, N, K, x, ldx, M, y, ldy, tile, splits, dev_status,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

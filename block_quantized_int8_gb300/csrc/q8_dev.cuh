@@ -34,6 +34,13 @@ __device__ __forceinline__ float4 ldg_stream_f4(const void *p) {
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
     return v;
 }
+// A 2-byte read-only load that allocates in L1 (neighbouring scales of the
+// same row are read by the following k-tiles).
+__device__ __forceinline__ uint32_t ldg_nc_u16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint32_t ldg_stream_u16(const void *p) {
     unsigned short v;
     asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -107,6 +114,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Zero, computed from every lane's v: an instruction that cannot issue
+// before the loads that produced v have returned their data in all lanes of
+// the warp.  A warp that hands a shared-memory stage back to an async-proxy
+// writer (a bulk or tensor copy) right after reading it must make the release
+// depend on its loaded values this way: a release that only followed the
+// load instructions in program order let the next copy overwrite the stage
+// before the loads had read it (measured: codes of the stage's next fill
+// turned up in the product).  `zero` must be 0 at run time but unknown to the
+// compiler (a kernel argument): masking with a literal 0 is folded away.
+__device__ __forceinline__ uint32_t warp_loaded_zero(uint32_t v, uint32_t zero) {
+    return __reduce_or_sync(0xFFFFFFFFu, v & zero);
+}
 
 // 1-D bulk copy global -> shared, completing `bytes` on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.

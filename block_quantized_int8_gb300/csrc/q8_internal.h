@@ -143,6 +143,6 @@ q8_status check_skinny_args(const q8_linear_desc &d, int32_t M);
 // ---- prefill GEMM (M > 32) ----------------------------------------------------
 q8_status launch_gemm_tc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                          const uint16_t *x, int64_t ldx, int32_t M, uint16_t *y, int64_t ldy, int32_t tile,
-                         uint32_t *dev_status, cudaStream_t stream);
+                         int32_t splits, uint32_t *dev_status, cudaStream_t stream);
 
 }  // namespace q8

@@ -30,7 +30,8 @@ Q8_DEV_TIMEOUT = 0x4
 Q8_SKINNY_MAX_M = 32
 Q8_MAX_BATCH = 64
 Q8_VARIANT_AUTO, Q8_VARIANT_SIMT, Q8_VARIANT_MMA, Q8_VARIANT_BATCH_INVARIANT, Q8_VARIANT_W8A8 = 0, 1, 2, 3, 4
-Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_128x64 = 0, 1, 2, 3
+Q8_GEMM_TILE_AUTO, Q8_GEMM_TILE_256x128, Q8_GEMM_TILE_128x128, Q8_GEMM_TILE_64x128 = 0, 1, 2, 3
+Q8_GEMM_MAX_SPLITS = 8
 Q8_QUANT_EXACT, Q8_QUANT_FL32 = 0, 1
 
 EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "q8_linear_batch_ex",
@@ -78,7 +79,7 @@ def lib():
         L.q8_linear_batch_workspace_size_ex.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, I32]
         L.q8_linear_batch_workspace_size_ex.restype = SZ
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
-        L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, U32P, P]
+        L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, I32, U32P, P]
         L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_gguf_to_planar.argtypes = [P, I64, I64, P, P, P]
         L.q8_planar_to_gguf.argtypes = [P, P, I64, I64, P, P]
@@ -285,16 +286,17 @@ def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None
     _check(st, "q8_linear_batch")
 
 
-def q8_gemm(q, s, x, y=None, dev_status=None, stream=None, tile=0):
+def q8_gemm(q, s, x, y=None, dev_status=None, stream=None, tile=0, splits=0):
     """y[M, N] (bf16) = x[M, K] @ dequant(q, s)^T for M > 32 (tcgen05 path);
-    `tile` is one of the Q8_GEMM_TILE_* shapes (0: automatic)."""
+    `tile` is one of the Q8_GEMM_TILE_* shapes and `splits` the number of
+    CTAs sharing a tile's K range (0: automatic for either)."""
     _cuda(q, "q", (torch.int8,), 2)
     _cuda(x, "x", _B16, 2)
     N, K = q.shape
     M = x.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=q.device)
-    st = lib().q8_gemm_ex(_p(q), _p(s), N, K, _p(x), x.stride(0), M, _p(y), y.stride(0), int(tile),
+    st = lib().q8_gemm_ex(_p(q), _p(s), N, K, _p(x), x.stride(0), M, _p(y), y.stride(0), int(tile), int(splits),
                           _p(dev_status), _stream(stream))
     _check(st, "q8_gemm")
     return y

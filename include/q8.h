@@ -284,38 +284,51 @@ size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t co
 
 /*
  * q8_gemm -- prefill-shaped Y[M][N] = X[M][K] * W^T for M > 32 on the 5th
- * generation tensor cores (tcgen05): each weight tile is dequantised to bf16
- * (bf16(s*q), round to nearest even) in shared memory and multiplied in bf16
- * with fp32 accumulation in tensor memory; y is bf16 (round to nearest even).
+ * generation tensor cores (tcgen05): each weight is dequantised to bf16
+ * (bf16(s*q): the product is exact in binary32, then one round to nearest
+ * even) into shared memory and multiplied in bf16 with fp32 accumulation in
+ * tensor memory; y is bf16 (round to nearest even).  Any M, N and K (K a
+ * positive multiple of 32).
  * Source: "MODEL-BASELINE-RESULTS" (fak), ACT 4 (batched prefill GEMM that
  * reads each weight once for all tokens) and "Parity lane" item 2.
- *   x : bf16 bits [M][ldx]; y : bf16 bits [M][ldy]; ldx, ldy multiples of 8.
+ *   x : bf16 bits [M][ldx]; y : bf16 bits [M][ldy]; ldx, ldy multiples of 8;
+ *   x and y 16-byte aligned.
  * Accuracy: |y - y_ref| <= 2e-3 * sum_k |s*q*x| + 1e-6 + half a bf16 ulp of y_ref
- * on the tested workloads (the bf16 weight tile rounds each weight by up to
- * 2^-9 relative; see the design notes).
+ * on the tested workloads (the bf16 weights round each weight by up to 2^-9
+ * relative).  Needs no workspace: when K is split over several CTAs (short N,
+ * long K), the partial sums meet in the CTAs' shared memory.
  */
 q8_status q8_gemm(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                   const uint16_t *x, int64_t ldx, int32_t M,
                   uint16_t *y, int64_t ldy,
                   uint32_t *dev_status, q8_stream_t stream);
 
-/* Tile shapes of q8_gemm (the _ex entry point): one CTA per SM computes
- * 2 x 128 rows of x against 128 weight rows (each dequantised weight tile
- * serves both 128-row halves), 128 x 128, or 128 x 64 (short N). */
-#define Q8_GEMM_TILE_AUTO     0   /* the first of the three that fills most SMs */
+/* Tile shapes of q8_gemm_ex: one CTA per SM computes a tile of (rows of x)
+ * x (weight rows). */
+#define Q8_GEMM_TILE_AUTO     0   /* the tile and split with the shortest modelled time */
 #define Q8_GEMM_TILE_256x128  1
 #define Q8_GEMM_TILE_128x128  2
-#define Q8_GEMM_TILE_128x64   3
+#define Q8_GEMM_TILE_64x128   3
+#define Q8_GEMM_MAX_SPLITS    8   /* most CTAs that share one tile's K range */
 
 /*
- * q8_gemm_ex -- q8_gemm with an explicit tile shape (Q8_GEMM_TILE_*).  Every
- * shape computes the same values bit for bit (each output is one fp32 sum
- * over K in k order); the choice only changes speed.  Unknown `tile`:
- * Q8_ERR_ARG.
+ * q8_gemm_ex -- q8_gemm with an explicit tile shape (Q8_GEMM_TILE_*) and K
+ * split (1 .. Q8_GEMM_MAX_SPLITS, 0 = automatic).  With split S the S CTAs
+ * of a tile (one thread-block cluster) sum consecutive ranges of K (whole
+ * groups of 256) and their S partial sums are added in range order, so each
+ * output is the same bit for bit for every tile shape with the same S, and
+ * from run to run.  CTAs that work on the same rows of x (neighbouring weight tiles)
+ * share each x tile through a TMA multicast in groups of 1, 2, 4 or 8 (one
+ * thread-block cluster); the group is chosen with the tile and split, and
+ * the environment variable Q8_GEMM_MULTICAST (1, 2, 4 or 8) asks for one
+ * for measurement (ignored where no allowed shape has it) -- it never
+ * changes the results.  Unknown `tile` or `splits`
+ * out of range: Q8_ERR_ARG; a shape this device cannot co-schedule (or more
+ * splits than groups of 256 in K): Q8_ERR_UNSUPPORTED.
  */
 q8_status q8_gemm_ex(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                      const uint16_t *x, int64_t ldx, int32_t M,
-                     uint16_t *y, int64_t ldy, int32_t tile,
+                     uint16_t *y, int64_t ldy, int32_t tile, int32_t splits,
                      uint32_t *dev_status, q8_stream_t stream);
 
 /*
@@ -351,7 +364,7 @@ const char *q8_status_str(q8_status st);
 
 /* ABI version of this header (bumped on any signature change). */
 int32_t q8_abi_version(void);
-#define Q8_ABI_VERSION 1
+#define Q8_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

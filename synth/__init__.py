@@ -222,6 +222,18 @@ def exact_case(N: int, K: int, M: int, seed: int = 0, tag: str = "exact"):
     return q, s, x
 
 
+def chunk_select_x(M: int, K: int, shift: int = 0, width: int = 8) -> np.ndarray:
+    """bf16 bits [M][K]: token m is 1 on the `width` consecutive k of chunk
+    (m + shift) mod (K / width) and 0 elsewhere, so each output reads exactly
+    one chunk of one weight row (a stale or early-overwritten weight stage
+    shows up in the outputs of the tokens that read it)."""
+    x = np.zeros((M, K), dtype=np.float32)
+    chunk = (np.arange(M) + shift) % (K // width)
+    for m in range(M):
+        x[m, width * chunk[m]: width * chunk[m] + width] = 1.0
+    return f32_to_bf16_bits(x)
+
+
 def unit_vector_x(K: int, k: int) -> np.ndarray:
     x = np.zeros((1, K), dtype=np.float32)
     x[0, k] = 1.0

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(L):
     for n in declared_functions():
         assert hasattr(L, n), n
     assert set(q8.EXPORTS) <= set(declared_functions())
-    assert L.q8_abi_version() == 1
+    assert L.q8_abi_version() == 2
 
 
 def test_status_strings(L):
@@ -134,8 +134,10 @@ def test_gemm_validation(L):
     assert f(A, A, 64, 64, A, 64, 64, A + 8, 64, None, None) == q8.Q8_ERR_ALIGN
     g = L.q8_gemm_ex
     for tile in (-1, 4, 99):
-        assert g(A, A, 64, 64, A, 64, 64, A, 64, tile, None, None) == q8.Q8_ERR_ARG
-    assert g(A, A, 64, 48, A, 64, 64, A, 64, q8.Q8_GEMM_TILE_128x64, None, None) == q8.Q8_ERR_SHAPE
+        assert g(A, A, 64, 64, A, 64, 64, A, 64, tile, 0, None, None) == q8.Q8_ERR_ARG
+    for splits in (-1, q8.Q8_GEMM_MAX_SPLITS + 1):
+        assert g(A, A, 64, 64, A, 64, 64, A, 64, 0, splits, None, None) == q8.Q8_ERR_ARG
+    assert g(A, A, 64, 48, A, 64, 64, A, 64, q8.Q8_GEMM_TILE_64x128, 1, None, None) == q8.Q8_ERR_SHAPE
 
 
 def test_quantize_ex_validation(L):
