@@ -94,6 +94,7 @@ struct GParams {
     int32_t cta_begin[kMaxGrid + 1];  // CTA c's balanced range [cta_begin[c], cta_begin[c+1])
     int32_t cta_split[kMaxGrid];      // it owns [cta_begin[c], cta_split[c]); the rest is pooled
     int32_t pool_off[kMaxGrid + 1];   // pool index of the first pooled stage of CTA c's range
+    uint32_t zero;                    // 0 (a value the compiler cannot see: see warp_loaded_zero)
 };
 
 struct Smem {
@@ -206,31 +207,34 @@ __device__ __forceinline__ void dot_rows(const RowPair<NJ> &rp, const unsigned l
     }
 }
 
-// Load a row pair of the stage into registers, release the slot if this is
-// the warp's last pair of the stage (empty_bar != nullptr), then compute.
+// Load a row pair of the stage into registers and compute; release the slot
+// if this is the warp's last pair of the stage (empty_bar != nullptr).
 template <int NJ, int KJ, bool FULL>
 __device__ __forceinline__ void stage_rows(const uint8_t *cA, const uint8_t *cB, const uint16_t *sA,
                                            const uint16_t *sB, bool vA, bool vB, int lane, int chunks_slice,
                                            const unsigned long long (&xr)[KJ][8], uint64_t *empty_bar,
-                                           float &accA, float &accB) {
+                                           uint32_t zero, float &accA, float &accB) {
     RowPair<NJ> rp;
     load_rows<NJ, FULL>(rp, cA, cB, sA, sB, vA, vB, lane, chunks_slice);
+    dot_rows<NJ, KJ>(rp, xr, accA, accB);
     if (empty_bar) {
-        // the arrive has release semantics: every lane's shared-memory reads
-        // above are ordered before the producer may overwrite the slot
-        __syncwarp();
+        // the slot goes back to the bulk-copy producer once every lane's
+        // loads above have returned, not when they were issued: the release
+        // depends on the two sums, which every loaded word feeds (see
+        // warp_loaded_zero)
+        const uint32_t dep = warp_loaded_zero(__float_as_uint(accA) | __float_as_uint(accB), zero);
         if (lane == 0) {
-            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar)) : "memory");
+            asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(empty_bar) + dep)
+                         : "memory");
         }
     }
-    dot_rows<NJ, KJ>(rp, xr, accA, accB);
 }
 
 // This warp's share of one stage.  Its (row, slice) units are warp + 8j, all
 // of slice `slice`, taken as row pairs (warp + 16t, warp + 16t + 8): rows
 // (warp >> lp) + t * (16 >> lp) and that plus (8 >> lp), t < nsteps <= kMaxPairs.
 // Only a ragged last stage (U < RT * P valid units) leaves a pair with one
-// row.  The slot is released after the warp's last loads of the stage.  The
+// row.  The slot is released once the warp's last pair of the stage is summed.  The
 // lanes' partial sums of all (up to 8) rows are reduced together at the end:
 // a transposed butterfly halves the values a lane carries at each of the
 // first three exchanges, so lane l ends with row value (l >> 2) & 7 and the
@@ -239,7 +243,7 @@ template <int NJ, int KJ>
 __device__ __forceinline__ void stage_pairs(Smem &sm, int slot, int rs, const uint8_t *cA, const uint16_t *sA,
                                             int K, int nb, int lp, int U, int nsteps, int warp, int lane, int slice,
                                             bool full_slice, int chunks_slice, float *yrow, int wrow,
-                                            const unsigned long long (&xr)[KJ][8]) {
+                                            const unsigned long long (&xr)[KJ][8], uint32_t zero) {
     const int pstride = 16 >> lp;  // rows from one pair of the warp to the next
     const int boff = 8 >> lp;      // row B - row A
     float acc[2 * kMaxPairs];
@@ -254,10 +258,10 @@ __device__ __forceinline__ void stage_pairs(Smem &sm, int slot, int rs, const ui
             uint64_t *rel = (t == nsteps - 1) ? &sm.empty[slot] : nullptr;
             if (vB && full_slice)
                 stage_rows<NJ, KJ, true>(ca, ca + boff * K, sa, sa + boff * nb, true, vB, lane, chunks_slice, xr,
-                                         rel, acc[2 * t], acc[2 * t + 1]);
+                                         rel, zero, acc[2 * t], acc[2 * t + 1]);
             else
                 stage_rows<NJ, KJ, false>(ca, ca + boff * K, sa, sa + boff * nb, true, vB, lane, chunks_slice, xr,
-                                          rel, acc[2 * t], acc[2 * t + 1]);
+                                          rel, zero, acc[2 * t], acc[2 * t + 1]);
         }
     }
     // transposed butterfly: keep the half of the values selected by the lane
@@ -525,9 +529,9 @@ __device__ __forceinline__ void cta_work(const GParams &p, Smem &sm, int begin, 
         const bool full_slice = chunks_slice == 32 * nj;
         float *yrow = D.y + r0;
         switch (nj) {
-            case 1: stage_pairs<1, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr); break;
-            case 2: stage_pairs<2, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr); break;
-            default: stage_pairs<3, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr); break;
+            case 1: stage_pairs<1, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr, p.zero); break;
+            case 2: stage_pairs<2, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr, p.zero); break;
+            default: stage_pairs<3, KJ>(sm, slot, rs, cA, sA, D.K, D.nb, D.lp, U, nsteps, warp, lane, slice, full_slice, chunks_slice, yrow, wrow, xr, p.zero); break;
         }
     }
 }
@@ -608,6 +612,7 @@ q8_status launch_gemv(const q8_linear_desc *descs, int count, uint32_t *sched, u
         total_bytes += static_cast<double>(D.N) * K * 1.0625 * (D.P > 1 ? kSplitCost : 1.0);
     }
     p.status = dev_status;
+    p.zero = 0u;
     p.count = count;
     p.total_stages = stages;
     if (stages == 0) return Q8_OK;
