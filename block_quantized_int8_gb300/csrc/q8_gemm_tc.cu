@@ -28,21 +28,23 @@
 //                   memory, fp32 accumulators in tensor memory; stages freed
 //                   in pairs by one commit per ring (none for a stage no
 //                   later k-tile uses); a last commit signals the epilogue.
-//   12 converters   the warps 4..19 of schedulers 0, 2 and 3; all of them
-//                   work on every k-tile (a short latency per stage), each on
-//                   32 weight rows and a third of the 8-code chunks, turning
+//   16 converters   warp 3 and the warps 4..23 of schedulers 0, 2 and 3;
+//                   all of them work on every k-tile (a short latency per
+//                   stage), both k-tiles of a code stage per pass, each on 32
+//                   weight rows and 16 of the 64 codes of a row, turning
 //                   codes into bf16(s q) (the product is exact in fp32, one
-//                   rounding) and storing them into the A stage.  A code
+//                   rounding) and storing them into the A stages.  A code
 //                   stage goes back to its producer as soon as every
 //                   converter's loads of it have returned (the release
 //                   depends on the loaded values), not when they are used.
-//   The 4 warps of scheduler 1 convert nothing: the MMA thread shares that
-//   scheduler, and a warp busy with the conversion arithmetic beside it
-//   holds the tensor pipe at 40-60 % of its rate (measured), so scheduler 1
-//   is left to the MMA issue.  After the main loop all 16 warps 4..19 run
-//   the epilogue: tcgen05.ld of the accumulators (a thread holds one weight
-//   row), bf16, transposed through shared memory into Y's row-major order,
-//   one TMA store.
+//   The warps of scheduler 1 convert nothing: the MMA thread shares that
+//   scheduler, and warps busy with the conversion arithmetic beside it hold
+//   the tensor pipe well below its rate (measured; also with the weights in
+//   tensor memory, where rows 32..63 can only be written from scheduler 1),
+//   so scheduler 1 is left to the MMA issue.  After the main loop the 16
+//   warps 4..19 run the epilogue: tcgen05.ld of the accumulators (a thread
+//   holds one weight row), bf16, transposed through shared memory into Y's
+//   row-major order, one TMA store.
 //
 // Split K (short N, long K: too few tiles for the SMs): the S CTAs of one
 // tile form a thread-block cluster and take consecutive ranges of k-tiles.
@@ -70,8 +72,9 @@ namespace {
 constexpr int kWRows = 128;              // weight rows per tile (MMA M)
 constexpr int kBK = 64;                  // k per k-tile (one 128-byte bf16 row of x)
 constexpr int kRing = 8;                 // most stages of any ring
-constexpr int kEpiWarps = 16;            // warps 4..19: conversion (12 of them) and the epilogue (all)
-constexpr int kThreads = 32 * (4 + kEpiWarps);  // warps 0-2 roles, 3 idle
+constexpr int kEpiWarps = 16;            // warps 4..19: the epilogue
+constexpr int kConverters = 16;          // warp 3 and the warps 4..23 off the MMA warp's scheduler
+constexpr int kThreads = 32 * 24;        // warps 0-2 roles, 3 converter, 4..23 converters / epilogue
 constexpr int kCodeTile = 2 * kWRows * kBK;  // codes of two k-tiles of all 128 rows: [128 rows][128 bytes]
 constexpr int kATile = kWRows * kBK * 2;     // bf16 weights of one k-tile: [128 rows][128 bytes]
 constexpr int kCS = 2;                   // code ring stages (two k-tiles each)
@@ -91,7 +94,7 @@ struct GemmCtl {
     uint64_t x_free[kRing / 2]; // MMAs of x stages 2j, 2j + 1 done (commits of every CTA sharing the x tiles)
     uint64_t a_free[kRing / 2]; // MMAs of A stages 2j, 2j + 1 done (commits of every CTA sharing the A tiles)
     uint64_t c_full[kRing];     // code tile landed (TMA bytes)
-    uint64_t c_empty[kRing];    // code tile read by the 12 converter warps for each of its 2 k-tiles
+    uint64_t c_empty[kRing];    // code tile read by every converter warp
     uint64_t acc_full;          // all MMAs done
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -328,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (tid == 0) {
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&sm.x_full[i], 1);
-            mbar_init(&sm.a_full[i], 12);    // the 12 converter warps
+            mbar_init(&sm.a_full[i], kConverters);
             mbar_init(&sm.c_full[i], 1);
-            mbar_init(&sm.c_empty[i], 24);   // the 12 converter warps, for each of the stage's 2 k-tiles
+            mbar_init(&sm.c_empty[i], kConverters);       // every converter, once per stage (both k-tiles)
             if (i < kRing / 2) {
                 mbar_init(&sm.x_free[i], C);  // the MMAs of every CTA that shares the x tiles
                 mbar_init(&sm.a_free[i], 1);
@@ -428,79 +431,83 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         if (lane == 0) umma_commit(&sm.acc_full);
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 3) {
         if ((warp & 3) != kMmaSched) {
             // --------------------------------------------------- converters
-            // every k-tile is converted by all 12 converter warps (short
-            // latency: the A ring is only 4 deep at BT = 256): converter c
-            // owns weight rows 32 (c % 4) .. +31 and the 8-code chunks
-            // [lo, hi) of the third c / 4 of each row
+            // every k-tile is converted by all 16 converter warps (short
+            // latency: the A ring is only 4 deep at BT = 256), both k-tiles of
+            // a code stage in one pass (twice the independent work per
+            // wait): converter c owns weight rows 32 (c % 4) .. +31 and the
+            // 16 codes 16 (c / 4) .. +15 of each row's 64 in a k-tile, i.e.
+            // one 16-byte unit of the code row, two 16-byte chunks of the A
+            // row and one block scale per k-tile
             const int wi = warp - 4;
-            const int c = wi - (wi + 3 - kMmaSched) / 4;  // index among the warps of the other schedulers
-            const int third = c >> 2;
-            const int j_lo = third == 0 ? 0 : (third == 1 ? 3 : 6), j_hi = third == 0 ? 3 : (third == 1 ? 6 : 8);
+            const int c = warp == 3 ? 0 : 1 + wi - (wi + 3 - kMmaSched) / 4;
+            const int h = c >> 2;
             const int r = 32 * (c & 3) + lane;           // weight row in the tile
             const uint16_t *srow = p.s + static_cast<int64_t>(min(n0 + r, p.N - 1)) * p.nb;
             const bool row_ok = n0 + r < p.N;
             // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7)
             const int sw = r & 7;
-            auto scale_of = [&](int i, int half) -> uint32_t {
-                const int kb = 2 * (kt0 + i) + half;
+            auto scale_of = [&](int i) -> uint32_t {
+                const int kb = 2 * (kt0 + i) + (h >> 1);  // codes 16 h .. 16 h + 15 lie in one block
                 return (row_ok && i < nk && kb < p.nb) ? ldg_nc_u16(srow + kb) : 0u;
             };
-            uint32_t s0 = scale_of(0, 0), s1 = scale_of(0, 1);
-            for (int i = 0; i < nk; ++i) {
-                const int cs = (i >> 1) % kCS, as = i % AS;
-                bool good = wait_or_abort(sm, &sm.c_full[cs], ((i >> 1) / kCS) & 1, p.status) &&
-                            (i < AS || wait_pair(sm.a_free, AS, i));
+            // 8 codes -> 4 bf16x2 words -> 16-byte chunk j of the A row
+            auto put = [&](uint8_t *arow, int j, uint32_t w0, uint32_t w1, unsigned long long sc) {
+                uint32_t o0, o1, o2, o3;
+                codes4_scaled_bf16(w0, sc, o0, o1);
+                codes4_scaled_bf16(w1, sc, o2, o3);
+                *reinterpret_cast<uint4 *>(arow + ((j ^ sw) << 4)) = make_uint4(o0, o1, o2, o3);
+            };
+            uint32_t sa = scale_of(0), sb = scale_of(1);
+            for (int m = 0; 2 * m < nk; ++m) {
+                const int i0 = 2 * m;
+                const bool two = i0 + 1 < nk;
+                const int cs = m % kCS, as = i0 % AS;   // the pair's A stages as, as + 1 (AS is even)
+                // (one pair barrier frees both A stages)
+                bool good = wait_or_abort(sm, &sm.c_full[cs], (m / kCS) & 1, p.status) &&
+                            (i0 < AS || wait_pair(sm.a_free, AS, i0));
                 if (!__all_sync(0xFFFFFFFFu, good)) {
                     ok = false;
                     break;
                 }
-                // my 8-code chunks j of the row: bytes 8 j .. 8 j + 7 of the
-                // k-tile's 64, in the 128-byte swizzled code row
-                uint2 cw[3] = {make_uint2(0u, 0u), make_uint2(0u, 0u), make_uint2(0u, 0u)};
+                // my 16 codes of each k-tile: 16-byte units h and 4 + h of
+                // the 128-byte code row, swizzled
                 const uint8_t *crow = code_tile(cs) + r * 128;
-#pragma unroll
-                for (int jj = 0; jj < 3; ++jj) {
-                    const int j = j_lo + jj;
-                    if (j < j_hi) {
-                        const int cb = 8 * (i & 1) + j;  // 8-byte unit within the 128-byte row
-                        cw[jj] = *reinterpret_cast<const uint2 *>(crow + ((((cb >> 1) ^ sw) << 4) | ((cb & 1) << 3)));
-                    }
-                }
+                const uint4 ca = *reinterpret_cast<const uint4 *>(crow + ((h ^ sw) << 4));
+                const uint4 cb = *reinterpret_cast<const uint4 *>(crow + (((4 + h) ^ sw) << 4));
                 // the codes are in registers: hand the stage back to its
                 // producer once the loads have returned (see warp_loaded_zero)
                 {
-                    const uint32_t v = cw[0].x | cw[0].y | cw[1].x | cw[1].y | cw[2].x | cw[2].y;
-                    const uint32_t dep = warp_loaded_zero(v, p.zero);
+                    const uint32_t dep = warp_loaded_zero(ca.x | ca.y | ca.z | ca.w | cb.x | cb.y | cb.z | cb.w, p.zero);
                     if (lane == 0)
                         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
                                      :: "r"(smem_addr(&sm.c_empty[cs]) + dep) : "memory");
                 }
-                const float fs0 = f16_bits_to_f32(s0), fs1 = f16_bits_to_f32(s1);  // blocks 2 kt and 2 kt + 1
-                s0 = scale_of(i + 1, 0);
-                s1 = scale_of(i + 1, 1);
-                const unsigned long long sc0 = static_cast<unsigned long long>(__float_as_uint(fs0)) * 0x100000001ull;
-                const unsigned long long sc1 = static_cast<unsigned long long>(__float_as_uint(fs1)) * 0x100000001ull;
-                // 8 codes -> 4 bf16x2 words = one 16-byte chunk j of the A row
+                const unsigned long long sca =
+                    static_cast<unsigned long long>(__float_as_uint(f16_bits_to_f32(sa))) * 0x100000001ull;
+                const unsigned long long scb =
+                    static_cast<unsigned long long>(__float_as_uint(f16_bits_to_f32(sb))) * 0x100000001ull;
+                sa = scale_of(i0 + 2);
+                sb = scale_of(i0 + 3);
                 uint8_t *arow = a_tile(as) + r * 128;
-#pragma unroll
-                for (int jj = 0; jj < 3; ++jj) {
-                    const int j = j_lo + jj;
-                    if (j < j_hi) {
-                        const unsigned long long sc = j < 4 ? sc0 : sc1;  // block 2 kt or 2 kt + 1
-                        uint32_t o0, o1, o2, o3;
-                        codes4_scaled_bf16(cw[jj].x, sc, o0, o1);
-                        codes4_scaled_bf16(cw[jj].y, sc, o2, o3);
-                        *reinterpret_cast<uint4 *>(arow + ((j ^ sw) << 4)) = make_uint4(o0, o1, o2, o3);
-                    }
+                put(arow, 2 * h, ca.x, ca.y, sca);
+                put(arow, 2 * h + 1, ca.z, ca.w, sca);
+                if (two) {
+                    arow += kATile;
+                    put(arow, 2 * h, cb.x, cb.y, scb);
+                    put(arow, 2 * h + 1, cb.z, cb.w, scb);
                 }
                 // generic stores -> visible to the tensor core (async proxy)
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&sm.a_full[as])) : "memory");
+                    if (two)
+                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
+                                     :: "r"(smem_addr(&sm.a_full[as + 1])) : "memory");
+                }
             }
         }
         ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(sm, &sm.acc_full, 0, p.status));
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // ------------------------------------------------------------- epilogue
     // warps 4..: warp (qd, part) drains TMEM lanes 32 qd .. +31 (weight rows)
     // and columns [part BT / 4, (part + 1) BT / 4) (tokens)
-    const bool epi = warp >= 4;
+    const bool epi = warp >= 4 && warp < 4 + kEpiWarps;
     const int qd = warp & 3;
     const int part = (warp - 4) >> 2;
     const int r = 32 * qd + lane;
