@@ -28,7 +28,7 @@
 //    kernel reads x from that copy.  For M > 16 they are bf16, x read in
 //    place.
 //  * Work units: the chunks of a matrix fall into C classes of consecutive
-//    chunks (up to 4 of at least 2 chunks each for M <= 16, 1 above); an item is one class
+//    chunks (up to 4 of at least 2 chunks each, 4 for M > 16); an item is one class
 //    of one block of 128 rows.  A class's blocks are summed in chunk order,
 //    and a row block's classes are added in class order, so the result
 //    depends on the matrix and M only: the same bits alone or in any batch,
@@ -38,6 +38,9 @@
 //    row block is shared between CTAs, each writes its partial (the running
 //    sum through its last class, or single classes) to the workspace and the
 //    last to arrive on the row block's ticket adds them in class order.
+//    For M > 16 the running class sum does not fit the registers (128 per
+//    thread at two CTAs per SM): each thread keeps it in its own slot of the
+//    workspace (16 KB per CTA, L2-resident), read and written once per class.
 //  * Batch-invariant mode (any 1 <= M <= 32): bf16 operands from the
 //    caller's x and one class, so every row's arithmetic is the same for
 //    every M (a warp MMA computes each output from its own row only).
@@ -82,14 +85,14 @@ static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte alignment of t
 // conversion of the codes gains nothing, and the second operand path costs
 // registers)
 constexpr bool tile_uses_x_copy(int MT) { return MT < 4; }
-// classes of a matrix with KC chunks: the most, up to 4, that divide KC
-// into classes of at least two chunks (measured: single-chunk classes cost
-// more at their ends than they balance); one for M > 16 (the accumulators
-// of a running class sum fit the registers for M <= 16 only)
+// classes of a matrix with KC chunks at M rows: the most, up to 4, that
+// divide KC into classes of at least two chunks for M <= 16, four for M > 16
+// (measured: shorter classes cost more at their ends than they balance --
+// at M > 16 the running sum also goes through the workspace at each end)
 int classes_for(int64_t KC, int MT) {
-    if (MT >= 4) return 1;
+    const int64_t min_chunks = MT == 4 ? 4 : 2;
     for (int c = kMaxClasses; c > 1; --c)
-        if (KC % c == 0 && KC / c >= 2) return c;
+        if (KC % c == 0 && KC / c >= min_chunks) return c;
     return 1;
 }
 
@@ -120,6 +123,7 @@ struct TParams {
     uint32_t *status;
     uint32_t *tickets;   // [split id][8 warps], zero between launches
     float4 *parts;       // [split id][class][8 warps][32 lanes][MT]
+    float4 *fold;        // MT = 4 with classes: [CTA][8 warps][32 lanes][4], the running class sums
     int32_t count;
     int32_t M;
     int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
@@ -383,6 +387,10 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     // once (its CTAs can only take the slots ours free); a smaller one late
     if (p.early_signal && tid == 0) pdl_launch_dependents();
     if (ie <= ib) return;
+    // MT = 4: this thread's running class sum (16 floats) in the workspace
+    float4 *fold_slot = MT == 4 && p.fold != nullptr
+                            ? p.fold + ((static_cast<size_t>(blockIdx.x) * kWarps + warp) * 32 + lane) * MT
+                            : nullptr;
 
     // total stages of this CTA: the chunks of each item's class
     int nstages = 0;
@@ -416,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     };
     auto issue = [&](int k, const Pos &pos, bool with_x) {
         const int slot = k % kSlots;
-        const TDesc &D = p.d[pos.d];
         const TMaps &T = p.m[pos.d];
         uint8_t *st = base + slot * kStage;
         const int row0 = pos.row0;
@@ -507,7 +514,37 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             const bool prefix = pos.item - c >= ib;
             const bool last_here = c == D.C - 1 || pos.item == ie - 1;
             if constexpr (MT == 4) {
-                store_tile<MT>(D, row0, ra, t, M, acc);  // one class: the item is the row block
+                if (D.C == 1) {
+                    store_tile<MT>(D, row0, ra, t, M, acc);  // one class: the item is the row block
+                } else if (prefix) {
+                    // the same steps as below, the running sum in the
+                    // workspace, added into acc in place (acc is cleared after)
+                    if (c > 0) {
+#pragma unroll
+                        for (int j = 0; j < MT; ++j) {
+                            const float4 u = fold_slot[j];
+                            acc[j][0] += u.x;
+                            acc[j][1] += u.y;
+                            acc[j][2] += u.z;
+                            acc[j][3] += u.w;
+                        }
+                    }
+                    if (c == D.C - 1) {
+                        store_tile<MT>(D, row0, ra, t, M, acc);
+                    } else if (last_here && p.last_sid[blockIdx.x] >= 0) {
+                        const int sid = p.last_sid[blockIdx.x];
+                        put_part<MT>(part_slot<MT>(p, sid, c, warp), lane, acc);
+                        finish_split<MT>(p, D, sid, warp, lane, row0, ra, t);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < MT; ++j)
+                            fold_slot[j] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+                    }
+                } else if (p.first_sid[blockIdx.x] >= 0) {
+                    const int sid = p.first_sid[blockIdx.x];
+                    put_part<MT>(part_slot<MT>(p, sid, c, warp), lane, acc);
+                    if (last_here) finish_split<MT>(p, D, sid, warp, lane, row0, ra, t);
+                }
             } else if (prefix) {
 #pragma unroll
                 for (int j = 0; j < MT; ++j)
@@ -634,8 +671,11 @@ __global__ void __launch_bounds__(kThreads) w8a8_widen_kernel(const __grid_const
     }
 }
 
+
 int g_configured_dev = -1;
-int g_occ = 0;
+// resident CTAs per SM of tile_kernel<1>, <2>, <4>
+int g_occ[3] = {0, 0, 0};
+constexpr int occ_index(int MT) { return MT == 1 ? 0 : (MT == 2 ? 1 : 2); }
 
 template <int MT>
 bool configure(int &occ) {
@@ -644,7 +684,7 @@ bool configure(int &occ) {
     int o = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT>, kThreads, smem_bytes()) != cudaSuccess)
         return false;
-    occ = std::min(occ, std::max(o, 1));
+    occ = std::max(o, 1);
     return true;
 }
 
@@ -655,7 +695,7 @@ bool configure(int &occ) {
 template <int MT>
 q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, int max_sids, cudaStream_t stream,
               bool chained) {
-    const int grid = std::min(std::min(items, di->sm_count * g_occ), kMaxGrid);
+    const int grid = std::min(std::min(items, di->sm_count * g_occ[occ_index(MT)]), kMaxGrid);
     int c = 0;
     double acc = 0.0;
     p.cta_begin[0] = 0;
@@ -719,7 +759,7 @@ q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, i
             p.pe[s] = static_cast<int8_t>(e - 1 - kl);
         }
     }
-    p.early_signal = grid >= di->sm_count * g_occ ? 1 : 0;
+    p.early_signal = grid >= di->sm_count * g_occ[occ_index(MT)] ? 1 : 0;
     return launch_kernel(tile_kernel<MT>, dim3(grid), dim3(kThreads), smem_bytes(), stream, chained, p) ==
                    cudaSuccess
                ? Q8_OK
@@ -733,7 +773,7 @@ int mt_for(int M) { return M <= 8 ? 1 : (M <= 16 ? 2 : 4); }
 // Split row blocks a call may have: at most one per CTA boundary and one per
 // row block.
 int64_t max_splits(const q8_linear_desc *descs, int count, int M) {
-    if (mt_for(M) == 4) return 0;
+    (void)M;
     int64_t rbs = 0;
     for (int i = 0; i < count; ++i) rbs += (descs[i].N + kRows - 1) / kRows;
     return std::min<int64_t>(kMaxGrid, rbs);
@@ -752,6 +792,22 @@ size_t tile_x_region(int64_t K, int M, bool w8a8) {
 
 bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
 
+// M > 16 with classes: the running class sums of the CTAs, one slot per
+// thread, for at most min(items, kMaxGrid) CTAs
+int64_t fold_ctas(const q8_linear_desc *descs, int count, int M) {
+    if (mt_for(M) != 4) return 0;
+    int64_t items = 0;
+    bool classes = false;
+    for (int i = 0; i < count; ++i) {
+        const int C = classes_for(descs[i].K / kChunk, 4);
+        classes = classes || C > 1;
+        items += (descs[i].N + kRows - 1) / kRows * C;
+    }
+    return classes ? std::min<int64_t>(items, kMaxGrid) : 0;
+}
+
+size_t fold_bytes(int64_t ctas) { return static_cast<size_t>(ctas) * kWarps * 32 * 4 * 16; }
+
 size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *ticket_off, size_t *ticket_bytes,
                       bool w8a8) {
     const int MT = mt_for(M);
@@ -761,7 +817,8 @@ size_t tile_workspace(const q8_linear_desc *descs, int count, int M, size_t *tic
     if (ticket_off) *ticket_off = bytes;
     if (ticket_bytes) *ticket_bytes = up256(ms * kWarps * 4);
     if (ms > 0) bytes += up256(ms * kWarps * 4) + static_cast<size_t>(ms) * kMaxClasses * kWarps * 32 * MT * 16;
-    return bytes;
+    // (then the fold slots, 256-byte aligned: the sizes above are multiples of 256)
+    return bytes + fold_bytes(fold_ctas(descs, count, M));
 }
 
 q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xws, uint32_t *dev_status,
@@ -773,9 +830,7 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     for (int i = 0; i < count; ++i)
         if (!tile_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
     if (g_configured_dev != di->device) {
-        int o = 1 << 30;
-        if (!configure<1>(o) || !configure<2>(o) || !configure<4>(o)) return Q8_ERR_CUDA;
-        g_occ = o;
+        if (!configure<1>(g_occ[0]) || !configure<2>(g_occ[1]) || !configure<4>(g_occ[2])) return Q8_ERR_CUDA;
         g_configured_dev = di->device;
     }
     static thread_local TParams p;
@@ -791,6 +846,8 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     const int64_t ms = invariant ? 0 : max_splits(descs, count, M);
     p.tickets = ms > 0 ? reinterpret_cast<uint32_t *>(xws + ticket_off) : nullptr;
     p.parts = ms > 0 ? reinterpret_cast<float4 *>(xws + ticket_off + ticket_bytes) : nullptr;
+    const int64_t fc = invariant ? 0 : fold_ctas(descs, count, M);
+    p.fold = fc > 0 ? reinterpret_cast<float4 *>(xws + need - fold_bytes(fc)) : nullptr;
 
     // x copies: matrix i owns the workspace region after those of 0 .. i-1;
     // a matrix whose x (pointer, row stride, K) an earlier one already has
