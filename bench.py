@@ -545,6 +545,30 @@ def extra_rows(torch, q8, peak):
                 del ws8
             del ys, wsb
         del cps
+    # a K that is not a multiple of 256 (K % 256 = 32): M <= 8 go to the
+    # warp-MMA pipeline, larger M to the general kernel
+    K, N = synth.ODD_K_SHAPE
+    name = f"oddk_K{K}_N{N}"
+    q0, s0 = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, name)).to(dev))
+    ncp = copies_for(N * K * 1.0625)
+    cps = [(q0.clone(), s0.clone()) for _ in range(ncp)]
+    for M in (2, 8, 16):
+        x = torch.from_numpy(synth.activations(M, K, 0, f"{name}.x{M}").view(np.int16)).view(torch.bfloat16).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        by = matmul_bytes(N, K, M)
+        descs = [q8.make_descs([(q, s, x, y)])[0] for (q, s) in cps]
+        wsc = q8.workspace(q8.q8_linear_batch_workspace_size(descs[0], M), dev)
+        t = timed([lambda d=d, M=M: q8.q8_linear_batch(descs=d, M=M, ws=wsc) for d in descs])
+        rows[f"{name}_M{M}_calls"] = row(by, t)
+        nb_ = min(len(cps), q8.Q8_MAX_BATCH)
+        ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(nb_)]
+        bd, _ = q8.make_descs([(cps[i][0], cps[i][1], x, ys[i]) for i in range(nb_)])
+        wsb = q8.workspace(q8.q8_linear_batch_workspace_size(bd, M), dev)
+        t = timed([lambda bd=bd, M=M, wsb=wsb: q8.q8_linear_batch(descs=bd, M=M, ws=wsb)])
+        rows[f"{name}_M{M}_batch{nb_}"] = row(by * nb_, t)
+        del ys, wsb
+    del cps
+
     # prefill-shaped GEMM on tcgen05 (compute-bound: report TFLOP/s)
     peaks, _ = measured_peaks()
     tpk = float(peaks.get("bf16_tflops", 1900.0))

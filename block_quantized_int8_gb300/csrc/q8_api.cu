@@ -164,11 +164,18 @@ size_t q8_workspace_size(int64_t N, int64_t K, int32_t M) {
 }
 
 size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant) {
-    if (variant == Q8_VARIANT_BATCH_INVARIANT) return 0;
-    if (variant != Q8_VARIANT_W8A8) return q8_linear_batch_workspace_size(descs, count, M);
+    if (variant != Q8_VARIANT_W8A8 && variant != Q8_VARIANT_BATCH_INVARIANT)
+        return q8_linear_batch_workspace_size(descs, count, M);
     if (!descs || count < 1 || count > Q8_MAX_BATCH || M < 1 || M > Q8_SKINNY_MAX_M) return 0;
     q8_linear_desc tmp[Q8_MAX_BATCH];
     int n = 0;
+    if (variant == Q8_VARIANT_BATCH_INVARIANT) {
+        // the general kernel's partial sums for the matrices off the 256 grid
+        for (int i = 0; i < count; ++i)
+            if (descs[i].N > 0 && descs[i].K > 0 && descs[i].K % 256) tmp[n++] = descs[i];
+        SplitPlan pl[Q8_MAX_BATCH];
+        return n > 0 ? plan_skinny(tmp, n, M, pl, true) : 0;
+    }
     for (int i = 0; i < count; ++i) {
         if (descs[i].N <= 0 || descs[i].K <= 0 || descs[i].K % 256) continue;
         tmp[n++] = descs[i];
@@ -204,8 +211,7 @@ q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, in
     for (int i = 0; i < count; ++i) {
         q8_status st = check_desc(descs[i], M);
         if (st != Q8_OK) return st;
-        if ((variant == Q8_VARIANT_BATCH_INVARIANT || variant == Q8_VARIANT_W8A8) && descs[i].K % 256 != 0)
-            return Q8_ERR_SHAPE;
+        if (variant == Q8_VARIANT_W8A8 && descs[i].K % 256 != 0) return Q8_ERR_SHAPE;
         if (descs[i].N > 0) live[n++] = descs[i];
     }
     if (M == 0 || n == 0) return Q8_OK;

@@ -46,7 +46,8 @@ struct SplitPlan {
 };
 
 // Plans every descriptor and returns the workspace bytes needed.
-size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans);
+// invariant: the split depends on K alone (the batch-invariant variant).
+size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, bool invariant = false);
 
 // Workspace of a skinny call: the general kernel's plan of every matrix, then
 // (when some matrix is served by the GEMV) a 256-byte block whose first word

@@ -357,10 +357,18 @@ q8_status run(const BatchParams &p, const DeviceInfo *di, cudaStream_t stream, b
 
 // Split heuristic: a function of (N, K, M) only, so a matrix gets the same
 // split -- hence the same bits -- alone or inside a batch.
-static void plan_one(int64_t N, int64_t K, int M, SplitPlan &pl) {
+static void plan_one(int64_t N, int64_t K, int M, SplitPlan &pl, bool invariant) {
     constexpr int kTargetItems = 512;
     const int nb = static_cast<int>(K / 32);
     pl.tiles = static_cast<int32_t>((N + kTileRows - 1) / kTileRows);
+    if (invariant) {
+        // the split from K alone (the fewest ranges whose x slices fit the
+        // staging of every M): the sum order does not depend on M
+        const int S0 = (nb + ksb_for_m(Q8_SKINNY_MAX_M) - 1) / ksb_for_m(Q8_SKINNY_MAX_M);
+        pl.bps = (nb + S0 - 1) / S0;
+        pl.S = (nb + pl.bps - 1) / pl.bps;
+        return;
+    }
     const int s_min = (nb + ksb_for_m(M) - 1) / ksb_for_m(M);
     const int s_want = (kTargetItems + pl.tiles - 1) / pl.tiles;
     const int s_cap_blocks = std::max(1, nb / 8);                                   // >= 8 blocks per split
@@ -373,10 +381,10 @@ static void plan_one(int64_t N, int64_t K, int M, SplitPlan &pl) {
     pl.bps = bps;
 }
 
-size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans) {
+size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, bool invariant) {
     size_t off = 0;
     for (int i = 0; i < count; ++i) {
-        plan_one(descs[i].N, descs[i].K, M, plans[i]);
+        plan_one(descs[i].N, descs[i].K, M, plans[i], invariant);
         plans[i].part_off = plans[i].ticket_off = 0;
         if (plans[i].S > 1) {
             plans[i].ticket_off = off;
@@ -398,13 +406,17 @@ enum Route { kRouteGemv, kRoutePipe, kRouteTile, kRouteGeneral, kRoutes };
 // M = 2..8: the TMA-fed chunked tile kernel for K % 256 == 0 except
 // K = 1536, the warp-MMA bulk-copy pipeline otherwise (also M = 1 with MMA);
 // M = 9..32: the tile kernel (K % 256 == 0); everything else: the general
-// kernel below.  (Measured on 64-matrix batches at M = 2..8: the tiles are
+// kernel below.  The batch-invariant variant takes the tile kernel's
+// bf16 arithmetic for K % 256 == 0 and the general kernel's warp-MMA
+// arithmetic with a split of K that depends on K alone otherwise (for
+// both, each output row's sums depend on that row only, never on M); W8A8
+// takes the tiles.  (Measured on 64-matrix batches at M = 2..8: the tiles are
 // 10-35 % faster at K = 512..1280 and 4096; at K = 1536, the pipeline's
 // best stage shape, the two are within 4 % and a lone matrix takes 8.7 us
 // on the pipeline against 10.7 us on the tiles.)
 Route route_of(int64_t K, int M, int variant) {
-    if (variant == Q8_VARIANT_BATCH_INVARIANT || variant == Q8_VARIANT_W8A8)
-        return kRouteTile;  // every M, K % 256 == 0 (checked)
+    if (variant == Q8_VARIANT_BATCH_INVARIANT) return tile_k_supported(K) ? kRouteTile : kRouteGeneral;
+    if (variant == Q8_VARIANT_W8A8) return kRouteTile;  // every M, K % 256 == 0 (checked)
     if (M == 1 && variant != Q8_VARIANT_MMA && gemv_k_supported(K)) return kRouteGemv;
     if (variant == Q8_VARIANT_SIMT) return kRouteGeneral;
     if (M >= 2 && tile_k_supported(K) && (M > 8 || K != 1536)) return kRouteTile;
@@ -416,7 +428,7 @@ Route route_of(int64_t K, int M, int variant) {
 
 size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
                         size_t *tile_off) {
-    size_t need = count > 0 ? plan_skinny(descs, count, M, plans) : 0;
+    size_t need = count > 0 ? plan_skinny(descs, count, M, plans, false) : 0;
     *sched_off = SIZE_MAX;
     bool gemv = false;
     q8_linear_desc tiles[Q8_MAX_BATCH];
@@ -455,20 +467,27 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     // enqueued; the general kernel uses the front of it
     SplitPlan plans[Q8_MAX_BATCH];
     size_t sched_off = SIZE_MAX, tile_off = SIZE_MAX;
-    // the batch-invariant arithmetic (tiles only) needs none; W8A8 (tiles
-    // only) needs the tile kernel's, from the start of the workspace
+    // the batch-invariant arithmetic needs the general kernel's partial sums
+    // for its matrices (K % 256 != 0) only; W8A8 (tiles only) needs the tile
+    // kernel's, from the start of the workspace
     size_t need = 0;
     if (variant == Q8_VARIANT_W8A8) {
         need = tile_workspace(all, all_count, M, nullptr, nullptr, true);
         tile_off = 0;
-    } else if (variant != Q8_VARIANT_BATCH_INVARIANT) {
+    } else if (variant == Q8_VARIANT_BATCH_INVARIANT) {
+        need = n[kRouteGeneral] > 0 ? plan_skinny(part[kRouteGeneral], n[kRouteGeneral], M, plans, true) : 0;
+    } else {
         need = skinny_workspace(all, all_count, M, plans, &sched_off, &tile_off);
     }
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
     if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u)) return Q8_ERR_ALIGN;
     const q8_linear_desc *descs = part[kRouteGeneral];
     const int count = n[kRouteGeneral];
-    if (count > 0) plan_skinny(descs, count, M, plans);
+    if (count > 0) plan_skinny(descs, count, M, plans, variant == Q8_VARIANT_BATCH_INVARIANT);
+    // every item's x slice fits the staging buffer of this M (the plans keep
+    // to it; checked before anything is enqueued)
+    for (int i = 0; i < count; ++i)
+        if (plans[i].bps > ksb_for_m(M)) return Q8_ERR_UNSUPPORTED;
     if (n[kRouteGemv] > 0) {
         uint32_t *sched = sched_off == SIZE_MAX
                               ? nullptr
@@ -521,6 +540,7 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     if (items == 0) return Q8_OK;
 
     if (variant == Q8_VARIANT_AUTO) variant = (M == 1) ? Q8_VARIANT_SIMT : Q8_VARIANT_MMA;
+    if (variant == Q8_VARIANT_BATCH_INVARIANT) variant = Q8_VARIANT_MMA;
 
     if (variant == Q8_VARIANT_MMA) {
         if (M <= 8) return run<8, Q8_VARIANT_MMA>(p, di, stream, chained);

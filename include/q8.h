@@ -75,12 +75,14 @@ typedef enum q8_status {
  * in a batch).  Source: "Frigg" README, Finding 4 (a matmul over one row
  * is not bit-identical to the same matmul over a batch holding it, so a
  * decode row could not be compared with a batch row).  Every row takes the
- * same arithmetic whatever M is: the TMA-fed tile kernel with bf16
- * operands, exact products, per-block fp32 results times the block scale
- * added in block order, one sum per row over all of K (a warp MMA computes
- * each output from its own row only).  K must be a multiple of 256 (else
- * Q8_ERR_SHAPE); it needs no workspace.  Slower than AUTO where AUTO splits
- * K or uses binary16 operands. */
+ * same arithmetic whatever M is: bf16 operands, exact products, per-block
+ * fp32 results times the block scale added in block order, one sum per row
+ * over all of K (a warp MMA computes each output from its own row only) --
+ * in the TMA-fed tile kernel for K % 256 == 0 (no workspace), in the
+ * general kernel for other K (any multiple of 32), with K split into
+ * ceil(K / 512) ranges -- a split from K alone -- whose partial sums are
+ * added in range order (workspace: q8_linear_batch_workspace_size_ex).
+ * Slower than AUTO where AUTO splits K or uses binary16 operands. */
 #define Q8_VARIANT_BATCH_INVARIANT 3
 /* W8A8: each activation row is quantized to Q8_0 by the weights' rule (the
  * A1 quantizer of its binary32 values), then y = sum over blocks of
@@ -279,7 +281,8 @@ q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t
 size_t q8_workspace_size(int64_t N, int64_t K, int32_t M);
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M);
 /* The workspace of q8_linear_batch_ex with `variant` (the W8A8 variant needs
- * its own; the batch-invariant one none; the others as above). */
+ * its own; the batch-invariant one the general kernel's partial sums of its
+ * matrices with K % 256 != 0, none if there are none; the others as above). */
 size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant);
 
 /*

@@ -122,6 +122,7 @@ VOCAB = 262144
 SWEEP_M = (2, 4, 8, 16, 32)
 SWEEP_SHAPES = ((HIDDEN, 2 * INTER), (INTER, HIDDEN))  # (K, N)
 PREFILL_M = 512
+ODD_K_SHAPE = (2080, 4608)  # (K, N): K % 256 = 32, a shape off the 256 grid
 
 
 def layer_weight_tag(layer: int, name: str) -> str:

@@ -90,9 +90,8 @@ def test_batch_validation(L):
     assert L.q8_linear_batch(d, 65, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch(None, 1, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch_ex(d, 2, 1, 7, None, 0, None, None) == q8.Q8_ERR_ARG
-    # the batch-invariant variant takes K multiples of 256 only (checked
-    # before anything touches the device)
-    assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_BATCH_INVARIANT, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    # W8A8 takes K multiples of 256 only (checked before anything touches
+    # the device); the batch-invariant variant takes any K (a multiple of 32)
     assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_W8A8, None, 0, None, None) == q8.Q8_ERR_SHAPE
     assert L.q8_linear_batch_ex(d, 2, 3, 5, None, 0, None, None) == q8.Q8_ERR_ARG
     # workspace by variant: none for batch-invariant; W8A8 holds x as binary32
@@ -100,6 +99,12 @@ def test_batch_validation(L):
     w = (q8.LinearDesc * 1)()
     w[0] = q8.LinearDesc(A, A, A, A, 1536, 4096, 4096, 1536)
     assert L.q8_linear_batch_workspace_size_ex(w, 1, 4, q8.Q8_VARIANT_BATCH_INVARIANT) == 0
+    # off the 256 grid the batch-invariant variant keeps partial sums: K = 2080
+    # in ceil(2080 / 512) = 5 ranges, 4 rows of 1536 fp32 each, 256-byte rounded
+    odd = (q8.LinearDesc * 1)()
+    odd[0] = q8.LinearDesc(A, A, A, A, 1536, 2080, 2080, 1536)
+    inv = L.q8_linear_batch_workspace_size_ex(odd, 1, 4, q8.Q8_VARIANT_BATCH_INVARIANT)
+    assert inv >= 5 * 4 * 1536 * 4 and inv % 256 == 0
     assert L.q8_linear_batch_workspace_size_ex(w, 1, 4, 0) == L.q8_linear_batch_workspace_size(w, 1, 4)
     w8 = L.q8_linear_batch_workspace_size_ex(w, 1, 4, q8.Q8_VARIANT_W8A8)
     assert w8 >= 16 * 8 * 288 * 4 + 16 * 8 * (288 + 18) and w8 % 256 == 0

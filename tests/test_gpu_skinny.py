@@ -571,6 +571,46 @@ def test_batch_invariant_rows(oracle):
         assert np.array_equal(alone, full[1][:M])
 
 
+@pytest.mark.parametrize("K", [2080, 4128, 12800])
+def test_batch_invariant_rows_any_k(oracle, K):
+    """The batch-invariant variant at K % 256 != 0 (the general kernel, one K
+    range per row tile): row m is the same, bit for bit, for every M that
+    includes it, alone or beside a K % 256 == 0 matrix, and within the
+    tolerance of the oracle."""
+    from block_quantized_int8_gb300 import q8
+    shapes = [(300, K), (1000, 4096)]
+    mats = []
+    for i, (N, Kk) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, Kk, 0, f"invk{K}.{i}"))
+        mats.append((qn, sn, synth.activations(32, Kk, 0, f"invkx{K}.{i}")))
+    dev_w = [weights_dev(qn, sn) for (qn, sn, _) in mats]
+
+    def run(M, which):
+        outs, ms = [], []
+        for i in which:
+            q, s = dev_w[i]
+            x = x_dev(np.ascontiguousarray(mats[i][2][:M]))
+            y = torch.full((M, q.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+            ms.append((q, s, x, y))
+            outs.append(y)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q8.q8_linear_batch(ms, variant=q8.Q8_VARIANT_BATCH_INVARIANT, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        return [y.cpu().numpy() for y in outs]
+
+    full = run(32, [0, 1])
+    qn, sn, xn = mats[0]
+    y_ref, B = oracle.matmul(qn, sn, xn, threads=8)
+    check_tol(full[0], y_ref, B, f"invariant N=300 K={K}")
+    for M in (1, 2, 5, 8, 9, 16, 17, 31):
+        part = run(M, [0, 1])
+        for i in (0, 1):
+            assert np.array_equal(part[i], full[i][:M]), f"matrix {i} at M={M}"
+        (alone,) = run(M, [0])
+        assert np.array_equal(alone, full[0][:M])
+
+
 def _w8a8_run(mats_np, M):
     from block_quantized_int8_gb300 import q8
     mats, outs = [], []
