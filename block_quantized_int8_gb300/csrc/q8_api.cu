@@ -177,10 +177,10 @@ size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t co
         return n > 0 ? plan_skinny(tmp, n, M, pl, true) : 0;
     }
     for (int i = 0; i < count; ++i) {
-        if (descs[i].N <= 0 || descs[i].K <= 0 || descs[i].K % 256) continue;
+        if (descs[i].N <= 0 || descs[i].K <= 0 || descs[i].K % 32) continue;
         tmp[n++] = descs[i];
     }
-    return n > 0 ? tile_workspace(tmp, n, M, nullptr, nullptr, true) : 0;
+    return n > 0 ? w8a8_workspace(tmp, n, M) : 0;
 }
 
 size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count, int32_t M) {
@@ -211,7 +211,6 @@ q8_status linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M, in
     for (int i = 0; i < count; ++i) {
         q8_status st = check_desc(descs[i], M);
         if (st != Q8_OK) return st;
-        if (variant == Q8_VARIANT_W8A8 && descs[i].K % 256 != 0) return Q8_ERR_SHAPE;
         if (descs[i].N > 0) live[n++] = descs[i];
     }
     if (M == 0 || n == 0) return Q8_OK;

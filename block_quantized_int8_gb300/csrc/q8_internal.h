@@ -54,6 +54,11 @@ size_t plan_skinny(const q8_linear_desc *descs, int count, int M, SplitPlan *pla
 // is the GEMV's pool counter, at *sched_off (SIZE_MAX if none), then (when
 // some matrix is served by the tile kernel) the tile kernel's workspace
 // (tile_workspace of those matrices) at *tile_off (SIZE_MAX if none).
+// The workspace of the W8A8 variant (tile kernel for K % 256 == 0, general
+// kernel otherwise); gen_x_off / gen_plan_off: where the general kernel's
+// quantized activations and split partials start.
+size_t w8a8_workspace(const q8_linear_desc *all, int all_count, int M, size_t *gen_x_off = nullptr,
+                      size_t *gen_plan_off = nullptr);
 size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
                         size_t *tile_off = nullptr);
 

@@ -48,6 +48,8 @@ struct DescDev {
     const uint16_t *x;
     float *y;
     float *part;        // [S][M][N] fp32 partials, or null if S == 1
+    const int8_t *xq;   // W8A8: x quantized to Q8_0, codes [M][K] ...
+    const uint16_t *xs; // ... and binary16 scales [M][K / 32]
     uint32_t *tickets;  // [tiles], or null if S == 1
     int64_t K;
     int64_t ldx;
@@ -71,7 +73,8 @@ struct BatchParams {
 template <int MT, int VAR>
 struct Cfg {
     static constexpr int KSB = MT <= 8 ? 64 : (MT <= 16 ? 32 : 16);  // == ksb_for_m
-    static constexpr int XROW = KSB * 64 + 16;                           // bytes per staged x row
+    // bytes per staged x row: KSB blocks of 32 bf16 (W8A8: of 32 codes)
+    static constexpr int XROW = KSB * (VAR == Q8_VARIANT_W8A8 ? 32 : 64) + 16;
     static constexpr int XROWS = MT;                                     // rows per buffer
     static constexpr int XBUF = XROWS * XROW;
     static constexpr int SMEM = 128 + 2 * XBUF;
@@ -92,15 +95,22 @@ __device__ __forceinline__ void issue_x(const BatchParams &p, int item, uint8_t 
     const int split = local % D.S;
     const int kb0 = split * D.bps;
     const int nblk = min(D.bps, D.nb - kb0);
-    const uint32_t bytes = static_cast<uint32_t>(nblk) * 64u;
-    mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(p.M));
-    for (int m = 0; m < p.M; ++m) {
-        bulk_g2s(xb + m * Cfg<MT, VAR>::XROW, D.x + m * D.ldx + static_cast<int64_t>(kb0) * 32, bytes, bar);
+    if constexpr (VAR == Q8_VARIANT_W8A8) {
+        // the codes of x's blocks (16-byte aligned: K and kb0 * 32 are multiples of 32)
+        const uint32_t bytes = static_cast<uint32_t>(nblk) * 32u;
+        mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(p.M));
+        for (int m = 0; m < p.M; ++m)
+            bulk_g2s(xb + m * Cfg<MT, VAR>::XROW, D.xq + m * D.K + static_cast<int64_t>(kb0) * 32, bytes, bar);
+    } else {
+        const uint32_t bytes = static_cast<uint32_t>(nblk) * 64u;
+        mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(p.M));
+        for (int m = 0; m < p.M; ++m)
+            bulk_g2s(xb + m * Cfg<MT, VAR>::XROW, D.x + m * D.ldx + static_cast<int64_t>(kb0) * 32, bytes, bar);
     }
 }
 
 // Per-thread results of one item: rows g and g+8 of the warp's 16 rows.
-//   MMA : acc[j][0..1] = row g,   m = 8j + 2t + {0,1}
+//   MMA, W8A8: acc[j][0..1] = row g,   m = 8j + 2t + {0,1}
 //         acc[j][2..3] = row g+8, m = 8j + 2t + {0,1}
 //   SIMT: after the lane reduction, accg[m] / acch[m] for every m (all four
 //         t-lanes hold the sums; lane t stores m with m % 4 == t).
@@ -138,7 +148,7 @@ __device__ __forceinline__ void compute_item(const BatchParams &p, int item, con
 
     float acc[NT][4];
     float accg[MT], acch[MT];
-    if constexpr (VAR == Q8_VARIANT_MMA) {
+    if constexpr (VAR != Q8_VARIANT_SIMT) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     } else {
@@ -163,8 +173,32 @@ __device__ __forceinline__ void compute_item(const BatchParams &p, int item, con
             if (b + u < nblk) {
                 const float sgv = f16_bits_to_f32(sgr[u]);
                 const float shv = f16_bits_to_f32(shr[u]);
-                const uint8_t *xrow = xb + (b + u) * 64 + 16 * t;
-                if constexpr (VAR == Q8_VARIANT_MMA) {
+                if constexpr (VAR == Q8_VARIANT_W8A8) {
+                    // one int8 MMA per block and 8 activation rows: each
+                    // lane's 8 code bytes stand for the same k slots
+                    // {4t..4t+3, 16+4t..16+4t+3} of weights and x (the dot
+                    // product is the same for any common order of k); the
+                    // exact int32 dot times s_w * s_x (exact in fp32)
+                    const uint8_t *xrow = xb + (b + u) * 32 + 8 * t;
+                    const int kb = kb0 + b + u;
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        uint2 xa = make_uint2(0u, 0u);
+                        if (8 * j + g < M)
+                            xa = *reinterpret_cast<const uint2 *>(xrow + (8 * j + g) * Cfg<MT, VAR>::XROW);
+                        int d0, d1, d2, d3;
+                        mma_s8_16832(d0, d1, d2, d3, cg[u].x, ch[u].x, cg[u].y, ch[u].y, xa.x, xa.y);
+                        const int m0 = 8 * j + 2 * t;
+                        const float x0 = m0 < M ? f16_bits_to_f32(__ldg(D.xs + static_cast<int64_t>(m0) * D.nb + kb)) : 0.f;
+                        const float x1 =
+                            m0 + 1 < M ? f16_bits_to_f32(__ldg(D.xs + static_cast<int64_t>(m0 + 1) * D.nb + kb)) : 0.f;
+                        acc[j][0] = fmaf(sgv * x0, static_cast<float>(d0), acc[j][0]);
+                        acc[j][1] = fmaf(sgv * x1, static_cast<float>(d1), acc[j][1]);
+                        acc[j][2] = fmaf(shv * x0, static_cast<float>(d2), acc[j][2]);
+                        acc[j][3] = fmaf(shv * x1, static_cast<float>(d3), acc[j][3]);
+                    }
+                } else if constexpr (VAR == Q8_VARIANT_MMA) {
+                    const uint8_t *xrow = xb + (b + u) * 64 + 16 * t;
                     uint32_t g01, g23, g45, g67, h01, h23, h45, h67;
                     codes4_to_bf16x2(cg[u].x, g01, g23);
                     codes4_to_bf16x2(cg[u].y, g45, g67);
@@ -185,6 +219,7 @@ __device__ __forceinline__ void compute_item(const BatchParams &p, int item, con
                         acc[j][3] = fmaf(shv, d3, acc[j][3]);
                     }
                 } else {
+                    const uint8_t *xrow = xb + (b + u) * 64 + 16 * t;
                     float cgf[8], chf[8];
                     codes4_to_f32(cg[u].x, cgf[0], cgf[1], cgf[2], cgf[3]);
                     codes4_to_f32(cg[u].y, cgf[4], cgf[5], cgf[6], cgf[7]);
@@ -237,7 +272,7 @@ __device__ __forceinline__ void compute_item(const BatchParams &p, int item, con
         out = D.part + static_cast<int64_t>(split) * M * N;
         ld = N;
     }
-    if constexpr (VAR == Q8_VARIANT_MMA) {
+    if constexpr (VAR != Q8_VARIANT_SIMT) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int m0 = 8 * j + 2 * t;
@@ -410,13 +445,14 @@ enum Route { kRouteGemv, kRoutePipe, kRouteTile, kRouteGeneral, kRoutes };
 // bf16 arithmetic for K % 256 == 0 and the general kernel's warp-MMA
 // arithmetic with a split of K that depends on K alone otherwise (for
 // both, each output row's sums depend on that row only, never on M); W8A8
-// takes the tiles.  (Measured on 64-matrix batches at M = 2..8: the tiles are
+// takes the tiles' int8 block dots for K % 256 == 0 and the general
+// kernel's for other K.  (Measured on 64-matrix batches at M = 2..8: the tiles are
 // 10-35 % faster at K = 512..1280 and 4096; at K = 1536, the pipeline's
 // best stage shape, the two are within 4 % and a lone matrix takes 8.7 us
 // on the pipeline against 10.7 us on the tiles.)
 Route route_of(int64_t K, int M, int variant) {
-    if (variant == Q8_VARIANT_BATCH_INVARIANT) return tile_k_supported(K) ? kRouteTile : kRouteGeneral;
-    if (variant == Q8_VARIANT_W8A8) return kRouteTile;  // every M, K % 256 == 0 (checked)
+    if (variant == Q8_VARIANT_BATCH_INVARIANT || variant == Q8_VARIANT_W8A8)
+        return tile_k_supported(K) ? kRouteTile : kRouteGeneral;
     if (M == 1 && variant != Q8_VARIANT_MMA && gemv_k_supported(K)) return kRouteGemv;
     if (variant == Q8_VARIANT_SIMT) return kRouteGeneral;
     if (M >= 2 && tile_k_supported(K) && (M > 8 || K != 1536)) return kRouteTile;
@@ -425,6 +461,55 @@ Route route_of(int64_t K, int M, int variant) {
 }
 
 }  // namespace
+
+namespace {
+
+size_t up256b(int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); }
+
+// W8A8 on the general kernel: each distinct x (pointer, row stride, K) is
+// widened to binary32 [M][K] and quantized to Q8_0 by the A1 quantizer:
+// codes [M][K] and binary16 scales [M][K / 32], each 256-byte rounded.
+size_t w8a8_x_bytes(int64_t K, int M) {
+    return up256b(static_cast<int64_t>(M) * K * 4) + up256b(static_cast<int64_t>(M) * K) +
+           up256b(static_cast<int64_t>(M) * (K / 32) * 2);
+}
+// index of the first matrix with the same x as matrix i
+int first_same_x(const q8_linear_desc *d, int i) {
+    for (int j = 0; j < i; ++j)
+        if (d[j].x == d[i].x && d[j].ldx == d[i].ldx && d[j].K == d[i].K) return j;
+    return i;
+}
+
+// bf16 x [M][ldx] -> binary32 [M][K]
+__global__ void widen_rows_kernel(const uint16_t *__restrict__ x, int64_t ldx, int M, int64_t K,
+                                  float *__restrict__ xf) {
+    const int64_t total = static_cast<int64_t>(M) * K;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / K;
+        xf[i] = __uint_as_float(static_cast<uint32_t>(x[m * ldx + (i - m * K)]) << 16);
+    }
+}
+
+}  // namespace
+
+// The W8A8 workspace: the tile kernel's for K % 256 == 0, then the general
+// kernel's quantized x and its split-K partials for the other matrices.
+size_t w8a8_workspace(const q8_linear_desc *all, int all_count, int M, size_t *gen_x_off, size_t *gen_plan_off) {
+    q8_linear_desc tiles[Q8_MAX_BATCH], gen[Q8_MAX_BATCH];
+    int nt = 0, ng = 0;
+    for (int i = 0; i < all_count; ++i) {
+        if (tile_k_supported(all[i].K)) tiles[nt++] = all[i];
+        else gen[ng++] = all[i];
+    }
+    size_t off = nt > 0 ? tile_workspace(tiles, nt, M, nullptr, nullptr, true) : 0;
+    if (gen_x_off) *gen_x_off = off;
+    for (int i = 0; i < ng; ++i)
+        if (first_same_x(gen, i) == i) off += w8a8_x_bytes(gen[i].K, M);
+    if (gen_plan_off) *gen_plan_off = off;
+    SplitPlan plans[Q8_MAX_BATCH];
+    return off + (ng > 0 ? plan_skinny(gen, ng, M, plans, false) : 0);
+}
 
 size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
                         size_t *tile_off) {
@@ -470,9 +555,9 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     // the batch-invariant arithmetic needs the general kernel's partial sums
     // for its matrices (K % 256 != 0) only; W8A8 (tiles only) needs the tile
     // kernel's, from the start of the workspace
-    size_t need = 0;
+    size_t need = 0, w8_x_off = 0, w8_plan_off = 0;
     if (variant == Q8_VARIANT_W8A8) {
-        need = tile_workspace(all, all_count, M, nullptr, nullptr, true);
+        need = w8a8_workspace(all, all_count, M, &w8_x_off, &w8_plan_off);
         tile_off = 0;
     } else if (variant == Q8_VARIANT_BATCH_INVARIANT) {
         need = n[kRouteGeneral] > 0 ? plan_skinny(part[kRouteGeneral], n[kRouteGeneral], M, plans, true) : 0;
@@ -507,10 +592,44 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     }
     if (count == 0) return Q8_OK;
 
+    // W8A8: quantize each distinct x of the general kernel's matrices
+    // (binary32 copy, then the A1 quantizer) ahead of the kernel, in order
+    const int8_t *w8_q[Q8_MAX_BATCH] = {};
+    const uint16_t *w8_s[Q8_MAX_BATCH] = {};
+    if (variant == Q8_VARIANT_W8A8) {
+        size_t off = w8_x_off;
+        for (int i = 0; i < count; ++i) {
+            const int j = first_same_x(descs, i);
+            if (j < i) {
+                w8_q[i] = w8_q[j];
+                w8_s[i] = w8_s[j];
+                continue;
+            }
+            const int64_t K = descs[i].K;
+            uint8_t *base = static_cast<uint8_t *>(ws) + off;
+            float *xf = reinterpret_cast<float *>(base);
+            int8_t *xq = reinterpret_cast<int8_t *>(base + up256b(static_cast<int64_t>(M) * K * 4));
+            uint16_t *xs = reinterpret_cast<uint16_t *>(base + up256b(static_cast<int64_t>(M) * K * 4) +
+                                                        up256b(static_cast<int64_t>(M) * K));
+            off += w8a8_x_bytes(K, M);
+            const int64_t total = static_cast<int64_t>(M) * K;
+            const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 4096));
+            widen_rows_kernel<<<blocks, 256, 0, stream>>>(descs[i].x, descs[i].ldx, M, K, xf);
+            if (cudaGetLastError() != cudaSuccess) return Q8_ERR_CUDA;
+            const q8_status st = launch_quantize(xf, M, K, xq, xs, dev_status, stream);
+            if (st != Q8_OK) return st;
+            w8_q[i] = xq;
+            w8_s[i] = xs;
+        }
+    }
+    uint8_t *plan_base = static_cast<uint8_t *>(ws) + (variant == Q8_VARIANT_W8A8 ? w8_plan_off : 0);
+
     BatchParams p;
     int items = 0;
     for (int i = 0; i < count; ++i) {
         DescDev &D = p.d[i];
+        D.xq = w8_q[i];
+        D.xs = w8_s[i];
         D.q = descs[i].q;
         D.s = descs[i].s;
         D.x = descs[i].x;
@@ -525,8 +644,8 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
         D.tiles = plans[i].tiles;
         D.item_begin = items;
         if (plans[i].S > 1) {
-            D.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plans[i].part_off);
-            D.tickets = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + plans[i].ticket_off);
+            D.part = reinterpret_cast<float *>(plan_base + plans[i].part_off);
+            D.tickets = reinterpret_cast<uint32_t *>(plan_base + plans[i].ticket_off);
         } else {
             D.part = nullptr;
             D.tickets = nullptr;
@@ -541,6 +660,11 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
 
     if (variant == Q8_VARIANT_AUTO) variant = (M == 1) ? Q8_VARIANT_SIMT : Q8_VARIANT_MMA;
     if (variant == Q8_VARIANT_BATCH_INVARIANT) variant = Q8_VARIANT_MMA;
+    if (variant == Q8_VARIANT_W8A8) {
+        if (M <= 8) return run<8, Q8_VARIANT_W8A8>(p, di, stream, chained);
+        if (M <= 16) return run<16, Q8_VARIANT_W8A8>(p, di, stream, chained);
+        return run<32, Q8_VARIANT_W8A8>(p, di, stream, chained);
+    }
 
     if (variant == Q8_VARIANT_MMA) {
         if (M <= 8) return run<8, Q8_VARIANT_MMA>(p, di, stream, chained);

@@ -161,19 +161,6 @@ __device__ __forceinline__ int find_tdesc(const TParams &p, int item) {
     return d;
 }
 
-// D = A B on int8: A 16 x 32 (row), B 32 x 8 (column), int32 out.
-// Fragments: a0 / a1 rows g / g + 8 at k = 4t..4t+3, a2 / a3 the same rows at
-// k = 16 + 4t..; b0 / b1 column g at k = 4t.. and 16 + 4t..; d0 d1 row g,
-// columns 2t, 2t + 1, d2 d3 row g + 8.
-__device__ __forceinline__ void mma_s8_16832(int &d0, int &d1, int &d2, int &d3, uint32_t a0, uint32_t a1,
-                                             uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
-        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
-}
-
 // Position in a CTA's sequence of stages: descriptor, item, the chunk of
 // this stage and the end of the item's class.
 struct Pos {

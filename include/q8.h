@@ -91,10 +91,12 @@ typedef enum q8_status {
  * (weights and activations in Q8_0 blocks, integer block dots).  Accuracy
  * against the W8A8 definition as for the other variants (2e-3 * sum |w' x'|
  * + 1e-6, x' the dequantised activations); against the bf16 activations it
- * adds the activations' quantization error.  K must be a multiple of 256
- * (else Q8_ERR_SHAPE); workspace: q8_linear_batch_workspace_size_ex(...,
- * Q8_VARIANT_W8A8) bytes (the binary32 blocks, codes and scales of each
- * distinct x, and the tile kernel's shared-row-block area). */
+ * adds the activations' quantization error.  Any K (a multiple of 32):
+ * K % 256 == 0 runs in the tile kernel, other K in the general kernel (x
+ * quantized to rows of Q8_0 codes and scales, the same block dot and
+ * scaling); workspace: q8_linear_batch_workspace_size_ex(..., Q8_VARIANT_W8A8)
+ * bytes (per distinct x its binary32 copy, codes and scales, plus the
+ * kernels' split-K areas). */
 #define Q8_VARIANT_W8A8 4
 
 /*

@@ -90,9 +90,12 @@ def test_batch_validation(L):
     assert L.q8_linear_batch(d, 65, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch(None, 1, 1, None, 0, None, None) == q8.Q8_ERR_ARG
     assert L.q8_linear_batch_ex(d, 2, 1, 7, None, 0, None, None) == q8.Q8_ERR_ARG
-    # W8A8 takes K multiples of 256 only (checked before anything touches
-    # the device); the batch-invariant variant takes any K (a multiple of 32)
+    # every variant takes any K that is a multiple of 32 (checked before
+    # anything touches the device)
+    d[0].K = 40
     assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_W8A8, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_linear_batch_ex(d, 2, 3, q8.Q8_VARIANT_BATCH_INVARIANT, None, 0, None, None) == q8.Q8_ERR_SHAPE
+    d[0].K = 64
     assert L.q8_linear_batch_ex(d, 2, 3, 5, None, 0, None, None) == q8.Q8_ERR_ARG
     # workspace by variant: none for batch-invariant; W8A8 holds x as binary32
     # blocks, codes and scales (per 256-wide chunk and 8-row group: 9 blocks)
@@ -105,6 +108,9 @@ def test_batch_validation(L):
     odd[0] = q8.LinearDesc(A, A, A, A, 1536, 2080, 2080, 1536)
     inv = L.q8_linear_batch_workspace_size_ex(odd, 1, 4, q8.Q8_VARIANT_BATCH_INVARIANT)
     assert inv >= 5 * 4 * 1536 * 4 and inv % 256 == 0
+    # W8A8 off the 256 grid: x as binary32, codes and scales (M = 4 rows)
+    w8odd = L.q8_linear_batch_workspace_size_ex(odd, 1, 4, q8.Q8_VARIANT_W8A8)
+    assert w8odd >= 4 * 2080 * 4 + 4 * 2080 + 4 * 65 * 2 and w8odd % 256 == 0
     assert L.q8_linear_batch_workspace_size_ex(w, 1, 4, 0) == L.q8_linear_batch_workspace_size(w, 1, 4)
     w8 = L.q8_linear_batch_workspace_size_ex(w, 1, 4, q8.Q8_VARIANT_W8A8)
     assert w8 >= 16 * 8 * 288 * 4 + 16 * 8 * (288 + 18) and w8 % 256 == 0

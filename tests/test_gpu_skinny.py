@@ -658,6 +658,80 @@ def test_w8a8_exact_case(oracle):
     assert np.array_equal(y.astype(np.float64), y_ref)
 
 
+@pytest.mark.parametrize("M", [1, 12, 32])
+@pytest.mark.parametrize("K", [2080, 4128, 12800])
+def test_w8a8_any_k(oracle, K, M):
+    """W8A8 at K % 256 != 0 (the general kernel: x quantized to Q8_0 rows in
+    the workspace, one int8 MMA per block): within the tolerance of the
+    oracle's W8A8 definition, and the same bits alone as beside a K % 256
+    == 0 matrix (which the tile kernel serves)."""
+    mats = []
+    for i, (N, Kk) in enumerate([(300, K), (1536, 4096)]):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, Kk, 0, f"w8k{K}.{i}"))
+        mats.append((qn, sn, synth.activations(M, Kk, 0, f"w8kx{K}.{i}.{M}")))
+    together = _w8a8_run(mats, M)
+    y_ref, B = oracle.matmul_w8a8(*mats[0])
+    check_tol(together[0], y_ref, B, f"W8A8 N=300 K={K} M={M}")
+    (alone,) = _w8a8_run([mats[0]], M)
+    assert np.array_equal(alone, together[0])
+
+
+def test_w8a8_exact_case_any_k(oracle):
+    """The exact case of test_w8a8_exact_case at K = 2080 (general kernel):
+    bit for bit the W8A8 definition."""
+    N, K, M = 300, 2080, 9
+    q, s, _ = synth.exact_case(N, K, M, 0, "w8exk")
+    rng = np.random.default_rng(12)
+    xv = rng.integers(-126, 127, size=(M, K)).astype(np.float32)
+    xv[:, ::32] = 127.0
+    xb = (xv.view(np.uint32) >> 16).astype(np.uint16)
+    (y,) = _w8a8_run([(q, s, xb)], M)
+    y_ref, _ = oracle.matmul_w8a8(q, s, xb)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("M,kind", [(5, "normal"), (17, "wide"), (32, "small")])
+def test_w8a8_activation_codes_any_k(oracle, M, kind):
+    """At K % 256 != 0 the W8A8 activations are quantized into the workspace
+    as binary32 rows [M][K], then codes [M][K] and binary16 scales
+    [M][K / 32] (each region rounded up to 256 bytes).  Read back, the codes
+    and scales equal the oracle's quantize_rows of the binary32 activations
+    bit for bit, and the device status equals the oracle's flags."""
+    from block_quantized_int8_gb300 import q8
+    N, K = 130, 2080
+    qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"w8qk{M}"))
+    if kind == "normal":
+        xn = synth.activations(M, K, 0, f"w8qkx{M}")
+    elif kind == "wide":
+        xn = synth.wide_range_activations(M, K, 0, f"w8qkw{M}")
+    else:
+        xn = _small_scale_activations(M, K, f"w8qks{M}")
+    q, s = weights_dev(qn, sn)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    x = x_dev(xn)  # the descriptor holds a bare pointer: keep x alive
+    descs, _ = q8.make_descs([(q, s, x, y)])
+    need = int(q8.lib().q8_linear_batch_workspace_size_ex(descs, 1, M, q8.Q8_VARIANT_W8A8))
+    up = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert need >= up(M * K * 4) + up(M * K) + up(M * (K // 32) * 2)
+    ws = q8.workspace(need)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8.q8_linear_batch(descs=descs, M=M, ws=ws, variant=q8.Q8_VARIANT_W8A8, dev_status=st)
+    torch.cuda.synchronize()
+    raw = ws.cpu().numpy().view(np.uint8)
+    o_q = up(M * K * 4)
+    o_s = o_q + up(M * K)
+    codes = raw[o_q:o_q + M * K].view(np.int8).reshape(M, K)
+    scales = raw[o_s:o_s + M * (K // 32) * 2].view(np.uint16).reshape(M, K // 32)
+    xf = synth.bf16_bits_to_f32(xn)
+    ref_q, ref_s, flags = oracle.quantize_rows(xf)
+    assert np.array_equal(codes, ref_q)
+    assert np.array_equal(scales, ref_s)
+    assert int(st.item()) == int(flags)
+    if int(flags) == 0:
+        y_ref, B = oracle.matmul_w8a8(qn, sn, xn)
+        check_tol(y.cpu().numpy(), y_ref, B, f"W8A8 codes case M={M} {kind}")
+
+
 def _small_scale_activations(M, K, tag):
     """bf16 bits [M][K]: N(0, 1) draws times one magnitude per 32-block,
     cycling over 2^-8 .. 2^-24, 0 and 1, so that blocks get normal,
