@@ -77,8 +77,11 @@ bool pipe_k_supported(int64_t K);
 q8_status launch_pipe(const q8_linear_desc *descs, int count, int M, uint32_t *dev_status, cudaStream_t stream,
                       bool chained = false);
 
-// 2 <= M <= 32 chunked tile kernel (q8_tile.cu): K a multiple of 256.
+// 2 <= M <= 32 chunked tile kernel (q8_tile.cu).  The default arithmetic
+// takes any K >= 256 (a multiple of 32: the last chunk of 256 may be
+// partial); the batch-invariant and W8A8 modes take whole chunks only.
 bool tile_k_supported(int64_t K);
+bool tile_k_whole_chunks(int64_t K);
 // workspace bytes of the tile kernel for these matrices: each one's x copy
 // and per-chunk flags (M <= 16), in call order, then the tickets and
 // partials of the row blocks that CTAs share; the tickets (zero between

@@ -439,9 +439,10 @@ enum Route { kRouteGemv, kRoutePipe, kRouteTile, kRouteGeneral, kRoutes };
 // so a matrix gets the same kernel -- hence the same bits -- whatever else
 // shares its call.  M = 1: the CUDA-core bulk-copy GEMV (AUTO, SIMT);
 // M = 2..8: the TMA-fed chunked tile kernel for K % 256 == 0 except
-// K = 1536, the warp-MMA bulk-copy pipeline otherwise (also M = 1 with MMA);
-// M = 9..32: the tile kernel (K % 256 == 0); everything else: the general
-// kernel below.  The batch-invariant variant takes the tile kernel's
+// K = 1536, the warp-MMA bulk-copy pipeline for K = 1536 and for the other
+// K it takes (also M = 1 with MMA), the tile kernel with a partial last
+// chunk beyond; M = 9..32: the tile kernel (any K >= 256); everything else:
+// the general kernel below.  The batch-invariant variant takes the tile kernel's
 // bf16 arithmetic for K % 256 == 0 and the general kernel's warp-MMA
 // arithmetic with a split of K that depends on K alone otherwise (for
 // both, each output row's sums depend on that row only, never on M); W8A8
@@ -452,10 +453,11 @@ enum Route { kRouteGemv, kRoutePipe, kRouteTile, kRouteGeneral, kRoutes };
 // on the pipeline against 10.7 us on the tiles.)
 Route route_of(int64_t K, int M, int variant) {
     if (variant == Q8_VARIANT_BATCH_INVARIANT || variant == Q8_VARIANT_W8A8)
-        return tile_k_supported(K) ? kRouteTile : kRouteGeneral;
+        return tile_k_whole_chunks(K) ? kRouteTile : kRouteGeneral;
     if (M == 1 && variant != Q8_VARIANT_MMA && gemv_k_supported(K)) return kRouteGemv;
     if (variant == Q8_VARIANT_SIMT) return kRouteGeneral;
-    if (M >= 2 && tile_k_supported(K) && (M > 8 || K != 1536)) return kRouteTile;
+    if (M <= 8 && pipe_k_supported(K) && (K == 1536 || !tile_k_whole_chunks(K))) return kRoutePipe;
+    if (M >= 2 && tile_k_supported(K)) return kRouteTile;
     if (M <= 8 && pipe_k_supported(K)) return kRoutePipe;
     return kRouteGeneral;
 }
@@ -499,7 +501,7 @@ size_t w8a8_workspace(const q8_linear_desc *all, int all_count, int M, size_t *g
     q8_linear_desc tiles[Q8_MAX_BATCH], gen[Q8_MAX_BATCH];
     int nt = 0, ng = 0;
     for (int i = 0; i < all_count; ++i) {
-        if (tile_k_supported(all[i].K)) tiles[nt++] = all[i];
+        if (tile_k_whole_chunks(all[i].K)) tiles[nt++] = all[i];
         else gen[ng++] = all[i];
     }
     size_t off = nt > 0 ? tile_workspace(tiles, nt, M, nullptr, nullptr, true) : 0;

@@ -1,7 +1,8 @@
 // q8_tile.cu -- Q8_0 W8A16 matmul for 2 <= M <= 32 activation rows over one or
-// several matrices in one persistent launch (K a multiple of 256).  Serves
-// M = 9..32, and M = 2..8 unless K = 1536 (there q8_pipe.cu's whole-row
-// stages are as fast in batches and faster for a lone matrix).
+// several matrices in one persistent launch (any K >= 256, a multiple of
+// 32).  Serves M = 9..32, and M = 2..8 where q8_pipe.cu does not (K = 1536
+// and K not a multiple of 256 up to 4096 go there: whole-row stages are as
+// fast in batches and faster for a lone matrix).
 //
 // Y[m][n] = sum_k s[n][k/32] * q[n][k] * x[m][k]; "Frigg" README, Finding 8
 // (a batched W8A16 kernel reads each weight once for the whole batch of rows)
@@ -41,6 +42,12 @@
 //    For M > 16 the running class sum does not fit the registers (128 per
 //    thread at two CTAs per SM): each thread keeps it in its own slot of the
 //    workspace (16 KB per CTA, L2-resident), read and written once per class.
+//  * K not a multiple of 256: the last chunk is partial.  Its codes come
+//    as two 2-D boxes of [N][K] (TMA writes zeros past K), x from a copy
+//    padded with zeros (M <= 16) or four 2-D boxes of the caller's x (zeros
+//    past K), so the blocks past K add exact zeros.  Such a matrix's scale
+//    rows are not 16-byte aligned, so no TMA box reads them: each lane loads
+//    its rows' 8 scales of a stage from global memory one stage ahead.
 //  * Batch-invariant mode (any 1 <= M <= 32): bf16 operands from the
 //    caller's x and one class, so every row's arithmetic is the same for
 //    every M (a warp MMA computes each output from its own row only).
@@ -77,8 +84,15 @@ constexpr int kW8Row = kW8Blocks * 32;
 constexpr int kW8ScaleOff = 32 * kW8Row;
 static_assert(kW8ScaleOff + 32 * kW8Blocks * 2 <= kXBytes, "W8A8 x of a stage exceeds its region");
 enum TileMode { kModeDefault = 0, kModeInvariant = 1, kModeW8A8 = 2 };
-// shared memory of tile_kernel: alignment slack, ring, barriers and counters
-constexpr int smem_bytes() { return 1024 + kSlots * kStage + 128; }
+// K not a multiple of 256: per warp two buffers with the block scales of its
+// 16 rows for one stage, 5 words (10 halves) per row in slots of 12 halves
+constexpr int kScWords = 5;
+constexpr int kScSlot = 12;
+constexpr int kScBuf = 16 * kScSlot;
+constexpr int kScBytes = kWarps * 2 * kScBuf * 2;
+// shared memory of tile_kernel: alignment slack, ring, barriers and counters,
+// and with matrices whose K is not a multiple of 256 the scale buffers
+constexpr int smem_bytes(bool ragged) { return 1024 + kSlots * kStage + 128 + (ragged ? kScBytes : 0); }
 static_assert(kStage % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled boxes");
 // M <= 16 reads x from the workspace copy (binary16 where exact); M > 16 reads
 // the caller's bf16 x (measured: with four 8-row tiles per block the binary16
@@ -105,7 +119,9 @@ struct TMaps {
 struct TDesc {
     float *y;
     const uint32_t *xflag;  // per chunk: 0 = x copy is binary16, 1 = bf16; W8A8: the x codes
+    const uint16_t *s;      // block scales [N][nb], read in place when nb % 8 != 0
     int64_t ldy;
+    int32_t nb;             // blocks per row, K / 32 (nb % 8 != 0: the last chunk is partial)
     int32_t N;
     int32_t KC;          // chunks per row, K / 256
     int32_t item_begin;  // first global item of this matrix
@@ -155,6 +171,17 @@ __device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *tm, int c0,
         : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared; the bytes past src_bytes (0, 2
+// or 4) are written as zeros and nothing is read for them
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the most recent group of this thread's copies have landed
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ int find_tdesc(const TParams &p, int item) {
     int d = 0;
     while (d + 1 < p.count && item >= p.d[d + 1].item_begin) ++d;
@@ -194,7 +221,7 @@ struct Pos {
 // One chunk (8 blocks of 32) of a warp's 16-row tile into the accumulators a.
 //   cb: the chunk's first code box (128 K-bytes x 128 rows, swizzled), rb = 128 x 128
 //   xb: the chunk's first x box (64 K x MP rows, swizzled)
-//   sa, sb: the block scales of rows ra and ra + 8
+//   sa, sb: the block scales of rows ra and ra + 8 (shared memory)
 //   F16: x of the chunk is binary16 (else bf16)
 template <int MT, bool F16>
 __device__ __forceinline__ void chunk_mma(float (&a)[MT][4], const uint8_t *cb, int rb, const uint8_t *xb,
@@ -344,7 +371,9 @@ __device__ __forceinline__ void finish_split(const TParams &p, const TDesc &D, i
     if (lane == 0) p.tickets[sid * kWarps + warp] = 0u;
 }
 
-template <int MT>
+// RAGGED: some matrix of the launch has K % 256 != 0 (the launches without
+// one run without its code and shared memory)
+template <int MT, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant__ TParams p) {
     constexpr int MP = MT * 8;
     constexpr bool kCopy = tile_uses_x_copy(MT);
@@ -353,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(base + kSlots * kStage);
     uint32_t *rel = reinterpret_cast<uint32_t *>(full + kSlots);  // per slot: warps done with it
+    uint16_t *scb = reinterpret_cast<uint16_t *>(base + kSlots * kStage + 128);  // the warps' scale buffers
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -405,6 +435,11 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             bulk_g2s(dst, xq + static_cast<size_t>(pos.chunk) * MP * kW8Row, MP * kW8Row, &full[slot]);
             bulk_g2s(dst + kW8ScaleOff, xs + static_cast<size_t>(pos.chunk) * MP * kW8Blocks * 2, MP * kW8Blocks * 2,
                      &full[slot]);
+        } else if (RAGGED && !kCopy && (p.d[pos.d].nb & 7) != 0) {
+            // the caller's x, K not a multiple of 256: four 2-D boxes of 64
+            // columns in the 3-D box's layout (zeros past K)
+            for (int i = 0; i < 4; ++i)
+                tma_2d(dst + i * (MP * 128), &p.m[pos.d].x, kChunk * pos.chunk + 64 * i, 0, &full[slot]);
         } else {
             tma_3d(dst, &p.m[pos.d].x, 0, 0, 4 * pos.chunk, &full[slot]);
         }
@@ -414,9 +449,17 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         const TMaps &T = p.m[pos.d];
         uint8_t *st = base + slot * kStage;
         const int row0 = pos.row0;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + kScaleBytes) + xbytes);
-        tma_3d(st, &T.q, 0, row0, 2 * pos.chunk, &full[slot]);
-        tma_2d(st + kCodeBytes + kXBytes, &T.s, 8 * pos.chunk, row0, &full[slot]);
+        if (RAGGED && (p.d[pos.d].nb & 7) != 0) {
+            // K not a multiple of 256: the codes as two 2-D boxes of 128
+            // K-bytes (zeros past K), the scales by the consumers
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes) + xbytes);
+            tma_2d(st, &T.q, kChunk * pos.chunk, row0, &full[slot]);
+            tma_2d(st + kRows * 128, &T.q, kChunk * pos.chunk + 128, row0, &full[slot]);
+        } else {
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(kCodeBytes + kScaleBytes) + xbytes);
+            tma_3d(st, &T.q, 0, row0, 2 * pos.chunk, &full[slot]);
+            tma_2d(st + kCodeBytes + kXBytes, &T.s, 8 * pos.chunk, row0, &full[slot]);
+        }
         if (with_x) issue_x(k, pos);
     };
     Pos pos;
@@ -459,6 +502,35 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     // read through L2
     uint32_t xmask = 0u;
     int xd = -1, xbase = 0;
+    // K not a multiple of 256: the block scales of the warp's 16 rows for a
+    // stage are gathered by 4-byte cp.async into the warp's two buffers, one
+    // stage ahead (row i of the warp in slot i; a slot holds the 8 scales
+    // from half (row * nb) & 1 on, as the copies start 4-byte aligned).
+    // Zeros past K and past N (the copies' zero fill), so the blocks past K
+    // add exact zeros whatever the scales beyond the row hold.
+    uint16_t *wsc = scb + warp * (2 * kScBuf);
+    auto gather_scales = [&](const Pos &q, uint16_t *buf) {
+        const TDesc &E = p.d[q.d];
+        const int left = min(8, E.nb - 8 * q.chunk);  // scales of this chunk inside the row
+        for (int e = lane; e < 16 * kScWords; e += 32) {
+            const int r = e / kScWords, w = e - kScWords * r;
+            const int n = q.row0 + 16 * warp + r;
+            const int64_t o = static_cast<int64_t>(min(n, E.N - 1)) * E.nb + 8 * q.chunk;
+            const int sh = static_cast<int>(o & 1);
+            const int h = 2 * w - sh;  // the word's first scale, relative to o
+            uint32_t bytes = 0u;
+            if (n < E.N) {
+                const bool v0 = h >= 0 && h < left, v1 = h + 1 < left;  // h + 1 >= 0 always
+                bytes = v1 ? 4u : (v0 ? 2u : 0u);
+            }
+            const uint16_t *src = bytes ? E.s + (o - sh) + 2 * w : E.s;
+            cp_async_4(buf + r * kScSlot + 2 * w, src, bytes);
+        }
+    };
+    if constexpr (RAGGED) {
+        if ((p.d[pos.d].nb & 7) != 0) gather_scales(pos, wsc);
+        cp_async_commit();
+    }
 
     for (int k = 0; k < nstages; ++k) {
         // every stage of this CTA is issued: a chained launch after this one
@@ -474,8 +546,24 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             xmask = __ballot_sync(0xffffffffu, ch < D.KC && __ldcg(D.xflag + ch) != 0u);
         }
         const uint32_t xbf = kCopy && p.mode == kModeDefault ? (xmask >> (pos.chunk & 31)) & 1u : 1u;
+        const bool ragged = RAGGED && (D.nb & 7) != 0;
+        if constexpr (RAGGED) {
+            // the next stage's scales into the other buffer (one group per
+            // stage, empty if none), then this stage's group is complete
+            if (k + 1 < nstages) {
+                Pos q = pos;
+                q.next(p);
+                if ((p.d[q.d].nb & 7) != 0) gather_scales(q, wsc + ((k + 1) & 1) * kScBuf);
+            }
+            cp_async_commit();
+            if (ragged) {
+                cp_async_wait_1();
+                __syncwarp();
+            }
+        }
         if (!mbar_wait_bounded(&full[slot], (k / kSlots) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, Q8_DEV_TIMEOUT);
+            if constexpr (RAGGED) cp_async_wait_all();
             drain_after_timeout();
             return;
         }
@@ -484,6 +572,12 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             const uint8_t *xb = st + kCodeBytes;
             const uint16_t *sa = reinterpret_cast<const uint16_t *>(st + kCodeBytes + kXBytes) + ra * 8;
             const uint16_t *sb = sa + 64;
+            if (ragged) {
+                const uint16_t *buf = wsc + (k & 1) * kScBuf;
+                const int na = min(pos.row0 + ra, D.N - 1), nbr = min(pos.row0 + ra + 8, D.N - 1);
+                sa = buf + g * kScSlot + static_cast<int>((static_cast<int64_t>(na) * D.nb) & 1);
+                sb = buf + (g + 8) * kScSlot + static_cast<int>((static_cast<int64_t>(nbr) * D.nb) & 1);
+            }
             if (p.mode == kModeW8A8)
                 chunk_mma_w8a8<MT>(acc, st, kRows * 128, xb,
                                    reinterpret_cast<const uint16_t *>(xb + kW8ScaleOff), sa, sb, ra, offq, g, t);
@@ -572,6 +666,8 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         __syncwarp();
         pos.next(p);
     }
+    // (every scale gather was waited for by its stage; none may outlive the CTA)
+    if constexpr (RAGGED) cp_async_wait_all();
 }
 
 // ---- the x copy ------------------------------------------------------------------
@@ -582,7 +678,8 @@ struct XJob {
     float *xf;            // W8A8: x as binary32 in the chunk-major block order of xq
     int8_t *xq;           // W8A8: codes [K / 256][MP][9 x 32], then scales [K / 256][MP][9]
     int64_t ldx;
-    int64_t K;
+    int64_t K;            // K rounded up to a multiple of 256: the copy's row length
+    int64_t kx;           // columns of x (the copy is zero from there to K)
     int32_t chunk_begin;  // first CTA of this x
 };
 
@@ -594,8 +691,9 @@ struct XParams {
 
 // One CTA per chunk of 256 columns of one x, all M <= 32 rows: thread t
 // holds the 8 values at columns 8 (t % 32) .. 8 (t % 32) + 7 of rows t / 32,
-// t / 32 + 8, t / 32 + 16 and t / 32 + 24.  The chunk goes out as binary16 if
-// binary16 holds every one of its values exactly, else bit for bit as bf16.
+// t / 32 + 8, t / 32 + 16 and t / 32 + 24 (zeros past the columns of x).
+// The chunk goes out as binary16 if binary16 holds every one of its values
+// exactly, else bit for bit as bf16.
 __global__ void __launch_bounds__(kThreads) x_copy_kernel(const __grid_constant__ XParams p) {
     // the tile kernel may start launching at once: it reads weights only
     // until this kernel has completed
@@ -614,7 +712,7 @@ __global__ void __launch_bounds__(kThreads) x_copy_kernel(const __grid_constant_
     for (int i = 0; i < 4; ++i) {
         const int r = r0 + 8 * i;
         v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < p.M) {
+        if (r < p.M && col < J.kx) {
             v[i] = __ldcg(reinterpret_cast<const uint4 *>(J.x + r * J.ldx + col));
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
@@ -660,18 +758,20 @@ __global__ void __launch_bounds__(kThreads) w8a8_widen_kernel(const __grid_const
 
 
 int g_configured_dev = -1;
-// resident CTAs per SM of tile_kernel<1>, <2>, <4>
-int g_occ[3] = {0, 0, 0};
+// resident CTAs per SM of tile_kernel<1>, <2>, <4>, without and with RAGGED
+int g_occ[2][3] = {{0, 0, 0}, {0, 0, 0}};
 constexpr int occ_index(int MT) { return MT == 1 ? 0 : (MT == 2 ? 1 : 2); }
 
-template <int MT>
-bool configure(int &occ) {
-    if (cudaFuncSetAttribute(tile_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes()) != cudaSuccess)
+template <int MT, bool RAGGED>
+bool configure() {
+    if (cudaFuncSetAttribute(tile_kernel<MT, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes(RAGGED)) != cudaSuccess)
         return false;
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT>, kThreads, smem_bytes()) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, tile_kernel<MT, RAGGED>, kThreads, smem_bytes(RAGGED)) !=
+        cudaSuccess)
         return false;
-    occ = std::max(o, 1);
+    g_occ[RAGGED ? 1 : 0][occ_index(MT)] = std::max(o, 1);
     return true;
 }
 
@@ -679,10 +779,11 @@ bool configure(int &occ) {
 // Cuts the item list into `grid` ranges of (nearly) equal bytes and marks
 // the row blocks that two or more ranges share: a split id each, the number
 // of CTAs that share it and the last class of the one that holds class 0.
-template <int MT>
+template <int MT, bool RAGGED>
 q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, int max_sids, cudaStream_t stream,
               bool chained) {
-    const int grid = std::min(std::min(items, di->sm_count * g_occ[occ_index(MT)]), kMaxGrid);
+    const int occ = g_occ[RAGGED ? 1 : 0][occ_index(MT)];
+    const int grid = std::min(std::min(items, di->sm_count * occ), kMaxGrid);
     int c = 0;
     double acc = 0.0;
     p.cta_begin[0] = 0;
@@ -746,8 +847,9 @@ q8_status run(TParams &p, const DeviceInfo *di, int items, double total_bytes, i
             p.pe[s] = static_cast<int8_t>(e - 1 - kl);
         }
     }
-    p.early_signal = grid >= di->sm_count * g_occ[occ_index(MT)] ? 1 : 0;
-    return launch_kernel(tile_kernel<MT>, dim3(grid), dim3(kThreads), smem_bytes(), stream, chained, p) ==
+    p.early_signal = grid >= di->sm_count * occ ? 1 : 0;
+    return launch_kernel(tile_kernel<MT, RAGGED>, dim3(grid), dim3(kThreads), smem_bytes(RAGGED), stream, chained,
+                         p) ==
                    cudaSuccess
                ? Q8_OK
                : Q8_ERR_CUDA;
@@ -768,16 +870,18 @@ int64_t max_splits(const q8_linear_desc *descs, int count, int M) {
 
 // workspace of one matrix's x: the binary16 copy and its flags (M <= 16),
 // or for W8A8 the binary32 blocks, then the codes and scales of x
+// (K not a multiple of 256: the copy's rows are padded to whole chunks)
 size_t tile_x_region(int64_t K, int M, bool w8a8) {
-    const int64_t KC = K / kChunk, MP = 8 * mt_for(M);
+    const int64_t KC = (K + kChunk - 1) / kChunk, MP = 8 * mt_for(M);
     if (w8a8) return up256(KC * MP * kW8Row * 4) + up256(KC * MP * (kW8Row + 2 * kW8Blocks));
     if (!tile_uses_x_copy(mt_for(M))) return 0;
-    return up256(static_cast<int64_t>(M) * K * 2) + up256(KC * 4);
+    return up256(static_cast<int64_t>(M) * KC * kChunk * 2) + up256(KC * 4);
 }
 
 }  // namespace
 
-bool tile_k_supported(int64_t K) { return K % kChunk == 0; }
+bool tile_k_supported(int64_t K) { return K >= kChunk && K % 32 == 0; }
+bool tile_k_whole_chunks(int64_t K) { return K > 0 && K % kChunk == 0; }
 
 // M > 16 with classes: the running class sums of the CTAs, one slot per
 // thread, for at most min(items, kMaxGrid) CTAs
@@ -786,7 +890,7 @@ int64_t fold_ctas(const q8_linear_desc *descs, int count, int M) {
     int64_t items = 0;
     bool classes = false;
     for (int i = 0; i < count; ++i) {
-        const int C = classes_for(descs[i].K / kChunk, 4);
+        const int C = classes_for((descs[i].K + kChunk - 1) / kChunk, 4);
         classes = classes || C > 1;
         items += (descs[i].N + kRows - 1) / kRows * C;
     }
@@ -815,9 +919,12 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     const bool invariant = mode == kModeInvariant, w8 = mode == kModeW8A8;
     if (M < (mode != kModeDefault ? 1 : 2) || M > 32 || count > Q8_MAX_BATCH) return Q8_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i)
-        if (!tile_k_supported(descs[i].K)) return Q8_ERR_UNSUPPORTED;
+        if (mode == kModeDefault ? !tile_k_supported(descs[i].K) : !tile_k_whole_chunks(descs[i].K))
+            return Q8_ERR_UNSUPPORTED;
     if (g_configured_dev != di->device) {
-        if (!configure<1>(g_occ[0]) || !configure<2>(g_occ[1]) || !configure<4>(g_occ[2])) return Q8_ERR_CUDA;
+        if (!configure<1, false>() || !configure<2, false>() || !configure<4, false>() || !configure<1, true>() ||
+            !configure<2, true>() || !configure<4, true>())
+            return Q8_ERR_CUDA;
         g_configured_dev = di->device;
     }
     static thread_local TParams p;
@@ -852,16 +959,18 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         for (int j = 0; j < i && xcopy[i] < 0; ++j)
             if (descs[j].x == d.x && descs[j].ldx == d.ldx && descs[j].K == d.K) xcopy[i] = xcopy[j];
         if (xcopy[i] >= 0) continue;
+        const int64_t KC = (d.K + kChunk - 1) / kChunk;
         XJob &J = xp.j[xp.count];
         J.x = d.x;
         J.xo = reinterpret_cast<uint16_t *>(xws + region);
-        J.flag = reinterpret_cast<uint32_t *>(xws + region + up256(static_cast<int64_t>(M) * d.K * 2));
+        J.flag = reinterpret_cast<uint32_t *>(xws + region + up256(static_cast<int64_t>(M) * KC * kChunk * 2));
         J.xf = reinterpret_cast<float *>(xws + region);
-        J.xq = reinterpret_cast<int8_t *>(xws + region + up256(d.K / kChunk * MP * kW8Row * 4));
+        J.xq = reinterpret_cast<int8_t *>(xws + region + up256(KC * MP * kW8Row * 4));
         J.ldx = d.ldx;
-        J.K = d.K;
+        J.K = KC * kChunk;
+        J.kx = d.K;
         J.chunk_begin = chunks;
-        chunks += static_cast<int>(d.K / kChunk);
+        chunks += static_cast<int>(KC);
         xcopy[i] = xp.count++;
     }
     int items = 0;
@@ -870,23 +979,39 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         TDesc &D = p.d[i];
         TMaps &T = p.m[i];
         const q8_linear_desc &d = descs[i];
-        // x as the kernel reads it: the copy [M][K], or the caller's [M][ldx]
+        // x as the kernel reads it: the copy [M][K rounded up to 256], or the
+        // caller's [M][ldx]
+        const bool whole = tile_k_whole_chunks(d.K);
+        const int64_t KC = (d.K + kChunk - 1) / kChunk;
         const void *xsrc = copy ? static_cast<const void *>(xp.j[xcopy[i]].xo) : static_cast<const void *>(d.x);
-        const int64_t xld = copy ? d.K : d.ldx;
-        const int64_t KC = d.K / kChunk;
+        const int64_t xld = copy ? KC * kChunk : d.ldx;
         const uint64_t qdims[3] = {128, static_cast<uint64_t>(d.N), static_cast<uint64_t>(d.K / 128)};
         const uint64_t qstr[2] = {static_cast<uint64_t>(d.K), 128};
         const uint32_t qbox[3] = {128, kRows, 2};
-        const uint64_t xdims[3] = {64, static_cast<uint64_t>(M), static_cast<uint64_t>(d.K / 64)};
+        const uint64_t xdims[3] = {64, static_cast<uint64_t>(M), static_cast<uint64_t>(KC * 4)};
         const uint64_t xstr[2] = {static_cast<uint64_t>(xld) * 2, 128};
         const uint32_t xbox[3] = {64, static_cast<uint32_t>(MP), 4};
         const int64_t nb = d.K / 32;
-        if (!encode_tmap(&T.q, 1, d.q, 3, qdims, qstr, qbox, true) ||
-            !encode_tmap(&T.x, 2, xsrc, 3, xdims, xstr, xbox, true) ||
-            !encode_2d(&T.s, 2, d.s, static_cast<uint64_t>(nb), static_cast<uint64_t>(d.N),
-                       static_cast<uint64_t>(nb) * 2, 8, kRows, false))
-            return Q8_ERR_CUDA;
+        bool ok;
+        if (whole) {
+            ok = encode_tmap(&T.q, 1, d.q, 3, qdims, qstr, qbox, true) &&
+                 encode_tmap(&T.x, 2, xsrc, 3, xdims, xstr, xbox, true) &&
+                 encode_2d(&T.s, 2, d.s, static_cast<uint64_t>(nb), static_cast<uint64_t>(d.N),
+                           static_cast<uint64_t>(nb) * 2, 8, kRows, false);
+        } else {
+            // codes [N][K] in boxes of 128 K-bytes x 128 rows; x the padded
+            // copy (3-D, as above) or the caller's [M][K] in boxes of 64
+            // columns x MP rows; no scale map (rows not 16-byte aligned)
+            ok = encode_2d(&T.q, 1, d.q, static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N),
+                           static_cast<uint64_t>(d.K), 128, kRows, true) &&
+                 (copy ? encode_tmap(&T.x, 2, xsrc, 3, xdims, xstr, xbox, true)
+                       : encode_2d(&T.x, 2, d.x, static_cast<uint64_t>(d.K), static_cast<uint64_t>(M),
+                                   static_cast<uint64_t>(d.ldx) * 2, 64, static_cast<uint32_t>(MP), true));
+        }
+        if (!ok) return Q8_ERR_CUDA;
         D.y = d.y;
+        D.s = d.s;
+        D.nb = static_cast<int32_t>(nb);
         D.xflag = copy ? xp.j[xcopy[i]].flag
                   : w8 ? reinterpret_cast<const uint32_t *>(xp.j[xcopy[i]].xq)
                        : nullptr;
@@ -899,12 +1024,16 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         D.item_begin = items;
         D.items = static_cast<int32_t>((d.N + kRows - 1) / kRows) * D.C;
         items += D.items;
-        total_bytes += static_cast<double>(d.N) * d.K * 1.0625;
+        // (the same measure as the cut in run(): a partial last chunk counts
+        // whole, as it costs a whole chunk's boxes and MMAs)
+        total_bytes += static_cast<double>(d.N) * KC * kChunk * 1.0625;
     }
     p.status = dev_status;
     p.count = count;
     p.M = M;
     p.mode = mode;
+    bool ragged = false;
+    for (int i = 0; i < count; ++i) ragged = ragged || !tile_k_whole_chunks(descs[i].K);
     if (items == 0) return Q8_OK;
     // the x copy (waits for the kernels before it when chained), then the
     // tiles as its dependent: their first weight stages load while it runs
@@ -925,9 +1054,14 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     }
     const bool dep = copy || chained;
     const int msi = static_cast<int>(ms);
-    if (MT == 1) return run<1>(p, di, items, total_bytes, msi, stream, dep);
-    return MT == 2 ? run<2>(p, di, items, total_bytes, msi, stream, dep)
-                   : run<4>(p, di, items, total_bytes, msi, stream, dep);
+    if (ragged) {
+        if (MT == 1) return run<1, true>(p, di, items, total_bytes, msi, stream, dep);
+        return MT == 2 ? run<2, true>(p, di, items, total_bytes, msi, stream, dep)
+                       : run<4, true>(p, di, items, total_bytes, msi, stream, dep);
+    }
+    if (MT == 1) return run<1, false>(p, di, items, total_bytes, msi, stream, dep);
+    return MT == 2 ? run<2, false>(p, di, items, total_bytes, msi, stream, dep)
+                   : run<4, false>(p, di, items, total_bytes, msi, stream, dep);
 }
 
 }  // namespace q8

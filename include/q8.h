@@ -67,7 +67,7 @@ typedef enum q8_status {
 #define Q8_MAX_BATCH 64      /* most descriptors per q8_linear_batch call */
 
 /* Kernel variants for the M <= 32 path (the _ex entry points). */
-#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: TMA-fed warp-MMA tiles (K % 256 == 0, K != 1536) or the warp-MMA pipeline; M > 8: the tiles */
+#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: the warp-MMA pipeline (K = 1536, and K % 256 != 0 up to 4096), else TMA-fed warp-MMA tiles; M > 8: the tiles (K >= 256) */
 #define Q8_VARIANT_SIMT 1    /* CUDA-core FFMA: codes dequantised in registers, one FMA per weight per row */
 #define Q8_VARIANT_MMA  2    /* warp mma.sync bf16 on exact bf16 codes, block scale applied in fp32 */
 /* Batch-invariant: row m of Y is the same, bit for bit, for every M in
@@ -270,11 +270,13 @@ q8_status q8_linear_batch_ex(const q8_linear_desc *descs, int32_t count, int32_t
 /* Workspace bytes for the calls above; depends only on the shapes, not on
  * the device.  0 means none is needed.  It holds the split-K partial sums and
  * tickets, at M = 1 the GEMV's counter block, and for every matrix that the
- * tile kernel serves with binary16 operands (K a multiple of 256, and
- * 9 <= M <= 16 or 2 <= M <= 8 with K != 1536) a copy of its x, M * K * 2 bytes rounded up to 256, plus a
- * 256-byte-rounded flag word per 256 columns of K: each 256-column chunk of
- * x (all M rows) is copied as binary16 where binary16 holds all its values
- * exactly, else as bf16, and the matmul takes the matching operand type.
+ * tile kernel serves with binary16 operands (9 <= M <= 16 with K >= 256, or
+ * 2 <= M <= 8 with K % 256 == 0 and K != 1536 or K > 4096) a copy of its x,
+ * M * Kp * 2 bytes rounded up to 256 (Kp = K rounded up to a multiple of
+ * 256; zero past K), plus a 256-byte-rounded flag word per 256 columns of
+ * Kp: each 256-column chunk of x (all M rows) is copied as binary16 where
+ * binary16 holds all its values exactly, else as bf16, and the matmul
+ * takes the matching operand type.
  * After the copies come, for M <= 16, the tickets (one 32-byte group each,
  * 256-byte rounded) and fp32 partials (16 KB x ceil(M / 8) each) of up to
  * min(320, total 128-row blocks of those matrices) row blocks whose work is

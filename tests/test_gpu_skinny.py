@@ -35,7 +35,8 @@ def run_batch(mats_np, M, variant, ws_extra=0):
 # exact cases: every product and sum is exact in fp32 -> bit-exact
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("N,K", [(1, 32), (7, 64), (128, 96), (129, 1536), (300, 4096), (1536, 1536)])
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 64), (128, 96), (129, 1536), (300, 4096), (1536, 1536),
+                                 (129, 2080), (130, 4384)])
 @pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16, 17, 32])
 def test_exact_cases_bit_exact(oracle, variant, N, K, M):
     q, s, x = synth.exact_case(N, K, M, 0, f"ex{N}.{K}.{M}")
@@ -277,6 +278,25 @@ def test_tile_k_split_keeps_bits(oracle, M, K):
     check_tol(alone, y_ref, B, f"K split N=1536 K={K} M={M}")
 
 
+@pytest.mark.parametrize("M", [2, 9, 16, 17, 32])
+@pytest.mark.parametrize("K", [288, 800, 2080, 4128, 6176, 12800])
+def test_tile_partial_chunk(oracle, K, M):
+    """K not a multiple of 256 on the tile kernel (M = 9..32, and M = 2..8
+    beyond the pipeline's K <= 4096): the last chunk is partial, the blocks
+    past K add exact zeros.  Within the tolerance of the oracle at 300 rows
+    (a partial last row block); a lone matrix (its row blocks' classes spread
+    over CTAs) gives the same bits as beside six large ones."""
+    qn, sn, _ = oracle.quantize_rows(synth.weights(300, K, 0, f"pc{K}"))
+    mat = (qn, sn, synth.activations(M, K, 0, f"pcx{K}.{M}"))
+    (alone,) = run_batch([mat], M, 0)
+    y_ref, B = oracle.matmul(qn, sn, mat[2], threads=8)
+    check_tol(alone, y_ref, B, f"partial chunk K={K} M={M}")
+    big_q, big_s, _ = oracle.quantize_rows(synth.weights(4096, K, 0, f"pcb{K}"))
+    big = (big_q, big_s, synth.activations(M, K, 0, f"pcbx{K}.{M}"))
+    together = run_batch([mat] + [big] * 6, M, 0)
+    assert np.array_equal(alone, together[0])
+
+
 def test_gemv_pool_counter_returns_to_zero(oracle):
     """The M = 1 kernel hands out its last stages through a counter in the
     workspace; every launch must leave it zero, or the next launch on the same
@@ -477,15 +497,19 @@ def test_gemv_mixed_batch_tolerance(oracle):
         assert np.array_equal(y1, y)
 
 
-@pytest.mark.parametrize("N,K,M", [(300, 1024, 12), (130, 2048, 3), (96, 1536, 16)])
+@pytest.mark.parametrize("N,K,M", [(300, 1024, 12), (130, 2048, 3), (96, 1536, 16), (130, 2080, 12),
+                                   (77, 4384, 5)])
 def test_tile_x_copy_chunks(oracle, N, K, M):
     """The tile kernel (M <= 16) reads x from a copy in the workspace: each 256-column
     chunk (all M rows) as binary16 when binary16 holds every value of the
     chunk exactly (zero, or magnitude in [2^-17, 65504]), else as the bf16
-    bits, with one flag word per chunk (0 = binary16).  Checked against that
-    rule restated on the float values, then the result against the oracle."""
+    bits, with one flag word per chunk (0 = binary16).  For K not a multiple
+    of 256 the copy's rows are K rounded up to 256 long, zero past K.
+    Checked against that rule restated on the float values, then the result
+    against the oracle."""
     from block_quantized_int8_gb300 import q8
-    KC = K // 256
+    KC = (K + 255) // 256
+    Kp = KC * 256
     qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"xc{N}.{K}"))
     xn = synth.activations(M, K, 0, f"xcx{M}.{K}").copy()
     # chunk 1 gets a value below binary16's exact range in its last row,
@@ -498,14 +522,14 @@ def test_tile_x_copy_chunks(oracle, N, K, M):
     xf = (xn.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     a = np.abs(xf)
     fits = (a == 0) | ((a >= 2.0 ** -17) & (a <= 65504.0))
-    want_flags = np.array([0 if fits[:, 256 * c:256 * (c + 1)].all() else 1 for c in range(KC)], np.uint32)
+    want_flags = np.array([0 if fits[:, 256 * c:min(K, 256 * (c + 1))].all() else 1 for c in range(KC)], np.uint32)
     assert want_flags[1] == 1 and 0 in want_flags
 
     q, s = weights_dev(qn, sn)
     x = x_dev(xn)
     need = q8.q8_workspace_size(N, K, M)
     up = lambda b: (b + 255) // 256 * 256
-    copy_bytes = up(M * K * 2)
+    copy_bytes = up(M * Kp * 2)
     # after the copy and its flags: the tickets and partials of row blocks
     # that CTAs share, for at most min(320, row blocks) of them
     MT = 1 if M <= 8 else 2
@@ -518,11 +542,12 @@ def test_tile_x_copy_chunks(oracle, N, K, M):
     torch.cuda.synchronize()
     w = ws.cpu().numpy()
     off = need - tile_bytes
-    got_copy = w[off:off + M * K * 2].view(np.uint16).reshape(M, K)
+    got_copy = w[off:off + M * Kp * 2].view(np.uint16).reshape(M, Kp)
     got_flags = w[off + copy_bytes:off + copy_bytes + KC * 4].view(np.uint32)
     assert np.array_equal(got_flags, want_flags)
+    assert not got_copy[:, K:].any()
     for c in range(KC):
-        cols = slice(256 * c, 256 * (c + 1))
+        cols = slice(256 * c, min(K, 256 * (c + 1)))
         if want_flags[c]:
             want = xn[:, cols]
         else:
