@@ -85,9 +85,9 @@ constexpr int kW8ScaleOff = 32 * kW8Row;
 static_assert(kW8ScaleOff + 32 * kW8Blocks * 2 <= kXBytes, "W8A8 x of a stage exceeds its region");
 enum TileMode { kModeDefault = 0, kModeInvariant = 1, kModeW8A8 = 2 };
 // K not a multiple of 256: per warp two buffers with the block scales of its
-// 16 rows for one stage, 5 words (10 halves) per row in slots of 12 halves
-constexpr int kScWords = 5;
-constexpr int kScSlot = 12;
+// 16 rows for one stage, each row the two 16-byte aligned segments that hold
+// its 8 scales (a slot of 16 halves)
+constexpr int kScSlot = 16;
 constexpr int kScBuf = 16 * kScSlot;
 constexpr int kScBytes = kWarps * 2 * kScBuf * 2;
 // shared memory of tile_kernel: alignment slack, ring, barriers and counters,
@@ -171,10 +171,10 @@ __device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *tm, int c0,
         : "memory");
 }
 
-// 4-byte asynchronous copy global -> shared; the bytes past src_bytes (0, 2
-// or 4) are written as zeros and nothing is read for them
-__device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned); the
+// bytes past src_bytes (0..16) are written as zeros and not read
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
                  :: "r"(smem_addr(dst)), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -503,29 +503,23 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
     uint32_t xmask = 0u;
     int xd = -1, xbase = 0;
     // K not a multiple of 256: the block scales of the warp's 16 rows for a
-    // stage are gathered by 4-byte cp.async into the warp's two buffers, one
-    // stage ahead (row i of the warp in slot i; a slot holds the 8 scales
-    // from half (row * nb) & 1 on, as the copies start 4-byte aligned).
-    // Zeros past K and past N (the copies' zero fill), so the blocks past K
-    // add exact zeros whatever the scales beyond the row hold.
+    // stage are gathered by cp.async into the warp's two buffers, one stage
+    // ahead: lane l copies the 16-byte aligned segment l % 2 of the two that
+    // hold row l / 2's 8 scales, which then start at half o % 8 of its slot
+    // (o: the first scale's index in the array).  Zeros past K and past N
+    // (the copies' zero fill), so the blocks past K add exact zeros whatever
+    // the scales beyond the row hold.
     uint16_t *wsc = scb + warp * (2 * kScBuf);
     auto gather_scales = [&](const Pos &q, uint16_t *buf) {
         const TDesc &E = p.d[q.d];
+        const int r = lane >> 1, sg = lane & 1;
+        const int n = q.row0 + 16 * warp + r;
         const int left = min(8, E.nb - 8 * q.chunk);  // scales of this chunk inside the row
-        for (int e = lane; e < 16 * kScWords; e += 32) {
-            const int r = e / kScWords, w = e - kScWords * r;
-            const int n = q.row0 + 16 * warp + r;
-            const int64_t o = static_cast<int64_t>(min(n, E.N - 1)) * E.nb + 8 * q.chunk;
-            const int sh = static_cast<int>(o & 1);
-            const int h = 2 * w - sh;  // the word's first scale, relative to o
-            uint32_t bytes = 0u;
-            if (n < E.N) {
-                const bool v0 = h >= 0 && h < left, v1 = h + 1 < left;  // h + 1 >= 0 always
-                bytes = v1 ? 4u : (v0 ? 2u : 0u);
-            }
-            const uint16_t *src = bytes ? E.s + (o - sh) + 2 * w : E.s;
-            cp_async_4(buf + r * kScSlot + 2 * w, src, bytes);
-        }
+        const int64_t o = static_cast<int64_t>(min(n, E.N - 1)) * E.nb + 8 * q.chunk;
+        const int64_t seg = (o & ~static_cast<int64_t>(7)) + 8 * sg;  // the segment's first half
+        const int64_t v = n < E.N ? o + left - seg : 0;  // halves of it to copy (clamped to 0..8)
+        const uint32_t bytes = v <= 0 ? 0u : (v >= 8 ? 16u : static_cast<uint32_t>(2 * v));
+        cp_async_16(buf + r * kScSlot + 8 * sg, bytes ? E.s + seg : E.s, bytes);
     };
     if constexpr (RAGGED) {
         if ((p.d[pos.d].nb & 7) != 0) gather_scales(pos, wsc);
@@ -575,8 +569,9 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
             if (ragged) {
                 const uint16_t *buf = wsc + (k & 1) * kScBuf;
                 const int na = min(pos.row0 + ra, D.N - 1), nbr = min(pos.row0 + ra + 8, D.N - 1);
-                sa = buf + g * kScSlot + static_cast<int>((static_cast<int64_t>(na) * D.nb) & 1);
-                sb = buf + (g + 8) * kScSlot + static_cast<int>((static_cast<int64_t>(nbr) * D.nb) & 1);
+                const int64_t c8 = 8 * pos.chunk;
+                sa = buf + g * kScSlot + static_cast<int>((static_cast<int64_t>(na) * D.nb + c8) & 7);
+                sb = buf + (g + 8) * kScSlot + static_cast<int>((static_cast<int64_t>(nbr) * D.nb + c8) & 7);
             }
             if (p.mode == kModeW8A8)
                 chunk_mma_w8a8<MT>(acc, st, kRows * 128, xb,
