@@ -545,14 +545,15 @@ def extra_rows(torch, q8, peak):
                 del ws8
             del ys, wsb
         del cps
-    # a K that is not a multiple of 256 (K % 256 = 32): M <= 8 go to the
-    # warp-MMA pipeline, larger M to the general kernel
+    # a K that is not a multiple of 256 (K % 256 = 32): M = 1 goes to the
+    # GEMV, M = 2..8 to the warp-MMA pipeline, larger M to the tile kernel
+    # with a partial last chunk
     K, N = synth.ODD_K_SHAPE
     name = f"oddk_K{K}_N{N}"
     q0, s0 = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, name)).to(dev))
     ncp = copies_for(N * K * 1.0625)
     cps = [(q0.clone(), s0.clone()) for _ in range(ncp)]
-    for M in (2, 8, 16):
+    for M in (1, 2, 8, 16, 32):
         x = torch.from_numpy(synth.activations(M, K, 0, f"{name}.x{M}").view(np.int16)).view(torch.bfloat16).to(dev)
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
         by = matmul_bytes(N, K, M)
