@@ -19,6 +19,10 @@ Functions and what they follow (page titles of the source pages):
   binary32 quotient w / d32 rounded half away from zero ("MODEL-BASELINE-
   RESULTS" (fak), ACT 4 "Correctness": q8round of a float32 value), with the
   same binary16 stored scale.
+* ``chain_next`` / ``f64_to_bf16`` -- the input of the next matmul of a
+  dependent chain: RMS normalisation (no learnable weight, eps 1e-6) of the
+  first K outputs, or of SwiGLU over the two halves ("Frigg" README, the
+  model card), rounded once to bf16.
 * ``gguf_to_planar`` / ``planar_to_gguf`` -- the GGUF Q8_0 block (34 bytes:
   binary16 scale, then 32 int8 codes; the model files of the "aubier" README,
   "Layout") split into planar codes and scales, and back: a numpy view of
@@ -241,3 +245,49 @@ def matmul_w8a8(q: np.ndarray, s: np.ndarray, x_bf16: np.ndarray):
     wd = q.astype(np.float64) * np.repeat(f16_to_f64(s), 32, axis=1)
     xd = qx.astype(np.float64) * np.repeat(f16_to_f64(sx), 32, axis=1)
     return xd @ wd.T, np.abs(xd) @ np.abs(wd).T
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    """binary64 -> bf16 bits (uint16), one rounding to nearest, ties to even.
+
+    bf16 is binary32 with 8 significant bits: normal values x = m 2^e with
+    1 <= |m| < 2 keep m to 2^-7, values below 2^-126 are multiples of
+    2^-133, and values at or above (2 - 2^-8) 2^127 round to infinity."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros(v.shape, dtype=np.uint16)
+    a = np.abs(v)
+    sign = np.where(np.signbit(v), 0x8000, 0).astype(np.uint32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+        # log2 of a binary64 may land one off next to a power of two
+        e = np.where(np.ldexp(1.0, e.astype(np.int64)) > a, e - 1, e)
+        e = np.where(np.ldexp(1.0, (e + 1).astype(np.int64)) <= a, e + 1, e)
+        step = np.ldexp(1.0, (np.maximum(e, -126) - 7).astype(np.int64))  # the spacing at a
+        r = np.rint(a / step) * step  # exact: a / step and its product are exact in binary64
+    r = np.where(a == 0, 0.0, r)
+    big = r >= np.ldexp(1.0, 128)
+    bits32 = np.where(big, 0x7F800000, np.where(big, 0.0, r).astype(np.float32).view(np.uint32)).astype(np.uint32)
+    bits32 = np.where(np.isnan(v), 0x7FC00000, bits32)
+    bits32 = np.where(np.isinf(v), 0x7F800000, bits32)
+    out[...] = ((bits32 >> 16) | sign).astype(np.uint16)
+    return out
+
+
+def chain_next(y: np.ndarray, K: int, swiglu: bool) -> np.ndarray:
+    """The next input of a dependent matmul chain, from y [M][N] (binary64
+    arithmetic on the given values): per row, v = y[0:K] or, with SwiGLU,
+    v[k] = silu(y[k]) * y[K + k] with silu(a) = a / (1 + e^-a); then
+    x = v / sqrt(mean(v^2) + 1e-6), rounded once to bf16 (``f64_to_bf16``).
+    Source: "Frigg" README, the model card (RMSNorm with no learnable weight,
+    eps 1e-6; the SwiGLU MLP between gate+up and down).  Returns bf16 bits
+    [M][K]."""
+    y = np.asarray(y, dtype=np.float64)
+    if y.ndim == 1:
+        y = y[None, :]
+    if swiglu:
+        a, b = y[:, :K], y[:, K:2 * K]
+        v = a / (1.0 + np.exp(-a)) * b
+    else:
+        v = y[:, :K]
+    ms = np.mean(v * v, axis=1, keepdims=True)
+    return f64_to_bf16(v / np.sqrt(ms + 1e-6))
