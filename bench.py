@@ -419,6 +419,67 @@ def e2e_gbs(torch, ls, steps, bytes_per_step, chained=False):
     return bytes_per_step * steps / dt / 1e9, h2d, d2h
 
 
+def chain_rows(torch, q8, ls, peak, ms=(1, 8)):
+    """The dependent decode chain of a token over the two modules in their
+    order L L L H L L L H: each of its 512 matmuls takes its input from the
+    one before it (q8_linear_chain: RMS normalisation, SwiGLU then RMS
+    normalisation between gate+up and down), the whole token one CUDA graph
+    of programmatic dependent launches.  L is the layer set's module, H a
+    second module of the same shapes (its own weights).  The same weight
+    bytes per token as one layer-set step (eight passes over a module)."""
+    dev = torch.device("cuda")
+    h = []
+    for layer in range(synth.LAYERS):
+        mats = {}
+        for (name, K, N) in synth.LAYER_MATRICES:
+            wf = torch.from_numpy(synth.weights(N, K, 1, synth.layer_weight_tag(layer, name))).to(dev)
+            mats[name] = q8.q8_quantize_rows(wf)
+            del wf
+        h.append(mats)
+    nxt = {"qkv": q8.Q8_CHAIN_RMSNORM, "o_proj": q8.Q8_CHAIN_RMSNORM,
+           "gate_up": q8.Q8_CHAIN_SWIGLU_RMSNORM, "down": q8.Q8_CHAIN_RMSNORM}
+    rows = {}
+    for M in ms:
+        steps = []
+        for module in "LLLHLLLH":
+            w = ls.w if module == "L" else h
+            for layer in range(synth.LAYERS):
+                for (name, K, N) in synth.LAYER_MATRICES:
+                    q, sc = w[layer][name]
+                    if not steps:
+                        x = torch.from_numpy(synth.activations(M, K, 0, "chain.x0").view(np.int16)).view(
+                            torch.bfloat16).to(dev)
+                    else:
+                        x = torch.zeros((M, K), dtype=torch.bfloat16, device=dev)
+                    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+                    steps.append([q, sc, x, y, nxt[name]])
+        steps[-1][4] = q8.Q8_CHAIN_END
+        arr, _ = q8.make_chain([tuple(t) for t in steps])
+        ws = q8.workspace(q8.q8_linear_chain_workspace_size(arr, M), dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        s_ = torch.cuda.Stream()
+        with torch.cuda.stream(s_):
+            q8.q8_linear_chain(arr, M, ws=ws, dev_status=st, stream=s_)
+        s_.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s_):
+            q8.q8_linear_chain(arr, M, ws=ws, dev_status=st, stream=s_)
+        reps = 20
+        dtg = time_steps(torch, g.replay, reps, 3)
+        if int(st.item()) != 0:
+            raise RuntimeError(f"decode chain M={M}: device status {int(st.item())}")
+        t = dtg / reps
+        nbytes = layer_set_bytes(M)[0]
+        rows[f"decode_chain_LLLH_M{M}"] = {
+            "GB/s": round(nbytes / t / 1e9, 1), "frac": round(nbytes / t / 1e9 / peak, 3),
+            "us_per_token": round(t * 1e6, 1), "tok_s": round(M / t, 1),
+            "launches_per_token": 2 * len(steps) - 1, "matmuls_per_token": len(steps)}
+        del g, arr, ws, steps
+    del h
+    torch.cuda.empty_cache()
+    return rows
+
+
 def extra_rows(torch, q8, peak):
     """Context rows: other workloads, each timed with CUDA events on distinct
     weight copies so that no call finds its weights in L2."""
@@ -832,6 +893,8 @@ def main():
                                                  "frac": round(bytes_step * 200 / dtg / 1e9 / peak, 3),
                                                  "us_per_step": round(dtg / 200 * 1e6, 2)}
             del g
+        # the token as a dependent chain (each matmul's input from the one before)
+        rows.update(chain_rows(torch, q8, ls, peak))
 
     cpu = None
     if rank == 0 and not args.no_cpu:

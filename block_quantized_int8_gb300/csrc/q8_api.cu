@@ -233,6 +233,25 @@ q8_status q8_linear_batch_chained(const q8_linear_desc *descs, int32_t count, in
     return linear_batch(descs, count, M, Q8_VARIANT_AUTO, ws, ws_bytes, dev_status, stream, true);
 }
 
+q8_status q8_linear_chain(const q8_chain_step *steps, int32_t count, int32_t M, void *ws, size_t ws_bytes,
+                          uint32_t *dev_status, q8_stream_t stream) {
+    q8_status st = check_chain(steps, count, M);
+    if (st != Q8_OK) return st;
+    if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
+    const size_t need = chain_workspace(steps, count, M);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
+    if (need > 0 && !aligned(ws, 256)) return Q8_ERR_ALIGN;
+    const DeviceInfo *di;
+    st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return launch_chain(steps, count, M, ws, ws_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t q8_linear_chain_workspace_size(const q8_chain_step *steps, int32_t count, int32_t M) {
+    if (check_chain(steps, count, M) != Q8_OK) return 0;
+    return chain_workspace(steps, count, M);
+}
+
 q8_status q8_linear_batch(const q8_linear_desc *descs, int32_t count, int32_t M,
                           void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream) {
     return q8_linear_batch_ex(descs, count, M, Q8_VARIANT_AUTO, ws, ws_bytes, dev_status, stream);

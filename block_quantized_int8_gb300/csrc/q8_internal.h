@@ -62,6 +62,13 @@ size_t w8a8_workspace(const q8_linear_desc *all, int all_count, int M, size_t *g
 size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan *plans, size_t *sched_off,
                         size_t *tile_off = nullptr);
 
+// Dependent matmul chains (q8_chain.cu): the host check of a chain, its
+// workspace (the largest of its steps') and its launches.
+q8_status check_chain(const q8_chain_step *steps, int count, int M);
+size_t chain_workspace(const q8_chain_step *steps, int count, int M);
+q8_status launch_chain(const q8_chain_step *steps, int count, int M, void *ws, size_t ws_bytes,
+                       uint32_t *dev_status, cudaStream_t stream);
+
 // M = 1 bulk-copy pipeline (q8_gemv.cu): matrices with K <= 12288.
 bool gemv_k_supported(int64_t K);
 // sched: a zeroed device word the launch uses as its pool counter and leaves

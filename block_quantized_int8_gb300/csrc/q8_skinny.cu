@@ -32,6 +32,9 @@
 // No wait in this kernel can block forever: the copy waits give up after a
 // time limit and report Q8_DEV_TIMEOUT; the split-K ticket never waits.
 #include <algorithm>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
 
 #include "q8_dev.cuh"
 #include "q8_internal.h"
@@ -539,6 +542,38 @@ size_t skinny_workspace(const q8_linear_desc *descs, int count, int M, SplitPlan
     return need;
 }
 
+namespace {
+
+// The words the kernels count with (split-K tickets, the GEMV's pool
+// counter) are left zero by every launch, but where they sit depends on the
+// call's shapes: another call's partial sums or x copies can cover them.  So
+// the library remembers, per workspace address, the counter ranges of the
+// last call enqueued on it; a call whose ranges differ (or the first call on
+// an address) clears its own ranges first, with one memset each.  Repeated
+// calls of the same shapes clear nothing.
+struct Range {
+    size_t off, len;
+    bool operator==(const Range &o) const { return off == o.off && len == o.len; }
+};
+std::mutex g_ws_mu;
+std::unordered_map<const void *, std::vector<Range>> g_ws_layout;
+constexpr size_t kMaxTrackedWorkspaces = 1 << 16;
+
+q8_status clear_moved_counters(void *ws, const std::vector<Range> &ranges, cudaStream_t stream) {
+    if (ws == nullptr || ranges.empty()) return Q8_OK;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    auto it = g_ws_layout.find(ws);
+    if (it != g_ws_layout.end() && it->second == ranges) return Q8_OK;
+    for (const Range &r : ranges)
+        if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + r.off, 0, r.len, stream) != cudaSuccess) return Q8_ERR_CUDA;
+    // (a forgotten address is cleared again on its next use)
+    if (it == g_ws_layout.end() && g_ws_layout.size() >= kMaxTrackedWorkspaces) g_ws_layout.clear();
+    g_ws_layout[ws] = ranges;
+    return Q8_OK;
+}
+
+}  // namespace
+
 q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int variant,
                         void *ws, size_t ws_bytes, uint32_t *dev_status, cudaStream_t stream, bool chained) {
     const DeviceInfo *di = device_info();
@@ -575,6 +610,23 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     // to it; checked before anything is enqueued)
     for (int i = 0; i < count; ++i)
         if (plans[i].bps > ksb_for_m(M)) return Q8_ERR_UNSUPPORTED;
+    {
+        // this call's counter words: cleared first if the workspace last held
+        // another layout
+        std::vector<Range> ranges;
+        if (sched_off != SIZE_MAX) ranges.push_back({sched_off, 256});
+        if (n[kRouteTile] > 0 && tile_off != SIZE_MAX && variant != Q8_VARIANT_BATCH_INVARIANT) {
+            size_t toff = 0, tbytes = 0;
+            (void)tile_workspace(part[kRouteTile], n[kRouteTile], M, &toff, &tbytes, variant == Q8_VARIANT_W8A8);
+            if (tbytes > 0) ranges.push_back({tile_off + toff, tbytes});
+        }
+        const size_t gbase = variant == Q8_VARIANT_W8A8 ? w8_plan_off : 0;
+        for (int i = 0; i < count; ++i)
+            if (plans[i].S > 1 && plans[i].part_off > plans[i].ticket_off)
+                ranges.push_back({gbase + plans[i].ticket_off, plans[i].part_off - plans[i].ticket_off});
+        const q8_status st = clear_moved_counters(ws, ranges, stream);
+        if (st != Q8_OK) return st;
+    }
     if (n[kRouteGemv] > 0) {
         uint32_t *sched = sched_off == SIZE_MAX
                               ? nullptr

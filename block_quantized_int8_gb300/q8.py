@@ -38,7 +38,7 @@ EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "
            "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_linear_batch_workspace_size_ex", "q8_gemm", "q8_status_str",
            "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex", "q8_gguf_to_planar",
            "q8_planar_to_gguf", "q8_quantize_rows_ex", "q8_selftest_wait_timeout",
-           "q8_stream_read", "q8_stream_read_out_words")
+           "q8_stream_read", "q8_stream_read_out_words", "q8_linear_chain", "q8_linear_chain_workspace_size")
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -53,6 +53,19 @@ class LinearDesc(ctypes.Structure):
                 ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("ldx", ctypes.c_int64), ("ldy", ctypes.c_int64)]
 
+
+class ChainStep(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("ldy", ctypes.c_int64), ("next", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+# how the next step of a chain takes its x from this step's y
+Q8_CHAIN_END = 0
+Q8_CHAIN_RMSNORM = 1
+Q8_CHAIN_SWIGLU_RMSNORM = 2
+Q8_MAX_CHAIN = 4096
 
 _lib = None
 
@@ -78,6 +91,9 @@ def lib():
         L.q8_linear_batch_workspace_size.restype = SZ
         L.q8_linear_batch_workspace_size_ex.argtypes = [ctypes.POINTER(LinearDesc), I32, I32, I32]
         L.q8_linear_batch_workspace_size_ex.restype = SZ
+        L.q8_linear_chain.argtypes = [ctypes.POINTER(ChainStep), I32, I32, P, SZ, U32P, P]
+        L.q8_linear_chain_workspace_size.argtypes = [ctypes.POINTER(ChainStep), I32, I32]
+        L.q8_linear_chain_workspace_size.restype = SZ
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, I32, U32P, P]
         L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
@@ -93,7 +109,7 @@ def lib():
         L.q8_abi_version.restype = I32
         for name in ("q8_quantize_rows", "q8_quantize_rows_ex", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
                      "q8_linear_batch_ex", "q8_linear_batch_chained", "q8_gguf_to_planar",
-                     "q8_planar_to_gguf", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc"):
+                     "q8_planar_to_gguf", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc", "q8_linear_chain"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -284,6 +300,36 @@ def q8_linear_batch(mats=None, ws=None, variant=Q8_VARIANT_AUTO, dev_status=None
         st = lib().q8_linear_batch_ex(descs, len(descs), M, variant, _p(ws), nbytes, _p(dev_status),
                                       _stream(stream))
     _check(st, "q8_linear_batch")
+
+
+def make_chain(steps):
+    """[(q, s, x, y, next), ...] -> (ctypes array of ChainStep, M).  Step 0's
+    x is the input; every later x is a buffer the chain writes (bf16 [M][K]);
+    y is fp32 [M][N]; `next` is a Q8_CHAIN_* code (Q8_CHAIN_END last)."""
+    arr = (ChainStep * len(steps))()
+    M = None
+    for i, (q, s, x, y, nxt) in enumerate(steps):
+        d, m = _desc(q, s, x, y)
+        if M is not None and m != M:
+            raise ValueError("all steps of a chain share M")
+        M = m
+        arr[i] = ChainStep(d.q, d.s, d.x, d.y, d.N, d.K, d.ldx, d.ldy, int(nxt), 0)
+    return arr, (M or 0)
+
+
+def q8_linear_chain_workspace_size(steps, M: int) -> int:
+    return int(lib().q8_linear_chain_workspace_size(steps, len(steps), M))
+
+
+def q8_linear_chain(steps, M, ws=None, dev_status=None, stream=None):
+    """Run a chain from make_chain(): each step's matmul, then the next
+    step's x made from its y on the device (q8_linear_chain)."""
+    need = q8_linear_chain_workspace_size(steps, M)
+    if ws is None and need:
+        ws = workspace(need)
+    nbytes = 0 if ws is None else ws.numel()
+    st = lib().q8_linear_chain(steps, len(steps), M, _p(ws), nbytes, _p(dev_status), _stream(stream))
+    _check(st, "q8_linear_chain")
 
 
 def q8_gemm(q, s, x, y=None, dev_status=None, stream=None, tile=0, splits=0):

@@ -235,7 +235,12 @@ typedef struct q8_linear_desc {
  *           At M = 1 it ends with a 256-byte block whose first word the GEMV
  *           uses as a work counter (it hands its last stages to whichever CTA
  *           is free first) and leaves zero; after a Q8_DEV_TIMEOUT zero the
- *           workspace again.
+ *           workspace again.  One workspace may serve later calls of other
+ *           shapes (at the same address, in stream order): where the words
+ *           a call counts with lie elsewhere than those of the previous call
+ *           enqueued on that address (or on its first use), the library
+ *           clears them first with one cudaMemsetAsync per range in the
+ *           call's stream; repeated calls of the same shapes clear nothing.
  * Each output equals, bit for bit, what q8_gemm_skinny returns for that matrix.
  * Outputs must not overlap each other or any input.
  */
@@ -288,6 +293,57 @@ size_t q8_linear_batch_workspace_size(const q8_linear_desc *descs, int32_t count
  * its own; the batch-invariant one the general kernel's partial sums of its
  * matrices with K % 256 != 0, none if there are none; the others as above). */
 size_t q8_linear_batch_workspace_size_ex(const q8_linear_desc *descs, int32_t count, int32_t M, int32_t variant);
+
+/*
+ * q8_linear_chain -- a chain of dependent skinny matmuls, each step's input
+ * made on the device from the output of the step before it.  Source:
+ * "Frigg" README, the model card (RMSNorm without learnable weights, eps
+ * 1e-6; a SwiGLU MLP; two 16-layer modules run L L L H L L L H per token)
+ * and Finding 3 (a decode step is a long chain of small dependent launches,
+ * launch-bound before it is bandwidth-bound).
+ *   Step i computes y_i[M][N_i] = x_i[M][K_i] * dequant(q_i, s_i)^T (fp32,
+ *   as q8_linear_batch, routed on its own K and M with the automatic
+ *   variant), then, unless it is the last step, writes the next step's
+ *   input x_{i+1}[M][K_{i+1}] (bf16, round to nearest even) from y_i:
+ *     Q8_CHAIN_RMSNORM:        v = y_i[m][0 .. K_{i+1})  (needs N_i >= K_{i+1})
+ *     Q8_CHAIN_SWIGLU_RMSNORM: v[k] = silu(y_i[m][k]) * y_i[m][K_{i+1} + k],
+ *                              silu(a) = a / (1 + e^-a)  (needs N_i >= 2 K_{i+1})
+ *   and x_{i+1}[m][k] = v[k] / sqrt(mean over k of v[k]^2 + 1e-6), in fp32
+ *   (the sum of squares in a fixed order).  The last step has Q8_CHAIN_END.
+ *   Every kernel of the chain is launched as a programmatic dependent of the
+ *   one before it (as q8_linear_batch_chained): a matmul loads its first
+ *   weight stages before the normalisation ahead of it completes, so no
+ *   work earlier in the stream may write any q or s of the chain.
+ *   steps : HOST array of `count` steps, 1 <= count <= Q8_MAX_CHAIN, checked
+ *           on the host before anything is enqueued.  Step 0's x is the
+ *           caller's; every later x is written by the chain.  x and y follow
+ *           q8_linear_desc's alignment rules; no x or y may overlap a q, s
+ *           or another step's x or y that the chain still reads.
+ *   ws    : DEVICE workspace of q8_linear_chain_workspace_size() bytes,
+ *           256-byte aligned, zeroed once: one region per distinct (N, K) of
+ *           the steps, shared by the steps of that shape (they run one after
+ *           another).
+ * Returns Q8_ERR_ARG for a bad `next` code or count, Q8_ERR_SHAPE when a
+ * step's K does not fit the previous step's N.
+ */
+#define Q8_MAX_CHAIN 4096
+#define Q8_CHAIN_END 0
+#define Q8_CHAIN_RMSNORM 1
+#define Q8_CHAIN_SWIGLU_RMSNORM 2
+typedef struct q8_chain_step {
+    const int8_t *q;     /* int8 [N][K] */
+    const uint16_t *s;   /* binary16 bits [N][K/32] */
+    uint16_t *x;         /* bf16 bits [M][ldx]: this step's input */
+    float *y;            /* float [M][ldy]: this step's output */
+    int64_t N, K, ldx, ldy;
+    int32_t next;        /* Q8_CHAIN_*: how the next step's x is made from y */
+    int32_t reserved;    /* 0 */
+} q8_chain_step;
+q8_status q8_linear_chain(const q8_chain_step *steps, int32_t count, int32_t M, void *ws, size_t ws_bytes,
+                          uint32_t *dev_status, q8_stream_t stream);
+/* Workspace bytes for q8_linear_chain (0 if the chain fails its checks or
+ * needs none). */
+size_t q8_linear_chain_workspace_size(const q8_chain_step *steps, int32_t count, int32_t M);
 
 /*
  * q8_gemm -- prefill-shaped Y[M][N] = X[M][K] * W^T for M > 32 on the 5th

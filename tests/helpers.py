@@ -24,9 +24,15 @@ def x_dev(x_bits: np.ndarray):
 
 def check_tol(y_gpu: np.ndarray, y_ref: np.ndarray, B: np.ndarray, what=""):
     y_gpu = np.asarray(y_gpu, dtype=np.float64)
-    err = np.abs(y_gpu - y_ref)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(y_gpu - y_ref)
     lim = TOL_REL * B + TOL_ABS
-    bad = err > lim
+    # a NaN where the reference is a number fails (a comparison with NaN is
+    # false either way); the same NaN or infinity on both sides passes
+    same_special = (np.isnan(y_gpu) & np.isnan(y_ref)) | (np.isinf(y_ref) & (y_gpu == y_ref))
+    bad = ~(err <= lim) & ~same_special
+    err = np.where(same_special, 0.0, err)
     ratio = float(np.max(err / np.maximum(B, 1e-30))) if err.size else 0.0
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outputs outside tolerance; "
                            f"worst err {err.max():.3e}, max err/B {ratio:.3e}")

@@ -127,6 +127,59 @@ def test_batch_validation(L):
     assert L.q8_linear_batch_chained(d, 0, 1, None, 0, None, None) == q8.Q8_OK
 
 
+def test_chain_validation(L):
+    """q8_linear_chain checks the whole chain on the host before anything is
+    enqueued: the `next` codes (the last step ends the chain), each step's K
+    against the previous step's N (N >= K for RMSNORM, N >= 2 K for SwiGLU),
+    M, the count, alignment and the workspace."""
+    from block_quantized_int8_gb300 import q8
+
+    def chain(*steps):
+        arr = (q8.ChainStep * len(steps))()
+        for i, (N, K, nxt) in enumerate(steps):
+            arr[i] = q8.ChainStep(A, A, A, A, N, K, K, N, nxt, 0)
+        return arr
+
+    ok = chain((4608, 1536, q8.Q8_CHAIN_RMSNORM), (8192, 1536, q8.Q8_CHAIN_SWIGLU_RMSNORM),
+               (1536, 4096, q8.Q8_CHAIN_END))
+    need = L.q8_linear_chain_workspace_size(ok, 3, 1)
+    # one 256-byte rounded region per distinct (N, K): a region always holds
+    # the same layout, so its counters stay zero from step to step
+    up = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert need == sum(up(L.q8_workspace_size(N, K, 1)) for (N, K) in [(4608, 1536), (8192, 1536), (1536, 4096)])
+    twice = chain((4608, 1536, q8.Q8_CHAIN_RMSNORM), (1536, 4608, q8.Q8_CHAIN_RMSNORM),
+                  (4608, 1536, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain_workspace_size(twice, 3, 4) == sum(
+        up(L.q8_workspace_size(N, K, 4)) for (N, K) in [(4608, 1536), (1536, 4608)])
+    assert L.q8_linear_chain(ok, 3, 1, None, 0, None, None) == q8.Q8_ERR_WORKSPACE
+    assert L.q8_linear_chain(ok, 3, 1, A + 16, 1 << 20, None, None) == q8.Q8_ERR_ALIGN
+    assert L.q8_linear_chain(ok, 3, 33, A, 1 << 20, None, None) == q8.Q8_ERR_SHAPE
+    assert L.q8_linear_chain(ok, 0, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_chain(None, 1, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ARG
+    assert L.q8_linear_chain_workspace_size(ok, 3, 33) == 0
+    # the last step must end the chain; a middle step must not
+    bad = chain((1536, 1536, q8.Q8_CHAIN_RMSNORM), (1536, 1536, q8.Q8_CHAIN_RMSNORM))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ARG
+    bad = chain((1536, 1536, q8.Q8_CHAIN_END), (1536, 1536, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ARG
+    bad = chain((1536, 1536, 7), (1536, 1536, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ARG
+    # the next K must fit this step's N (twice over for SwiGLU)
+    bad = chain((1536, 1536, q8.Q8_CHAIN_RMSNORM), (1536, 2048, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_SHAPE
+    bad = chain((4096, 1536, q8.Q8_CHAIN_SWIGLU_RMSNORM), (1536, 4096, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_SHAPE
+    # an empty step and a K off the 32 grid
+    bad = chain((0, 1536, q8.Q8_CHAIN_RMSNORM), (1536, 1536, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_SHAPE
+    bad = chain((1536, 1536, q8.Q8_CHAIN_RMSNORM), (1536, 1540, q8.Q8_CHAIN_END))
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_SHAPE
+    # a misaligned x of a later step
+    bad = chain((1536, 1536, q8.Q8_CHAIN_RMSNORM), (1536, 1536, q8.Q8_CHAIN_END))
+    bad[1].x = A + 2
+    assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ALIGN
+
+
 def test_quantize_validation(L):
     from block_quantized_int8_gb300 import q8
     f = L.q8_quantize_rows

@@ -297,6 +297,49 @@ def test_tile_partial_chunk(oracle, K, M):
     assert np.array_equal(alone, together[0])
 
 
+@pytest.mark.parametrize("M", [1, 4, 16, 32])
+def test_workspace_shared_by_other_shapes(oracle, M):
+    """One workspace serving calls of different shapes in turn: the split-K
+    tickets and counters of one call sit where another call's partial sums
+    went, so the library clears a call's counter words when the workspace
+    last held another layout.  Each result equals, bit for bit, the result
+    on a fresh workspace, through several alternations (QKV-shaped, then
+    gate+up-shaped matmuls: their tile tickets and partials overlap), and
+    also after a W8A8 call on the same workspace."""
+    from block_quantized_int8_gb300 import q8
+    shapes = [(4608, 1536), (8192, 1536), (1536, 1536), (1536, 4096)]
+    mats = []
+    for i, (N, K) in enumerate(shapes):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"wsx{i}"))
+        q, s = weights_dev(qn, sn)
+        x = x_dev(synth.activations(M, K, 0, f"wsxx{i}.{M}"))
+        mats.append((q, s, x))
+    fresh = []
+    for (q, s, x) in mats:
+        y = torch.empty((M, q.shape[0]), dtype=torch.float32, device="cuda")
+        q8.q8_linear_batch([(q, s, x, y)])
+        fresh.append(y)
+    need = 0
+    for (q, s, x) in mats:
+        d, _ = q8.make_descs([(q, s, x, torch.empty((M, q.shape[0]), dtype=torch.float32, device="cuda"))])
+        need = max(need, q8.q8_linear_batch_workspace_size(d, M),
+                   int(q8.lib().q8_linear_batch_workspace_size_ex(d, 1, M, q8.Q8_VARIANT_W8A8)))
+    ws = q8.workspace(need)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for rnd in range(3):
+        for i in [0, 1, 2, 1, 3, 0, 1]:
+            q, s, x = mats[i]
+            y = torch.full((M, q.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+            q8.q8_linear_batch([(q, s, x, y)], ws=ws, dev_status=st)
+            torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int32), fresh[i].view(torch.int32)), f"round {rnd} shape {shapes[i]}"
+        q, s, x = mats[rnd % len(mats)]
+        y8 = torch.empty((M, q.shape[0]), dtype=torch.float32, device="cuda")
+        q8.q8_linear_batch([(q, s, x, y8)], ws=ws, variant=q8.Q8_VARIANT_W8A8, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+
 def test_gemv_pool_counter_returns_to_zero(oracle):
     """The M = 1 kernel hands out its last stages through a counter in the
     workspace; every launch must leave it zero, or the next launch on the same
