@@ -547,28 +547,69 @@ namespace {
 // The words the kernels count with (split-K tickets, the GEMV's pool
 // counter) are left zero by every launch, but where they sit depends on the
 // call's shapes: another call's partial sums or x copies can cover them.  So
-// the library remembers, per workspace address, the counter ranges of the
-// last call enqueued on it; a call whose ranges differ (or the first call on
-// an address) clears its own ranges first, with one memset each.  Repeated
-// calls of the same shapes clear nothing.
+// the library keeps, per workspace address, the byte ranges that calls
+// enqueued on it may have left nonzero (their partial sums and x copies); a
+// call clears those of its counter ranges that meet one (one memset each,
+// in its stream), and an address seen for the first time is taken as all
+// nonzero.  Calls that write no such data (the GEMV) or repeat the same
+// shapes clear nothing.
 struct Range {
     size_t off, len;
-    bool operator==(const Range &o) const { return off == o.off && len == o.len; }
 };
 std::mutex g_ws_mu;
-std::unordered_map<const void *, std::vector<Range>> g_ws_layout;
+std::unordered_map<const void *, std::vector<Range>> g_ws_dirty;
 constexpr size_t kMaxTrackedWorkspaces = 1 << 16;
+constexpr size_t kMaxDirtyRanges = 64;
 
-q8_status clear_moved_counters(void *ws, const std::vector<Range> &ranges, cudaStream_t stream) {
-    if (ws == nullptr || ranges.empty()) return Q8_OK;
+bool meets(const std::vector<Range> &set, const Range &r) {
+    for (const Range &d : set)
+        if (d.off < r.off + r.len && r.off < d.off + d.len) return true;
+    return false;
+}
+
+// set minus r (pieces of at most two ranges per member)
+void subtract(std::vector<Range> &set, const Range &r) {
+    std::vector<Range> out;
+    for (const Range &d : set) {
+        if (d.off + d.len <= r.off || r.off + r.len <= d.off) {
+            out.push_back(d);
+            continue;
+        }
+        if (d.off < r.off) out.push_back({d.off, r.off - d.off});
+        if (d.off + d.len > r.off + r.len) out.push_back({r.off + r.len, d.off + d.len - (r.off + r.len)});
+    }
+    set.swap(out);
+}
+
+q8_status clear_met_counters(void *ws, const std::vector<Range> &counters, const std::vector<Range> &data,
+                             cudaStream_t stream) {
+    if (ws == nullptr) return Q8_OK;
     std::lock_guard<std::mutex> lock(g_ws_mu);
-    auto it = g_ws_layout.find(ws);
-    if (it != g_ws_layout.end() && it->second == ranges) return Q8_OK;
-    for (const Range &r : ranges)
+    auto it = g_ws_dirty.find(ws);
+    if (it == g_ws_dirty.end()) {
+        // (a forgotten address is taken as unknown again: cleared on its next use)
+        if (g_ws_dirty.size() >= kMaxTrackedWorkspaces) g_ws_dirty.clear();
+        it = g_ws_dirty.emplace(ws, std::vector<Range>{{0, SIZE_MAX / 2}}).first;
+    }
+    std::vector<Range> &dirty = it->second;
+    for (const Range &r : counters) {
+        if (!meets(dirty, r)) continue;
         if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + r.off, 0, r.len, stream) != cudaSuccess) return Q8_ERR_CUDA;
-    // (a forgotten address is cleared again on its next use)
-    if (it == g_ws_layout.end() && g_ws_layout.size() >= kMaxTrackedWorkspaces) g_ws_layout.clear();
-    g_ws_layout[ws] = ranges;
+        subtract(dirty, r);
+    }
+    for (const Range &r : data) {
+        subtract(dirty, r);
+        dirty.push_back(r);
+    }
+    // a long history collapses into one range over all of it (more clearing, never less)
+    if (dirty.size() > kMaxDirtyRanges) {
+        size_t lo = SIZE_MAX, hi = 0;
+        for (const Range &d : dirty) {
+            lo = std::min(lo, d.off);
+            hi = std::max(hi, d.off + d.len);
+        }
+        dirty.assign(1, Range{lo, hi - lo});
+    }
     return Q8_OK;
 }
 
@@ -611,20 +652,27 @@ q8_status launch_skinny(const q8_linear_desc *all, int all_count, int M, int var
     for (int i = 0; i < count; ++i)
         if (plans[i].bps > ksb_for_m(M)) return Q8_ERR_UNSUPPORTED;
     {
-        // this call's counter words: cleared first if the workspace last held
-        // another layout
-        std::vector<Range> ranges;
-        if (sched_off != SIZE_MAX) ranges.push_back({sched_off, 256});
+        // this call's counter words (cleared first where an earlier call on
+        // this workspace may have left data) and the data it writes
+        std::vector<Range> counters, data;
+        if (sched_off != SIZE_MAX) counters.push_back({sched_off, 256});
         if (n[kRouteTile] > 0 && tile_off != SIZE_MAX && variant != Q8_VARIANT_BATCH_INVARIANT) {
             size_t toff = 0, tbytes = 0;
-            (void)tile_workspace(part[kRouteTile], n[kRouteTile], M, &toff, &tbytes, variant == Q8_VARIANT_W8A8);
-            if (tbytes > 0) ranges.push_back({tile_off + toff, tbytes});
+            const size_t total =
+                tile_workspace(part[kRouteTile], n[kRouteTile], M, &toff, &tbytes, variant == Q8_VARIANT_W8A8);
+            if (tbytes > 0) counters.push_back({tile_off + toff, tbytes});
+            if (toff > 0) data.push_back({tile_off, toff});  // x copies and flags
+            if (total > toff + tbytes) data.push_back({tile_off + toff + tbytes, total - toff - tbytes});
         }
         const size_t gbase = variant == Q8_VARIANT_W8A8 ? w8_plan_off : 0;
-        for (int i = 0; i < count; ++i)
-            if (plans[i].S > 1 && plans[i].part_off > plans[i].ticket_off)
-                ranges.push_back({gbase + plans[i].ticket_off, plans[i].part_off - plans[i].ticket_off});
-        const q8_status st = clear_moved_counters(ws, ranges, stream);
+        if (variant == Q8_VARIANT_W8A8 && w8_plan_off > w8_x_off) data.push_back({w8_x_off, w8_plan_off - w8_x_off});
+        for (int i = 0; i < count; ++i) {
+            if (plans[i].S <= 1) continue;
+            counters.push_back({gbase + plans[i].ticket_off, plans[i].part_off - plans[i].ticket_off});
+            data.push_back({gbase + plans[i].part_off,
+                            static_cast<size_t>(plans[i].S) * M * static_cast<size_t>(descs[i].N) * 4});
+        }
+        const q8_status st = clear_met_counters(ws, counters, data, stream);
         if (st != Q8_OK) return st;
     }
     if (n[kRouteGemv] > 0) {

@@ -237,10 +237,11 @@ typedef struct q8_linear_desc {
  *           is free first) and leaves zero; after a Q8_DEV_TIMEOUT zero the
  *           workspace again.  One workspace may serve later calls of other
  *           shapes (at the same address, in stream order): where the words
- *           a call counts with lie elsewhere than those of the previous call
- *           enqueued on that address (or on its first use), the library
- *           clears them first with one cudaMemsetAsync per range in the
- *           call's stream; repeated calls of the same shapes clear nothing.
+ *           a call counts with may hold an earlier call's partial sums or x
+ *           copies (or on the first use of an address), the library clears
+ *           them first with one cudaMemsetAsync per range in the call's
+ *           stream; M = 1 calls and repeated calls of the same shapes clear
+ *           nothing.
  * Each output equals, bit for bit, what q8_gemm_skinny returns for that matrix.
  * Outputs must not overlap each other or any input.
  */
