@@ -780,6 +780,23 @@ def profile_case(torch, q8, args):
         ws = q8.workspace(q8.q8_linear_batch_workspace_size(bd, M))
         for _ in range(args.warmup + 3):
             q8.q8_linear_batch(descs=bd, M=M, ws=ws)
+    elif args.profile == "chain":
+        # one module run (16 layers, 64 dependent matmuls, 127 launches) as
+        # q8_linear_chain at M = 1, `--warmup` + 3 times
+        ls = LayerSet(torch, q8)
+        nxt = {"qkv": q8.Q8_CHAIN_RMSNORM, "o_proj": q8.Q8_CHAIN_RMSNORM,
+               "gate_up": q8.Q8_CHAIN_SWIGLU_RMSNORM, "down": q8.Q8_CHAIN_RMSNORM}
+        steps = []
+        for layer in range(synth.LAYERS):
+            for (name, K, N) in synth.LAYER_MATRICES:
+                q, sc = ls.w[layer][name]
+                x = ls.x[(0, K)] if not steps else torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
+                steps.append([q, sc, x, torch.empty((1, N), dtype=torch.float32, device="cuda"), nxt[name]])
+        steps[-1][4] = q8.Q8_CHAIN_END
+        arr, _ = q8.make_chain([tuple(t) for t in steps])
+        ws = q8.workspace(q8.q8_linear_chain_workspace_size(arr, 1))
+        for _ in range(args.warmup + 3):
+            q8.q8_linear_chain(arr, 1, ws=ws)
     elif args.profile == "prefill":
         K, N = synth.SWEEP_SHAPES[0]
         M = synth.PREFILL_M
@@ -812,7 +829,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-chain", action="store_true",
                     help="launch the passes with q8_linear_batch instead of q8_linear_batch_chained")
-    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16", "oddk16"], default=None,
+    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16", "oddk16", "chain"], default=None,
                     help="run a few launches of one workload and exit (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

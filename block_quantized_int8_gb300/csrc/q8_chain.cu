@@ -27,7 +27,8 @@ namespace q8 {
 
 namespace {
 
-constexpr int kGlueThreads = 256;
+constexpr int kGlueThreads = 256;   // the general kernel (any K)
+constexpr int kFastThreads = 1024;  // the register kernel: K <= 8 * 1024
 
 struct GlueParams {
     const float *y;
@@ -70,6 +71,59 @@ __global__ void __launch_bounds__(kGlueThreads) glue_kernel(const __grid_constan
     uint16_t *xr = p.x + m * p.ldx;
     for (int k = threadIdx.x; k < p.K; k += kGlueThreads)
         xr[k] = __bfloat16_as_ushort(__float2bfloat16_rn(glue_value(yr, p.K, k, p.swiglu) * r));
+}
+
+// K <= G * 1024: thread t holds the values k = t + 1024 j (j < G) in
+// registers, loaded all at once (so their latencies overlap) and read from
+// y only once; its sum of squares in j order, then the warps' shuffle trees
+// and the 32 warp sums in warp order.
+template <int G>
+__global__ void __launch_bounds__(kFastThreads) glue_regs_kernel(const __grid_constant__ GlueParams p) {
+    pdl_launch_dependents();
+    pdl_wait_prior();
+    __shared__ float warp_ss[kFastThreads / 32];
+    const int m = blockIdx.x;
+    const float *yr = p.y + m * p.ldy;
+    float a[G], b[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        const int k = threadIdx.x + kFastThreads * j;
+        a[j] = k < p.K ? yr[k] : 0.f;
+        b[j] = (p.swiglu && k < p.K) ? yr[p.K + k] : 0.f;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        if (p.swiglu) a[j] = a[j] / (1.0f + expf(-a[j])) * b[j];
+        ss = fmaf(a[j], a[j], ss);
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < kFastThreads / 32; ++w) tot += warp_ss[w];
+    const float r = 1.0f / sqrtf(tot / static_cast<float>(p.K) + 1e-6f);
+    uint16_t *xr = p.x + m * p.ldx;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        const int k = threadIdx.x + kFastThreads * j;
+        if (k < p.K) xr[k] = __bfloat16_as_ushort(__float2bfloat16_rn(a[j] * r));
+    }
+}
+
+q8_status launch_glue(const GlueParams &g, int M, cudaStream_t stream) {
+    cudaError_t e;
+    if (g.K <= kFastThreads)
+        e = launch_kernel(glue_regs_kernel<1>, dim3(M), dim3(kFastThreads), 0, stream, true, g);
+    else if (g.K <= 2 * kFastThreads)
+        e = launch_kernel(glue_regs_kernel<2>, dim3(M), dim3(kFastThreads), 0, stream, true, g);
+    else if (g.K <= 4 * kFastThreads)
+        e = launch_kernel(glue_regs_kernel<4>, dim3(M), dim3(kFastThreads), 0, stream, true, g);
+    else if (g.K <= 8 * kFastThreads)
+        e = launch_kernel(glue_regs_kernel<8>, dim3(M), dim3(kFastThreads), 0, stream, true, g);
+    else
+        e = launch_kernel(glue_kernel, dim3(M), dim3(kGlueThreads), 0, stream, true, g);
+    return e == cudaSuccess ? Q8_OK : Q8_ERR_CUDA;
 }
 
 q8_linear_desc desc_of(const q8_chain_step &st) {
@@ -155,8 +209,8 @@ q8_status launch_chain(const q8_chain_step *steps, int count, int M, void *ws, s
         g.ldx = steps[i + 1].ldx;
         g.K = static_cast<int32_t>(steps[i + 1].K);
         g.swiglu = steps[i].next == Q8_CHAIN_SWIGLU_RMSNORM ? 1 : 0;
-        if (launch_kernel(glue_kernel, dim3(M), dim3(kGlueThreads), 0, stream, true, g) != cudaSuccess)
-            return Q8_ERR_CUDA;
+        st = launch_glue(g, M, stream);
+        if (st != Q8_OK) return st;
     }
     return Q8_OK;
 }

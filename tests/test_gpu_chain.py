@@ -116,3 +116,67 @@ def test_chain_one_step_equals_linear_batch(oracle):
         q8.q8_linear_batch([(q, s, x, y2)])
         torch.cuda.synchronize()
         assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+
+
+@pytest.mark.parametrize("M", [1, 8, 12, 32])
+def test_chain_off_the_256_grid(oracle, M):
+    """A chain whose K are not multiples of 256 (2080 and 4128, so the tile
+    kernel's partial last chunk, the pipeline or the GEMV serve the steps),
+    with a shape repeated later in the chain (the steps of one shape share a
+    workspace region).  Each step against the oracle on its own input."""
+    from block_quantized_int8_gb300 import q8
+    plan = [(2080, 4608, q8.Q8_CHAIN_RMSNORM), (2080, 8256, q8.Q8_CHAIN_SWIGLU_RMSNORM),
+            (4128, 2080, q8.Q8_CHAIN_RMSNORM), (2080, 4608, q8.Q8_CHAIN_RMSNORM),
+            (2080, 2080, q8.Q8_CHAIN_END)]
+    host, dev_steps = [], []
+    for i, (K, N, nxt) in enumerate(plan):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"cho{i}"))
+        host.append((qn, sn))
+        q, s = weights_dev(qn, sn)
+        x = x_dev(synth.activations(M, K, 0, f"chox{M}")) if i == 0 else \
+            torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        dev_steps.append((q, s, x, y, nxt))
+    steps, _ = q8.make_chain(dev_steps)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8.q8_linear_chain(steps, M, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for i, ((qn, sn), (q, s, x, y, nxt)) in enumerate(zip(host, dev_steps)):
+        xb = x.view(torch.int16).cpu().numpy().view(np.uint16)
+        yg = y.cpu().numpy()
+        y_ref, B = oracle.matmul(qn, sn, xb, threads=8)
+        check_tol(yg, y_ref, B, f"odd-K chain step {i} M={M}")
+        if i + 1 < len(dev_steps):
+            xn = dev_steps[i + 1][2].view(torch.int16).cpu().numpy().view(np.uint16)
+            want = oracle.chain_next(yg, xn.shape[1], swiglu=(nxt == q8.Q8_CHAIN_SWIGLU_RMSNORM))
+            assert ulp_diff(xn, want).max() <= 1, f"odd-K chain step {i} -> {i + 1}"
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_chain_normalisation_widths(oracle, M):
+    """Next inputs of 512 values (one per thread of the register kernel) and
+    of 12800 (beyond its 8192: the strided kernel), against the oracle."""
+    from block_quantized_int8_gb300 import q8
+    plan = [(1536, 512, q8.Q8_CHAIN_RMSNORM), (512, 12800, q8.Q8_CHAIN_RMSNORM), (12800, 1536, q8.Q8_CHAIN_END)]
+    host, dev_steps = [], []
+    for i, (K, N, nxt) in enumerate(plan):
+        qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"chw{i}"))
+        host.append((qn, sn))
+        q, s = weights_dev(qn, sn)
+        x = x_dev(synth.activations(M, K, 0, f"chwx{M}")) if i == 0 else \
+            torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        dev_steps.append((q, s, x, y, nxt))
+    steps, _ = q8.make_chain(dev_steps)
+    q8.q8_linear_chain(steps, M)
+    torch.cuda.synchronize()
+    for i, ((qn, sn), (q, s, x, y, nxt)) in enumerate(zip(host, dev_steps)):
+        xb = x.view(torch.int16).cpu().numpy().view(np.uint16)
+        yg = y.cpu().numpy()
+        y_ref, B = oracle.matmul(qn, sn, xb, threads=8)
+        check_tol(yg, y_ref, B, f"width chain step {i} M={M}")
+        if i + 1 < len(dev_steps):
+            xn = dev_steps[i + 1][2].view(torch.int16).cpu().numpy().view(np.uint16)
+            want = oracle.chain_next(yg, xn.shape[1], swiglu=False)
+            assert ulp_diff(xn, want).max() <= 1, f"width chain step {i} -> {i + 1}"
