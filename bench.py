@@ -645,6 +645,16 @@ def extra_rows(torch, q8, peak):
             "TFLOP/s": round(tf, 1), "frac": round(tf / tpk, 4), "us": round(t * 1e6, 2),
             "us_p10": round(spread_of[0][0] * 1e6, 2), "us_p90": round(spread_of[0][1] * 1e6, 2),
             "GB/s": round(matmul_bytes(N, K, M, 2) / t / 1e9, 1)}
+        # the same shape as W8A8 (int8 warp MMA in 32-row slices; fp32 out):
+        # int8 TOPS, and that rate against the measured bf16 peak
+        y8 = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws8 = q8.workspace(int(q8.lib().q8_gemm_w8a8_workspace_size(N, K, M)), dev)
+        t = timed([lambda q0=q0, s0=s0, x=x, y8=y8, ws8=ws8: q8.q8_gemm_w8a8(q0, s0, x, y=y8, ws=ws8)], reps=20)
+        tf = 2.0 * M * N * K / t / 1e12
+        rows[f"prefill_w8a8_M{M}_K{K}_N{N}"] = {
+            "TOPS": round(tf, 1), "frac_of_bf16_peak": round(tf / tpk, 4), "us": round(t * 1e6, 2),
+            "us_p10": round(spread_of[0][0] * 1e6, 2), "us_p90": round(spread_of[0][1] * 1e6, 2)}
+        del y8, ws8
     torch.cuda.empty_cache()
     return rows
 

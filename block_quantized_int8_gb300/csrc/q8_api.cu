@@ -2,6 +2,8 @@
 // CUDA call), device checks, and dispatch to the kernels.
 #include <mutex>
 
+#include <algorithm>
+
 #include "q8_internal.h"
 
 namespace q8 {
@@ -270,6 +272,86 @@ q8_status q8_gemm_skinny(const int8_t *q, const uint16_t *s, int64_t N, int64_t 
     d.ldx = ldx;
     d.ldy = ldy;
     return q8_linear_batch_ex(&d, 1, M, Q8_VARIANT_AUTO, ws, ws_bytes, dev_status, stream);
+}
+
+extern "C++" {
+namespace {
+
+// q8_gemm_w8a8's launches: the full 32-row slices of x in groups of at most
+// Q8_MAX_BATCH (one q8_linear_batch launch each, the slices as matrices that
+// share the weights), then the remaining rows.
+template <typename F>
+q8_status for_w8a8_launches(const q8_linear_desc &d, int32_t M, F &&f) {
+    q8_linear_desc descs[Q8_MAX_BATCH];
+    const int32_t full = M / Q8_SKINNY_MAX_M;
+    for (int32_t b = 0; b < full; b += Q8_MAX_BATCH) {
+        const int32_t cnt = std::min<int32_t>(Q8_MAX_BATCH, full - b);
+        for (int32_t j = 0; j < cnt; ++j) {
+            descs[j] = d;
+            descs[j].x = d.x + static_cast<int64_t>(b + j) * Q8_SKINNY_MAX_M * d.ldx;
+            descs[j].y = d.y + static_cast<int64_t>(b + j) * Q8_SKINNY_MAX_M * d.ldy;
+        }
+        const q8_status st = f(descs, cnt, Q8_SKINNY_MAX_M);
+        if (st != Q8_OK) return st;
+    }
+    const int32_t rem = M - full * Q8_SKINNY_MAX_M;
+    if (rem > 0) {
+        descs[0] = d;
+        descs[0].x = d.x + static_cast<int64_t>(full) * Q8_SKINNY_MAX_M * d.ldx;
+        descs[0].y = d.y + static_cast<int64_t>(full) * Q8_SKINNY_MAX_M * d.ldy;
+        return f(descs, 1, rem);
+    }
+    return Q8_OK;
+}
+
+q8_linear_desc w8a8_desc(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
+                         float *y, int64_t ldy) {
+    q8_linear_desc d;
+    d.q = q;
+    d.s = s;
+    d.x = x;
+    d.y = y;
+    d.N = N;
+    d.K = K;
+    d.ldx = ldx;
+    d.ldy = ldy;
+    return d;
+}
+
+}  // namespace
+}  // extern "C++"
+
+size_t q8_gemm_w8a8_workspace_size(int64_t N, int64_t K, int32_t M) {
+    if (N <= 0 || K <= 0 || K % 32 || M < 1) return 0;
+    const q8_linear_desc d = w8a8_desc(nullptr, nullptr, N, K, nullptr, K, nullptr, N);
+    size_t need = 0;
+    (void)for_w8a8_launches(d, M, [&](const q8_linear_desc *ds, int cnt, int m) {
+        need = std::max(need, w8a8_workspace(ds, cnt, m));
+        return Q8_OK;
+    });
+    return need;
+}
+
+q8_status q8_gemm_w8a8(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, int64_t ldx,
+                       int32_t M, float *y, int64_t ldy, void *ws, size_t ws_bytes, uint32_t *dev_status,
+                       q8_stream_t stream) {
+    if (M < 0) return Q8_ERR_SHAPE;
+    if (dev_status && !aligned(dev_status, 4)) return Q8_ERR_ALIGN;
+    const q8_linear_desc d = w8a8_desc(q, s, N, K, x, ldx, y, ldy);
+    q8_status st = check_desc(d, std::min<int32_t>(M, Q8_SKINNY_MAX_M));
+    if (st != Q8_OK) return st;
+    if (M > 1 && ldy < N) return Q8_ERR_SHAPE;
+    if (M == 0 || N == 0) return Q8_OK;
+    const size_t need = q8_gemm_w8a8_workspace_size(N, K, M);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return Q8_ERR_WORKSPACE;
+    if (need > 0 && !aligned(ws, 256)) return Q8_ERR_ALIGN;
+    const DeviceInfo *di;
+    st = check_arch(&di);
+    if (st != Q8_OK) return st;
+    return for_w8a8_launches(d, M, [&](const q8_linear_desc *ds, int cnt, int m) {
+        return launch_skinny(ds, cnt, m, Q8_VARIANT_W8A8, ws, ws_bytes, dev_status,
+                             reinterpret_cast<cudaStream_t>(stream), false);
+    });
 }
 
 q8_status q8_gemv(const int8_t *q, const uint16_t *s, int64_t N, int64_t K, const uint16_t *x, float *y,

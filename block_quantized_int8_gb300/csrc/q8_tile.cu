@@ -145,6 +145,8 @@ struct TParams {
     int32_t early_signal;  // the grid fills every CTA slot: signal dependents at start
     int32_t mode;          // TileMode: batch-invariant (bf16 operands from the caller's x, one
                            // class) or W8A8 (x quantized to Q8_0, integer block dots)
+    const uint8_t *w8_codes;   // W8A8: the codes of every distinct x, one after another ...
+    const uint8_t *w8_scales;  // ... and their scales in the same order (18 bytes per 288 of codes)
     int32_t cta_begin[kMaxGrid + 1];
     int16_t first_sid[kMaxGrid];  // split id of a CTA's first row block, -1 if whole
     int16_t last_sid[kMaxGrid];   // split id of a CTA's last row block, -1 if whole
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2) tile_kernel(const __grid_constant
         if (p.mode == kModeW8A8) {
             const TDesc &D = p.d[pos.d];
             const uint8_t *xq = reinterpret_cast<const uint8_t *>(D.xflag);
-            const uint8_t *xs = xq + static_cast<size_t>(D.KC) * MP * kW8Row;
+            const uint8_t *xs = p.w8_scales + (xq - p.w8_codes) / 16;
             bulk_g2s(dst, xq + static_cast<size_t>(pos.chunk) * MP * kW8Row, MP * kW8Row, &full[slot]);
             bulk_g2s(dst + kW8ScaleOff, xs + static_cast<size_t>(pos.chunk) * MP * kW8Blocks * 2, MP * kW8Blocks * 2,
                      &full[slot]);
@@ -946,6 +948,18 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     xp.count = 0;
     xp.M = M;
     size_t off = 0;
+    // W8A8: the binary32 blocks, the codes and the scales of every distinct x
+    // each in one array (x after x), so one quantizer launch serves them all
+    int64_t w8_rows = 0, w8_before = 0;
+    for (int i = 0; i < count && w8; ++i) {
+        bool seen = false;
+        for (int j = 0; j < i && !seen; ++j)
+            seen = descs[j].x == descs[i].x && descs[j].ldx == descs[i].ldx && descs[j].K == descs[i].K;
+        if (!seen) w8_rows += (descs[i].K + kChunk - 1) / kChunk * MP;
+    }
+    float *w8_xf = reinterpret_cast<float *>(xws);
+    int8_t *w8_q = w8 ? reinterpret_cast<int8_t *>(xws + up256(w8_rows * kW8Row * 4)) : nullptr;
+    uint16_t *w8_s = w8 ? reinterpret_cast<uint16_t *>(w8_q + w8_rows * kW8Row) : nullptr;
     for (int i = 0; i < count && (copy || w8); ++i) {
         const q8_linear_desc &d = descs[i];
         const size_t region = off;
@@ -959,8 +973,9 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         J.x = d.x;
         J.xo = reinterpret_cast<uint16_t *>(xws + region);
         J.flag = reinterpret_cast<uint32_t *>(xws + region + up256(static_cast<int64_t>(M) * KC * kChunk * 2));
-        J.xf = reinterpret_cast<float *>(xws + region);
-        J.xq = reinterpret_cast<int8_t *>(xws + region + up256(KC * MP * kW8Row * 4));
+        J.xf = w8_xf + w8_before * kW8Row;
+        J.xq = w8 ? w8_q + w8_before * kW8Row : nullptr;
+        if (w8) w8_before += KC * MP;
         J.ldx = d.ldx;
         J.K = KC * kChunk;
         J.kx = d.K;
@@ -1027,6 +1042,8 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
     p.count = count;
     p.M = M;
     p.mode = mode;
+    p.w8_codes = reinterpret_cast<const uint8_t *>(w8_q);
+    p.w8_scales = reinterpret_cast<const uint8_t *>(w8_s);
     bool ragged = false;
     for (int i = 0; i < count; ++i) ragged = ragged || !tile_k_whole_chunks(descs[i].K);
     if (items == 0) return Q8_OK;
@@ -1039,13 +1056,8 @@ q8_status launch_tile(const q8_linear_desc *descs, int count, int M, uint8_t *xw
         // scales land in the stage layout); the tile kernel follows in order
         w8a8_widen_kernel<<<chunks, kThreads, 0, stream>>>(xp, MP);
         if (cudaGetLastError() != cudaSuccess) return Q8_ERR_CUDA;
-        for (int j = 0; j < xp.count; ++j) {
-            const XJob &J = xp.j[j];
-            const int64_t rows = J.K / kChunk * MP;
-            const q8_status st = launch_quantize(J.xf, rows, kW8Row, J.xq, reinterpret_cast<uint16_t *>(J.xq + rows * kW8Row),
-                                                 dev_status, stream);
-            if (st != Q8_OK) return st;
-        }
+        const q8_status st = launch_quantize(w8_xf, w8_rows, kW8Row, w8_q, w8_s, dev_status, stream);
+        if (st != Q8_OK) return st;
     }
     const bool dep = copy || chained;
     const int msi = static_cast<int>(ms);

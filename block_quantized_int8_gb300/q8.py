@@ -38,7 +38,8 @@ EXPORTS = ("q8_quantize_rows", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch", "
            "q8_linear_batch_chained", "q8_workspace_size", "q8_linear_batch_workspace_size", "q8_linear_batch_workspace_size_ex", "q8_gemm", "q8_status_str",
            "q8_abi_version", "q8_gemm_skinny_noalloc", "q8_gemm_ex", "q8_gguf_to_planar",
            "q8_planar_to_gguf", "q8_quantize_rows_ex", "q8_selftest_wait_timeout",
-           "q8_stream_read", "q8_stream_read_out_words", "q8_linear_chain", "q8_linear_chain_workspace_size")
+           "q8_stream_read", "q8_stream_read_out_words", "q8_linear_chain", "q8_linear_chain_workspace_size",
+           "q8_gemm_w8a8", "q8_gemm_w8a8_workspace_size")
 Q8_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -94,6 +95,9 @@ def lib():
         L.q8_linear_chain.argtypes = [ctypes.POINTER(ChainStep), I32, I32, P, SZ, U32P, P]
         L.q8_linear_chain_workspace_size.argtypes = [ctypes.POINTER(ChainStep), I32, I32]
         L.q8_linear_chain_workspace_size.restype = SZ
+        L.q8_gemm_w8a8.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, P, SZ, U32P, P]
+        L.q8_gemm_w8a8_workspace_size.argtypes = [I64, I64, I32]
+        L.q8_gemm_w8a8_workspace_size.restype = SZ
         L.q8_gemm.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
         L.q8_gemm_ex.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, I32, I32, U32P, P]
         L.q8_gemm_skinny_noalloc.argtypes = [P, P, I64, I64, P, I64, I32, P, I64, U32P, P]
@@ -109,7 +113,7 @@ def lib():
         L.q8_abi_version.restype = I32
         for name in ("q8_quantize_rows", "q8_quantize_rows_ex", "q8_gemv", "q8_gemm_skinny", "q8_linear_batch",
                      "q8_linear_batch_ex", "q8_linear_batch_chained", "q8_gguf_to_planar",
-                     "q8_planar_to_gguf", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc", "q8_linear_chain"):
+                     "q8_planar_to_gguf", "q8_gemm", "q8_gemm_ex", "q8_gemm_skinny_noalloc", "q8_linear_chain", "q8_gemm_w8a8"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -330,6 +334,24 @@ def q8_linear_chain(steps, M, ws=None, dev_status=None, stream=None):
     nbytes = 0 if ws is None else ws.numel()
     st = lib().q8_linear_chain(steps, len(steps), M, _p(ws), nbytes, _p(dev_status), _stream(stream))
     _check(st, "q8_linear_chain")
+
+
+def q8_gemm_w8a8(q, s, x, y=None, ws=None, dev_status=None, stream=None):
+    """y[M, N] (fp32) = the W8A8 product of x[M, K] (bf16, rows quantized to
+    Q8_0) and dequant(q, s)^T, any M (q8_gemm_w8a8)."""
+    _cuda(q, "q", (torch.int8,), 2)
+    _cuda(x, "x", _B16, 2)
+    N, K = q.shape
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=q.device)
+    need = int(lib().q8_gemm_w8a8_workspace_size(N, K, M))
+    if ws is None and need:
+        ws = workspace(need, q.device)
+    st = lib().q8_gemm_w8a8(_p(q), _p(s), N, K, _p(x), x.stride(0), M, _p(y), y.stride(0), _p(ws),
+                            0 if ws is None else ws.numel(), _p(dev_status), _stream(stream))
+    _check(st, "q8_gemm_w8a8")
+    return y
 
 
 def q8_gemm(q, s, x, y=None, dev_status=None, stream=None, tile=0, splits=0):

@@ -396,6 +396,27 @@ q8_status q8_gemm_ex(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
                      uint32_t *dev_status, q8_stream_t stream);
 
 /*
+ * q8_gemm_w8a8 -- the W8A8 product (Q8_VARIANT_W8A8's arithmetic) for any
+ * M, e.g. a prefill of M = 512: each activation row is quantized to Q8_0 by
+ * the weights' rule, and y[m][n] (fp32) = sum over blocks of
+ * s_w[n][b] * s_x[m][b] * (exact int8 block dot).  Source: "MODEL-BASELINE-
+ * RESULTS" (fak), ACT 3 items 1 and 3 (weights and activations in Q8_0
+ * blocks, integer block dots).  x is cut into slices of 32 rows, run as
+ * the matrices of q8_linear_batch launches (up to Q8_MAX_BATCH slices each,
+ * sharing the weights, which the slices then read mostly from L2), with the
+ * int8 warp MMA (mma.sync m16n8k32.s8): the 5th-generation tensor cores'
+ * int8 kind is not accepted for sm_103a by this toolchain.  Accuracy as for
+ * the W8A8 variant.  Any K (a multiple of 32).
+ *   x: bf16 [M][ldx]; y: float [M][ldy] (ldy >= N when M > 1); alignment as
+ *   for q8_linear_batch.  ws: q8_gemm_w8a8_workspace_size(N, K, M) bytes,
+ *   256-byte aligned, zeroed once (per slice: the quantized activations).
+ */
+q8_status q8_gemm_w8a8(const int8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                       const uint16_t *x, int64_t ldx, int32_t M, float *y, int64_t ldy,
+                       void *ws, size_t ws_bytes, uint32_t *dev_status, q8_stream_t stream);
+size_t q8_gemm_w8a8_workspace_size(int64_t N, int64_t K, int32_t M);
+
+/*
  * q8_gemm_skinny_noalloc -- q8_gemm_skinny for callers that cannot allocate
  * device memory when they run the matmul (a fixed memory pool, a loop that
  * must not enter the allocator, a host that passes only inputs and outputs).

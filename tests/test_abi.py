@@ -180,6 +180,28 @@ def test_chain_validation(L):
     assert L.q8_linear_chain(bad, 2, 1, A, 1 << 20, None, None) == q8.Q8_ERR_ALIGN
 
 
+def test_gemm_w8a8_validation(L):
+    """q8_gemm_w8a8 (any M, W8A8 in 32-row slices) checks its arguments on the
+    host; its workspace covers the largest launch (a group of up to 64 full
+    slices, or the remaining rows)."""
+    from block_quantized_int8_gb300 import q8
+    f = L.q8_gemm_w8a8
+    ws = L.q8_gemm_w8a8_workspace_size
+    assert ws(8192, 1536, 512) > 0 and ws(8192, 1536, 512) % 256 == 0
+    assert ws(8192, 1536, 512) >= ws(8192, 1536, 32) and ws(8192, 1536, 100) >= ws(8192, 1536, 4)
+    # 16 slices in one launch hold 16 quantized copies of x; one slice holds one
+    assert ws(8192, 1536, 512) > 8 * ws(8192, 1536, 32) // 2
+    assert ws(8192, 1540, 512) == 0 and ws(0, 1536, 512) == 0 and ws(8192, 1536, 0) == 0
+    need = ws(1536, 1536, 64)
+    assert f(A, A, 1536, 1536, A, 1536, -1, A, 1536, A, need, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, A, 1536, 1540, A, 1540, 64, A, 1536, A, need, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, A, 1536, 1536, A + 2, 1536, 64, A, 1536, A, need, None, None) == q8.Q8_ERR_ALIGN
+    assert f(A, A, 1536, 1536, A, 1536, 64, A, 1000, A, need, None, None) == q8.Q8_ERR_SHAPE
+    assert f(A, A, 1536, 1536, A, 1536, 64, A, 1536, None, 0, None, None) == q8.Q8_ERR_WORKSPACE
+    assert f(A, A, 1536, 1536, A, 1536, 64, A, 1536, A + 16, need, None, None) == q8.Q8_ERR_ALIGN
+    assert f(A, A, 1536, 1536, A, 1536, 0, A, 1536, None, 0, None, None) == q8.Q8_OK
+
+
 def test_quantize_validation(L):
     from block_quantized_int8_gb300 import q8
     f = L.q8_quantize_rows
