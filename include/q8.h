@@ -67,7 +67,7 @@ typedef enum q8_status {
 #define Q8_MAX_BATCH 64      /* most descriptors per q8_linear_batch call */
 
 /* Kernel variants for the M <= 32 path (the _ex entry points). */
-#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: the warp-MMA pipeline (K = 1536, and K % 256 != 0 up to 4096), else TMA-fed warp-MMA tiles; M > 8: the tiles (K >= 256) */
+#define Q8_VARIANT_AUTO 0    /* M = 1: CUDA-core GEMV; M = 2..8: the warp-MMA pipeline (K = 1536, and K % 256 != 0 up to 4096), else TMA-fed warp-MMA tiles; M > 8: the tiles (K >= 256; smaller K the general kernel) */
 #define Q8_VARIANT_SIMT 1    /* CUDA-core FFMA: codes dequantised in registers, one FMA per weight per row */
 #define Q8_VARIANT_MMA  2    /* warp mma.sync bf16 on exact bf16 codes, block scale applied in fp32 */
 /* Batch-invariant: row m of Y is the same, bit for bit, for every M in
