@@ -1,5 +1,6 @@
-"""q8_gemm_w8a8: the W8A8 product for any M (a prefill of 512 rows, and M
-with a remainder of rows) against the oracle's W8A8 definition, and bit for
+"""q8_gemm_w8a8: the W8A8 product for any M (a prefill of 512 rows, M with a
+remainder of rows, and M = 2100: more slices than one launch takes) against
+the oracle's W8A8 definition, and bit for
 bit equal to the W8A8 variant of q8_linear_batch run on each 32-row slice
 (the slices are the matrices of its launches)."""
 import numpy as np
@@ -12,7 +13,8 @@ from helpers import check_tol, weights_dev, x_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("N,K,M", [(8192, 1536, 512), (1536, 4096, 512), (1000, 2080, 100), (300, 1536, 33)])
+@pytest.mark.parametrize("N,K,M", [(8192, 1536, 512), (1536, 4096, 512), (1000, 2080, 100), (300, 1536, 33),
+                                   (260, 1536, 2100)])
 def test_gemm_w8a8_against_oracle(oracle, N, K, M):
     from block_quantized_int8_gb300 import q8
     qn, sn, _ = oracle.quantize_rows(synth.weights(N, K, 0, f"gw{N}.{K}"))
