@@ -20,8 +20,11 @@ from helpers import TOL_ABS, TOL_REL, weights_dev, x_dev
 pytestmark = pytest.mark.gpu
 
 # shapes that split K (so the scratch is really used) plus one that does not;
-# (1536, 4000, 12) takes the general split-K kernel (K not a multiple of 256,
-# M > 8), whose tickets this entry point clears before each call
+# (1536, 4000, 12) takes the tile kernel with a partial last chunk (K not a
+# multiple of 256, M > 8), whose shared row blocks count on tickets in the
+# scratch.  (No automatic route reaches the general kernel's split-K any
+# more: K off the 256 grid goes to the tiles or the pipeline, and K < 256
+# is never split.)
 CASES = [(1536, 4096, 4), (1536, 4096, 32), (8192, 1536, 16), (300, 1536, 3), (4097, 1536, 1),
          (1536, 4000, 12)]
 
