@@ -807,6 +807,16 @@ def profile_case(torch, q8, args):
         ws = q8.workspace(q8.q8_linear_chain_workspace_size(arr, 1))
         for _ in range(args.warmup + 3):
             q8.q8_linear_chain(arr, 1, ws=ws)
+    elif args.profile == "w8a8":
+        # the W8A8 GEMM at the prefill shape: M = 512, K1536 -> N8192
+        K, N = synth.SWEEP_SHAPES[0]
+        M = synth.PREFILL_M
+        q0, s0 = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, f"pf{K}.{N}")).cuda())
+        x = torch.from_numpy(synth.activations(M, K, 0, f"pfx{K}").view(np.int16)).view(torch.bfloat16).cuda()
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        ws = q8.workspace(int(q8.lib().q8_gemm_w8a8_workspace_size(N, K, M)))
+        for _ in range(args.warmup + 3):
+            q8.q8_gemm_w8a8(q0, s0, x, y=y, ws=ws)
     elif args.profile == "prefill":
         K, N = synth.SWEEP_SHAPES[0]
         M = synth.PREFILL_M
@@ -839,7 +849,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-chain", action="store_true",
                     help="launch the passes with q8_linear_batch instead of q8_linear_batch_chained")
-    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16", "oddk16", "chain"], default=None,
+    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16", "oddk16", "chain", "w8a8"], default=None,
                     help="run a few launches of one workload and exit (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
