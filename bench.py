@@ -777,6 +777,18 @@ def profile_case(torch, q8, args):
         bd, _ = q8.make_descs([(c[0], c[1], x, y) for c, y in zip(cps, ys)])
         for _ in range(args.warmup + 3):
             q8.q8_linear_batch(descs=bd, M=M)
+    elif args.profile == "tile32":
+        # M=32 over 32 distinct copies of the K4096 -> N1536 matrix in one launch
+        K, N = synth.SWEEP_SHAPES[1]
+        M = 32
+        q0, s0 = q8.q8_quantize_rows(torch.from_numpy(synth.weights(N, K, 0, f"sweep_K{K}_N{N}")).cuda())
+        x = torch.from_numpy(synth.activations(M, K, 0, "tile32.x").view(np.int16)).view(torch.bfloat16).cuda()
+        cps = [(q0.clone(), s0.clone()) for _ in range(32)]
+        ys = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in cps]
+        bd, _ = q8.make_descs([(c[0], c[1], x, y) for c, y in zip(cps, ys)])
+        ws = q8.workspace(q8.q8_linear_batch_workspace_size(bd, M))
+        for _ in range(args.warmup + 3):
+            q8.q8_linear_batch(descs=bd, M=M, ws=ws)
     elif args.profile == "oddk16":
         # M=16 over 32 distinct copies of the K2080 -> N4608 matrix (K not a
         # multiple of 256) in one launch
@@ -849,7 +861,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-chain", action="store_true",
                     help="launch the passes with q8_linear_batch instead of q8_linear_batch_chained")
-    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16", "oddk16", "chain", "w8a8"], default=None,
+    ap.add_argument("--profile", choices=["layerset", "vocab", "prefill", "sweep8", "tile16", "oddk16", "chain", "w8a8", "tile32"], default=None,
                     help="run a few launches of one workload and exit (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
