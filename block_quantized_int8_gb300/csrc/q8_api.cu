@@ -323,7 +323,11 @@ q8_linear_desc w8a8_desc(const int8_t *q, const uint16_t *s, int64_t N, int64_t 
 
 size_t q8_gemm_w8a8_workspace_size(int64_t N, int64_t K, int32_t M) {
     if (N <= 0 || K <= 0 || K % 32 || M < 1) return 0;
-    const q8_linear_desc d = w8a8_desc(nullptr, nullptr, N, K, nullptr, K, nullptr, N);
+    // placeholder addresses: only the slices' x must differ from one another
+    const uintptr_t base = uintptr_t(1) << 40;
+    const q8_linear_desc d = w8a8_desc(reinterpret_cast<const int8_t *>(base), reinterpret_cast<const uint16_t *>(base),
+                                       N, K, reinterpret_cast<const uint16_t *>(base), K,
+                                       reinterpret_cast<float *>(base), N);
     size_t need = 0;
     (void)for_w8a8_launches(d, M, [&](const q8_linear_desc *ds, int cnt, int m) {
         need = std::max(need, w8a8_workspace(ds, cnt, m));
